@@ -1,0 +1,610 @@
+// C ABI of liblstmstack.so: error reporting, the host weight packer, the
+// stack object (create / forward / destroy) and the step-level entry points.
+//
+// The stack follows the plan/enqueue split of the speakrs 0.6.0 pages
+// (lstmproj.rs `Oxide::with_recurrence` packs and uploads the four layers and
+// allocates the gate buffer once; `Oxide::enqueue` checks lengths and runs,
+// per layer, the projection and then both directions' recurrences, the
+// reverse one on a side stream joined back before the next layer).  What
+// differs: the projection runs once per layer for both directions (N = 1024),
+// the layers ping-pong between two scratch buffers instead of overwriting the
+// output in place, and there is no exchange buffer to clear (the recurrence
+// exchanges h through distributed shared memory).
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace lstm {
+
+namespace {
+thread_local std::string g_last_error;
+__device__ unsigned g_fault_word;
+}  // namespace
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int cuda_status(cudaError_t err, const char *what)
+{
+    if (err == cudaSuccess)
+        return LSTM_OK;
+    return fail(LSTM_E_CUDA, "%s: %s (%s)", what, cudaGetErrorString(err), cudaGetErrorName(err));
+}
+
+unsigned *fault_word()
+{
+    // one address per device; resolved with that device current
+    static std::mutex mu;
+    static unsigned *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess)
+            return nullptr;
+        addr[dev] = static_cast<unsigned *>(p);
+    }
+    return addr[dev];
+}
+
+namespace {
+
+// Round-to-nearest (ties away from zero) to TF32: keep 10 mantissa bits.
+float tf32_round(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u)  // inf / nan: unchanged
+        return x;
+    u = (u + 0x1000u) & 0xffffe000u;
+    float r;
+    memcpy(&r, &u, 4);
+    return r;
+}
+
+// Makes `device` current for the scope and restores the previous one.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int device)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess)
+            prev = -1;
+        ok = (prev == device) || cudaSetDevice(device) == cudaSuccess;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0)
+            cudaSetDevice(prev);
+    }
+};
+
+int check_device(int device)
+{
+    cudaDeviceProp prop;
+    int st = cuda_status(cudaGetDeviceProperties(&prop, device), "device properties");
+    if (st != LSTM_OK)
+        return st;
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(LSTM_E_DEVICE, "device %d is compute capability %d.%d; the kernels are built for 10.3 (sm_103a)",
+                    device, prop.major, prop.minor);
+    int cluster = 0;
+    st = cuda_status(cudaDeviceGetAttribute(&cluster, cudaDevAttrClusterLaunch, device),
+                     "cluster-launch attribute");
+    if (st != LSTM_OK)
+        return st;
+    if (!cluster)
+        return fail(LSTM_E_DEVICE, "device %d does not support cluster launch", device);
+    return LSTM_OK;
+}
+
+int prepare_device(int device)
+{
+    static std::mutex mu;
+    static bool done[64] = {};
+    if (device < 0 || device >= 64)
+        return fail(LSTM_E_INVALID, "device %d out of range", device);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[device])
+        return LSTM_OK;
+    int st = check_device(device);
+    if (st == LSTM_OK)
+        st = projection_prepare(device);
+    if (st == LSTM_OK)
+        st = recurrence_prepare(device);
+    if (st == LSTM_OK)
+        done[device] = true;
+    return st;
+}
+
+int check_aligned(const void *p, const char *what)
+{
+    if ((reinterpret_cast<uintptr_t>(p) & 15) != 0)
+        return fail(LSTM_E_INVALID, "%s (%p) is not 16-byte aligned", what, p);
+    return LSTM_OK;
+}
+
+int pointer_device(const void *p, int *device)
+{
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(LSTM_E_INVALID, "pointer %p is not known to CUDA", p);
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(LSTM_E_INVALID, "pointer %p is not device memory", p);
+    *device = attr.device;
+    return LSTM_OK;
+}
+
+constexpr int kLayers = LSTM_STACK_LAYERS;
+constexpr int kPhaseEvents = 3 * 2 * kLayers;  // (projection, fwd, rev) x (start, end) x layers
+
+}  // namespace
+}  // namespace lstm
+
+using namespace lstm;
+
+struct lstm_stack {
+    int device = 0;
+    int max_batch = 0;
+    int max_steps = 0;
+    long max_rows = 0;
+    int in_width[kLayers] = {};
+    int kp[kLayers] = {};
+    float *weights = nullptr;  // one allocation: all packed planes
+    float *wp_hi[kLayers] = {};
+    float *wp_lo[kLayers] = {};
+    float *rp[kLayers] = {};
+    float *bias[kLayers] = {};
+    float *gates = nullptr;     // [max_rows][1024]
+    float *ping[2] = {};        // [max_rows][256] each
+    float *x_stage = nullptr;   // [max_rows][60]   (forward_host)
+    float *y_stage = nullptr;   // [max_rows][256]  (forward_host)
+    CUtensorMap map_whi[kLayers];
+    CUtensorMap map_wlo[kLayers];
+    CUtensorMap map_ping[2];
+    CUtensorMap map_x;
+    const float *map_x_base = nullptr;
+    long map_x_rows = -1;
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork[kLayers] = {};
+    cudaEvent_t join[kLayers] = {};
+    bool timing = false;
+    bool timed_once = false;
+    cudaEvent_t phase[kPhaseEvents] = {};
+    unsigned *fault = nullptr;
+};
+
+extern "C" const char *lstm_stack_last_error(void)
+{
+    return g_last_error.c_str();
+}
+
+extern "C" int lstm_pack_layer(const float *w, const float *r, const float *b, int in_width,
+                               int kp, float *wp_hi, float *wp_lo, float *rp, float *bias)
+{
+    if (!w || !r || !b || !wp_hi || !wp_lo || !rp || !bias)
+        return fail(LSTM_E_INVALID, "lstm_pack_layer: null pointer");
+    if (in_width <= 0 || kp < in_width || kp % 32 != 0)
+        return fail(LSTM_E_INVALID, "lstm_pack_layer: in_width %d, kp %d (need 0 < in_width <= kp, kp %% 32 == 0)",
+                    in_width, kp);
+    const int H = kHidden;
+    for (int d = 0; d < 2; ++d) {
+        for (int u = 0; u < H; ++u) {
+            for (int k = 0; k < 4; ++k) {
+                const long src_row = static_cast<long>(d) * 4 * H + k * H + u;  // gate block k
+                const long dst_row = static_cast<long>(d) * 4 * H + 4 * u + k;  // interleaved
+                for (int j = 0; j < kp; ++j) {
+                    const float v = j < in_width ? w[src_row * in_width + j] : 0.0f;
+                    const float hi = tf32_round(v);
+                    wp_hi[dst_row * kp + j] = hi;
+                    wp_lo[dst_row * kp + j] = tf32_round(v - hi);
+                }
+                for (int j = 0; j < H; ++j)
+                    rp[dst_row * H + j] = r[src_row * H + j];
+                const float *bd = b + static_cast<long>(d) * 8 * H;
+                bias[static_cast<long>(d) * 4 * H + 4 * u + k] = bd[k * H + u] + bd[4 * H + k * H + u];
+            }
+        }
+    }
+    return LSTM_OK;
+}
+
+extern "C" void lstm_stack_destroy(lstm_stack *s)
+{
+    if (!s)
+        return;
+    DeviceGuard guard(s->device);
+    cudaDeviceSynchronize();
+    cudaFree(s->weights);
+    cudaFree(s->gates);
+    cudaFree(s->ping[0]);
+    cudaFree(s->ping[1]);
+    cudaFree(s->x_stage);
+    cudaFree(s->y_stage);
+    for (int l = 0; l < kLayers; ++l) {
+        if (s->fork[l])
+            cudaEventDestroy(s->fork[l]);
+        if (s->join[l])
+            cudaEventDestroy(s->join[l]);
+    }
+    for (int i = 0; i < kPhaseEvents; ++i)
+        if (s->phase[i])
+            cudaEventDestroy(s->phase[i]);
+    if (s->side)
+        cudaStreamDestroy(s->side);
+    delete s;
+}
+
+extern "C" int lstm_stack_create(const lstm_stack_weights *weights, int max_batch, int max_steps,
+                                 int device, lstm_stack **out)
+{
+    if (!out)
+        return fail(LSTM_E_INVALID, "lstm_stack_create: null output pointer");
+    *out = nullptr;
+    if (!weights)
+        return fail(LSTM_E_INVALID, "lstm_stack_create: null weights");
+    for (int l = 0; l < kLayers; ++l)
+        if (!weights->w[l] || !weights->r[l] || !weights->b[l])
+            return fail(LSTM_E_INVALID, "lstm_stack_create: layer %d has a null weight pointer", l);
+    if (max_batch <= 0 || max_steps <= 0)
+        return fail(LSTM_E_INVALID, "lstm_stack_create: max_batch %d, max_steps %d", max_batch,
+                    max_steps);
+    const long max_rows = static_cast<long>(max_batch) * max_steps;
+    if (max_rows > 65535L * 128 || max_rows * kGateColumns > 0x7fffffffL * 4)
+        return fail(LSTM_E_OVERFLOW, "lstm_stack_create: %ld rows exceed the kernels' indexing",
+                    max_rows);
+    int st = prepare_device(device);
+    if (st != LSTM_OK)
+        return st;
+    DeviceGuard guard(device);
+    if (!guard.ok)
+        return fail(LSTM_E_CUDA, "cannot make device %d current", device);
+
+    lstm_stack *s = new (std::nothrow) lstm_stack();
+    if (!s)
+        return fail(LSTM_E_ALLOC, "lstm_stack_create: host allocation failed");
+    s->device = device;
+    s->max_batch = max_batch;
+    s->max_steps = max_steps;
+    s->max_rows = max_rows;
+    s->fault = fault_word();
+    if (!s->fault) {
+        lstm_stack_destroy(s);
+        return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
+    }
+
+    // pack on the host, then one upload
+    long offs[kLayers][4];
+    long total = 0;
+    for (int l = 0; l < kLayers; ++l) {
+        s->in_width[l] = l == 0 ? kFeatures : kOutput;
+        s->kp[l] = (s->in_width[l] + 31) / 32 * 32;
+        const long wsz = static_cast<long>(kGateColumns) * s->kp[l];
+        offs[l][0] = total;  total += wsz;             // wp_hi
+        offs[l][1] = total;  total += wsz;             // wp_lo
+        offs[l][2] = total;  total += 2L * kGates * kHidden;  // rp
+        offs[l][3] = total;  total += 2L * kGates;            // bias
+        total = (total + 63) / 64 * 64;  // keep every plane 256-byte aligned
+    }
+    float *host = static_cast<float *>(calloc(total, sizeof(float)));
+    if (!host) {
+        lstm_stack_destroy(s);
+        return fail(LSTM_E_ALLOC, "lstm_stack_create: host staging allocation failed");
+    }
+    for (int l = 0; l < kLayers; ++l) {
+        st = lstm_pack_layer(weights->w[l], weights->r[l], weights->b[l], s->in_width[l], s->kp[l],
+                             host + offs[l][0], host + offs[l][1], host + offs[l][2],
+                             host + offs[l][3]);
+        if (st != LSTM_OK) {
+            free(host);
+            lstm_stack_destroy(s);
+            return st;
+        }
+    }
+    auto alloc = [&](float **p, long floats, const char *what) -> int {
+        cudaError_t e = cudaMalloc(reinterpret_cast<void **>(p), floats * sizeof(float));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(LSTM_E_ALLOC, "cudaMalloc of %s (%ld bytes): %s", what,
+                        floats * static_cast<long>(sizeof(float)), cudaGetErrorString(e));
+        }
+        return LSTM_OK;
+    };
+    st = alloc(&s->weights, total, "packed weights");
+    if (st == LSTM_OK)
+        st = cuda_status(cudaMemcpy(s->weights, host, total * sizeof(float), cudaMemcpyHostToDevice),
+                         "weight upload");
+    free(host);
+    if (st == LSTM_OK) st = alloc(&s->gates, max_rows * kGateColumns, "gate buffer");
+    if (st == LSTM_OK) st = alloc(&s->ping[0], max_rows * kOutput, "layer buffer 0");
+    if (st == LSTM_OK) st = alloc(&s->ping[1], max_rows * kOutput, "layer buffer 1");
+    if (st == LSTM_OK) st = alloc(&s->x_stage, max_rows * kFeatures, "input staging");
+    if (st == LSTM_OK) st = alloc(&s->y_stage, max_rows * kOutput, "output staging");
+    if (st != LSTM_OK) {
+        lstm_stack_destroy(s);
+        return st;
+    }
+    for (int l = 0; l < kLayers && st == LSTM_OK; ++l) {
+        s->wp_hi[l] = s->weights + offs[l][0];
+        s->wp_lo[l] = s->weights + offs[l][1];
+        s->rp[l] = s->weights + offs[l][2];
+        s->bias[l] = s->weights + offs[l][3];
+        st = encode_matrix_map(&s->map_whi[l], s->wp_hi[l], kGateColumns, s->kp[l], 256);
+        if (st == LSTM_OK)
+            st = encode_matrix_map(&s->map_wlo[l], s->wp_lo[l], kGateColumns, s->kp[l], 256);
+    }
+    for (int i = 0; i < 2 && st == LSTM_OK; ++i)
+        st = encode_matrix_map(&s->map_ping[i], s->ping[i], max_rows, kOutput, 128);
+    if (st == LSTM_OK)
+        st = cuda_status(cudaStreamCreateWithFlags(&s->side, cudaStreamNonBlocking), "side stream");
+    for (int l = 0; l < kLayers && st == LSTM_OK; ++l) {
+        st = cuda_status(cudaEventCreateWithFlags(&s->fork[l], cudaEventDisableTiming), "event");
+        if (st == LSTM_OK)
+            st = cuda_status(cudaEventCreateWithFlags(&s->join[l], cudaEventDisableTiming), "event");
+    }
+    for (int i = 0; i < kPhaseEvents && st == LSTM_OK; ++i)
+        st = cuda_status(cudaEventCreate(&s->phase[i]), "phase event");
+    if (st == LSTM_OK)
+        st = cuda_status(cudaDeviceSynchronize(), "create");
+    if (st != LSTM_OK) {
+        lstm_stack_destroy(s);
+        return st;
+    }
+    *out = s;
+    return LSTM_OK;
+}
+
+namespace {
+
+int check_forward_args(lstm_stack *s, const void *x, size_t x_len, const void *y, size_t y_len,
+                       int batch, int steps)
+{
+    if (!s || !x || !y)
+        return fail(LSTM_E_INVALID, "forward: null pointer");
+    if (batch <= 0 || steps <= 0)
+        return fail(LSTM_E_INVALID, "forward: batch %d, steps %d must be positive", batch, steps);
+    if (batch > s->max_batch || steps > s->max_steps)
+        return fail(LSTM_E_INVALID, "forward: batch %d x steps %d exceeds the created %d x %d",
+                    batch, steps, s->max_batch, s->max_steps);
+    const size_t rows = static_cast<size_t>(batch) * steps;
+    if (x_len != rows * kFeatures)
+        return fail(LSTM_E_LENGTH, "forward input: expected %zu floats, got %zu", rows * kFeatures,
+                    x_len);
+    if (y_len != rows * kOutput)
+        return fail(LSTM_E_LENGTH, "forward output: expected %zu floats, got %zu", rows * kOutput,
+                    y_len);
+    return LSTM_OK;
+}
+
+int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps,
+                   cudaStream_t stream)
+{
+    const long rows = static_cast<long>(batch) * steps;
+    int st;
+    if (x != s->map_x_base || rows != s->map_x_rows) {
+        st = encode_matrix_map(&s->map_x, x, rows, kFeatures, 128);
+        if (st != LSTM_OK)
+            return st;
+        s->map_x_base = x;
+        s->map_x_rows = rows;
+    }
+    auto ev = [&](int layer, int part, int end) { return s->phase[(layer * 3 + part) * 2 + end]; };
+    for (int l = 0; l < kLayers; ++l) {
+        const CUtensorMap &src = l == 0 ? s->map_x : s->map_ping[(l - 1) & 1];
+        float *dst = l == kLayers - 1 ? y : s->ping[l & 1];
+        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 0, 0), stream), "event")))
+            return st;
+        st = launch_projection(src, s->map_whi[l], s->map_wlo[l], s->gates, static_cast<int>(rows),
+                               s->kp[l], s->fault, stream);
+        if (st != LSTM_OK)
+            return st;
+        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 0, 1), stream), "event")))
+            return st;
+        if ((st = cuda_status(cudaEventRecord(s->fork[l], stream), "fork record")) ||
+            (st = cuda_status(cudaStreamWaitEvent(s->side, s->fork[l], 0), "fork wait")))
+            return st;
+        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 1, 0), stream), "event")))
+            return st;
+        st = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps, 0, stream);
+        if (st != LSTM_OK)
+            return st;
+        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 1, 1), stream), "event")))
+            return st;
+        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 2, 0), s->side), "event")))
+            return st;
+        st = launch_recurrence(s->gates, s->rp[l] + kGates * kHidden, s->bias[l] + kGates, dst,
+                               batch, steps, 1, s->side);
+        if (st != LSTM_OK)
+            return st;
+        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 2, 1), s->side), "event")))
+            return st;
+        if ((st = cuda_status(cudaEventRecord(s->join[l], s->side), "join record")) ||
+            (st = cuda_status(cudaStreamWaitEvent(stream, s->join[l], 0), "join wait")))
+            return st;
+    }
+    if (s->timing)
+        s->timed_once = true;
+    return LSTM_OK;
+}
+
+}  // namespace
+
+extern "C" int lstm_stack_forward(lstm_stack *s, const float *x, size_t x_len, float *y,
+                                  size_t y_len, int batch, int steps, void *stream)
+{
+    int st = check_forward_args(s, x, x_len, y, y_len, batch, steps);
+    if (st != LSTM_OK)
+        return st;
+    if ((st = check_aligned(x, "forward input")) != LSTM_OK)
+        return st;
+    if ((st = check_aligned(y, "forward output")) != LSTM_OK)
+        return st;
+    DeviceGuard guard(s->device);
+    if (!guard.ok)
+        return fail(LSTM_E_CUDA, "cannot make device %d current", s->device);
+    int dx = -1, dy = -1;
+    if ((st = pointer_device(x, &dx)) != LSTM_OK || (st = pointer_device(y, &dy)) != LSTM_OK)
+        return st;
+    if (dx != s->device || dy != s->device)
+        return fail(LSTM_E_INVALID, "forward: buffers on devices %d/%d, stack on device %d", dx, dy,
+                    s->device);
+    return forward_device(s, x, y, batch, steps, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_t x_len,
+                                       float *y_host, size_t y_len, int batch, int steps,
+                                       void *stream)
+{
+    int st = check_forward_args(s, x_host, x_len, y_host, y_len, batch, steps);
+    if (st != LSTM_OK)
+        return st;
+    DeviceGuard guard(s->device);
+    if (!guard.ok)
+        return fail(LSTM_E_CUDA, "cannot make device %d current", s->device);
+    cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+    if ((st = cuda_status(cudaMemcpyAsync(s->x_stage, x_host, x_len * sizeof(float),
+                                          cudaMemcpyHostToDevice, st_),
+                          "input copy")))
+        return st;
+    if ((st = forward_device(s, s->x_stage, s->y_stage, batch, steps, st_)))
+        return st;
+    if ((st = cuda_status(cudaMemcpyAsync(y_host, s->y_stage, y_len * sizeof(float),
+                                          cudaMemcpyDeviceToHost, st_),
+                          "output copy")))
+        return st;
+    return cuda_status(cudaStreamSynchronize(st_), "forward_host synchronize");
+}
+
+extern "C" int lstm_stack_enable_phase_timing(lstm_stack *s, int enable)
+{
+    if (!s)
+        return fail(LSTM_E_INVALID, "enable_phase_timing: null stack");
+    s->timing = enable != 0;
+    s->timed_once = false;
+    return LSTM_OK;
+}
+
+extern "C" int lstm_stack_phase_times(lstm_stack *s, float *ms)
+{
+    if (!s || !ms)
+        return fail(LSTM_E_INVALID, "phase_times: null pointer");
+    if (!s->timed_once)
+        return fail(LSTM_E_INVALID, "phase_times: no timed forward since timing was enabled");
+    DeviceGuard guard(s->device);
+    for (int i = 0; i < 3 * kLayers; ++i) {
+        int st = cuda_status(cudaEventSynchronize(s->phase[2 * i + 1]), "phase event sync");
+        if (st == LSTM_OK)
+            st = cuda_status(cudaEventElapsedTime(&ms[i], s->phase[2 * i], s->phase[2 * i + 1]),
+                             "phase elapsed");
+        if (st != LSTM_OK)
+            return st;
+    }
+    return LSTM_OK;
+}
+
+extern "C" int lstm_projection(const float *x, int rows, int in_width, const float *wp_hi,
+                               const float *wp_lo, int kp, float *g, void *stream)
+{
+    if (!x || !wp_hi || !wp_lo || !g)
+        return fail(LSTM_E_INVALID, "lstm_projection: null pointer");
+    if (rows <= 0 || in_width <= 0 || in_width > kp || kp % 32 != 0)
+        return fail(LSTM_E_INVALID, "lstm_projection: rows %d, in_width %d, kp %d", rows, in_width,
+                    kp);
+    int st;
+    if ((st = check_aligned(x, "projection input")) || (st = check_aligned(wp_hi, "wp_hi")) ||
+        (st = check_aligned(wp_lo, "wp_lo")) || (st = check_aligned(g, "projection output")))
+        return st;
+    int dev = 0;
+    if ((st = pointer_device(x, &dev)))
+        return st;
+    if ((st = prepare_device(dev)))
+        return st;
+    DeviceGuard guard(dev);
+    unsigned *fault = fault_word();
+    if (!fault)
+        return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
+    CUtensorMap xm, hm, lm;
+    if ((st = encode_matrix_map(&xm, x, rows, in_width, 128)) ||
+        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, 256)) ||
+        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, 256)))
+        return st;
+    return launch_projection(xm, hm, lm, g, rows, kp, fault, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+int recurrence_args(const float *g, const float *rp, const float *bias, float *y, int batch,
+                    int steps, int direction, int *dev)
+{
+    if (!g || !rp || !bias || !y)
+        return fail(LSTM_E_INVALID, "lstm_recurrence: null pointer");
+    if (batch <= 0 || steps <= 0)
+        return fail(LSTM_E_INVALID, "lstm_recurrence: batch %d, steps %d", batch, steps);
+    if (direction != 0 && direction != 1)
+        return fail(LSTM_E_INVALID, "lstm_recurrence: direction %d (0 forward, 1 reverse)", direction);
+    if (static_cast<long>(batch) * steps > 65535L * 128)
+        return fail(LSTM_E_OVERFLOW, "lstm_recurrence: %d x %d rows exceed %ld", batch, steps,
+                    65535L * 128);
+    int st;
+    if ((st = check_aligned(rp, "rp")) || (st = pointer_device(g, dev)))
+        return st;
+    return prepare_device(*dev);
+}
+}  // namespace
+
+extern "C" int lstm_recurrence(const float *g, const float *rp, const float *bias, float *y,
+                               int batch, int steps, int direction, void *stream)
+{
+    int dev = 0;
+    int st = recurrence_args(g, rp, bias, y, batch, steps, direction, &dev);
+    if (st != LSTM_OK)
+        return st;
+    DeviceGuard guard(dev);
+    return launch_recurrence(g, rp, bias, y, batch, steps, direction,
+                             static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
+                                       float *y, int batch, int steps, int direction,
+                                       int cluster_size, int windows_per_lane, void *stream)
+{
+    int dev = 0;
+    int st = recurrence_args(g, rp, bias, y, batch, steps, direction, &dev);
+    if (st != LSTM_OK)
+        return st;
+    DeviceGuard guard(dev);
+    return launch_recurrence_variant(g, rp, bias, y, batch, steps, direction, cluster_size,
+                                     windows_per_lane, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int lstm_fault_status(unsigned int *fault)
+{
+    if (!fault)
+        return fail(LSTM_E_INVALID, "lstm_fault_status: null pointer");
+    int st = cuda_status(cudaDeviceSynchronize(), "fault status synchronize");
+    if (st != LSTM_OK)
+        return st;
+    unsigned zero = 0;
+    if ((st = cuda_status(cudaMemcpyFromSymbol(fault, g_fault_word, sizeof(unsigned)),
+                          "fault word read")))
+        return st;
+    return cuda_status(cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(unsigned)), "fault word clear");
+}

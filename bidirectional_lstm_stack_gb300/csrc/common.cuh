@@ -1,0 +1,254 @@
+// Internal helpers shared by the library's translation units: error
+// reporting across the C ABI, and thin inline-PTX wrappers for the sm_103a
+// features the kernels use (mbarrier, TMA bulk tensor copies, tcgen05 /
+// tensor memory, thread-block clusters and distributed shared memory).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lstm_stack.h"
+
+namespace lstm {
+
+constexpr int kHidden = LSTM_STACK_HIDDEN;          // 128
+constexpr int kGates = LSTM_STACK_GATES;            // 512 per direction
+constexpr int kGateColumns = LSTM_STACK_GATE_COLUMNS; // 1024, both directions
+constexpr int kFeatures = LSTM_STACK_FEATURES;      // 60
+constexpr int kOutput = LSTM_STACK_OUTPUT;          // 256
+
+// Records a message for lstm_stack_last_error() and returns `code`.
+int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+// Maps a CUDA error to LSTM_E_CUDA with its string; LSTM_OK on success.
+int cuda_status(cudaError_t err, const char *what);
+
+// Fault bits a kernel sets in the library's device fault word when one of
+// its bounded waits runs out.
+enum : unsigned {
+    kFaultProducer = 1u << 0,
+    kFaultConverter = 1u << 1,
+    kFaultMma = 1u << 2,
+    kFaultEpilogue = 1u << 3,
+    kFaultDrain = 1u << 4,
+};
+
+// The device fault word of the current device (a __device__ variable;
+// resolved per device on first use).
+unsigned *fault_word();
+
+// ---- projection (projection.cu) ------------------------------------------
+// Encodes the tensor map of a row-major fp32 matrix [rows][cols] read in
+// boxes of 32 columns x box_rows rows with the 128-byte swizzle.
+int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols,
+                      int box_rows);
+// G[rows][1024] = X . Wp^T in 3xTF32; the maps come from encode_matrix_map
+// (X: box_rows 128; Wp planes: box_rows 256).
+int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
+                      const CUtensorMap &wlo_map, float *g, int rows, int kp,
+                      unsigned *fault, cudaStream_t stream);
+int projection_prepare(int device);
+
+// ---- recurrence (recurrence.cu) ------------------------------------------
+int launch_recurrence(const float *g, const float *rp, const float *bias,
+                      float *y, int batch, int steps, int direction,
+                      cudaStream_t stream);
+int launch_recurrence_variant(const float *g, const float *rp, const float *bias,
+                              float *y, int batch, int steps, int direction,
+                              int cluster, int nw, cudaStream_t stream);
+int recurrence_prepare(int device);
+
+} // namespace lstm
+
+// ---------------------------------------------------------------------------
+// Device-side PTX wrappers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+namespace lstm {
+namespace ptx {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ----
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with `parity` to complete, for at most `limit_ns`
+// nanoseconds, or until *abort becomes non-zero.  Returns false (after
+// setting `code` in *fault and *abort) when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort, unsigned *fault,
+                                                  unsigned code, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t start = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (globaltimer() - start > limit_ns) {
+            atomicOr(fault, code);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ---- TMA ----
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- tcgen05 / tensor memory ----
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::tf32, one CTA.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+// Arrives once on `bar` when every tcgen05 operation this thread issued
+// before has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns: thread (lane) gets its lane's row.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                 "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, "
+                 "%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+                   "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),
+                   "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- clusters / distributed shared memory ----
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+} // namespace ptx
+} // namespace lstm
+#endif

@@ -1,0 +1,327 @@
+// One direction's recurrence over one LSTM layer (the persistent kernel the
+// speakrs 0.6.0 pages launch per direction, lstmproj.rs module docs and
+// `recur` / `launch`):
+//     z_t = G[b, t, d*512 : d*512+512] + bias_d + Rp_d . h_prev
+//     i = s(z[4u]), f = s(z[4u+1]), g = tanh(z[4u+2]), o = s(z[4u+3])
+//     c = f*c + i*g,   h = o*tanh(c),   y[b, t, d*128 + u] = h
+// for t = 0..T-1 (forward) or T-1..0 (reverse), h and c starting at zero.
+//
+// Design (sm_103a): one thread-block cluster of C CTAs per tile of windows.
+// CTA `rank` owns hidden units [rank*128/C, (rank+1)*128/C); its slice of the
+// recurrent matrix (the four gate rows of each of its units, 128 columns)
+// lives in registers for the whole kernel: thread (slot, kc) holds the 4 x 16
+// weights of one unit for K chunk kc (16 columns).  Each step:
+//   1. every thread multiplies its weights with h_prev[kc*16 .. +16] of each
+//      of its NW windows from shared memory (paired FMAs, __ffma2_rn);
+//   2. the 8 lanes sharing a unit reduce their partial sums by a fixed
+//      butterfly (lane bits 2, 1, 0): a reduce-scatter that leaves each lane
+//      its share of the unit's gate pre-activations;
+//   3. add the prefetched projection value and the bias, apply the bounded
+//      activations, gather the four gates of a window (shuffles), update c
+//      and h (c stays in registers);
+//   4. write h to y, and store it into the next-step h buffer of every CTA of
+//      the cluster (distributed shared memory);
+//   5. barrier.cluster arrive.release / wait.acquire: after it, the next
+//      step's h buffer is complete in every CTA.  Two h buffers alternate by
+//      step parity, so one barrier per step suffices.
+// No global flag words and no spinning: the cluster barrier is hardware.
+// The arithmetic per (window, unit, gate) is the same for every cluster size
+// and tile width (same K chunks, same pairing, same reduction tree), so all
+// variants give bitwise-identical results.
+#include <stdio.h>
+
+#include "common.cuh"
+
+namespace lstm {
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int KC = 8;                 // K chunks = lanes per reduction group
+constexpr int KLEN = 16;              // columns per chunk
+constexpr int CHUNK_STRIDE = 20;      // padded chunk stride (conflict-free LDS.128)
+constexpr int HROW = KC * CHUNK_STRIDE;  // floats per window in the h buffer
+constexpr int PF = 4;                 // projection prefetch depth (steps)
+
+__device__ __forceinline__ float sigmoid_bounded(float z)
+{
+    z = fminf(fmaxf(z, -80.0f), 80.0f);
+    return __fdividef(1.0f, 1.0f + __expf(-z));
+}
+__device__ __forceinline__ float tanh_bounded(float z)
+{
+    return 2.0f * sigmoid_bounded(2.0f * z) - 1.0f;
+}
+
+// One butterfly level: lanes that differ in `mask` exchange half of their
+// N values; each keeps the sum for the half its mask bit selects.
+template <int N>
+__device__ __forceinline__ void reduce_level(const float (&in)[N], float (&out)[N / 2], int mask,
+                                             bool upper)
+{
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float keep = upper ? in[i + N / 2] : in[i];
+        const float send = upper ? in[i] : in[i + N / 2];
+        out[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+    }
+}
+
+template <int C, int NW>
+__global__ void __launch_bounds__(THREADS, 1)
+recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
+                  const float *__restrict__ bias, float *__restrict__ y, int batch, int steps,
+                  int direction)
+{
+    constexpr int U = kHidden / C;       // units per CTA
+    constexpr int SPU = 32 / U;          // slots per unit
+    constexpr int TW = SPU * NW;         // windows per tile (per cluster)
+    constexpr int V = 4 * NW;            // partial sums per thread
+    constexpr int HV = V >= 8 ? V / 8 : 1;  // values a lane holds after the reduction
+    constexpr int REPL = V >= 8 ? 4 / HV : 8;  // lanes holding one window's cell
+    static_assert(U * SPU == 32 && C * U == kHidden, "cluster shape");
+
+    __shared__ __align__(16) float hbuf[2][TW][HROW];
+
+    const int tid = threadIdx.x;
+    const int kc = tid & 7;
+    const int slot = tid >> 3;
+    const int ul = slot / SPU;
+    const int wg = slot % SPU;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int tile = static_cast<int>(ptx::cluster_id_x());
+    const int u = static_cast<int>(rank) * U + ul;  // this thread's hidden unit
+    const int win0 = tile * TW + wg * NW;           // this thread's first window
+
+    // weights: 4 gate rows of unit u, columns kc*16 .. kc*16+15, as pairs
+    float2 r2[4][KLEN / 2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 *src =
+            reinterpret_cast<const float2 *>(rp + (4 * u + q) * kHidden + kc * KLEN);
+#pragma unroll
+        for (int i = 0; i < KLEN / 2; ++i)
+            r2[q][i] = src[i];
+    }
+
+    // the values this lane holds after the reduction: index idx = w*4 + gate
+    float bias_v[HV];
+    const float *gsrc[HV];
+    bool gvalid[HV];
+#pragma unroll
+    for (int v = 0; v < HV; ++v) {
+        const int idx = V >= 8 ? kc * HV + v : (kc >> 1);
+        const int w = idx >> 2, q = idx & 3;
+        const int b = win0 + w;
+        bias_v[v] = bias[4 * u + q];
+        gvalid[v] = b < batch;
+        gsrc[v] = g + (gvalid[v] ? static_cast<long>(b) * steps * kGateColumns : 0) +
+                  direction * kGates + 4 * u + q;
+    }
+    // the window whose cell this lane updates, and its replica index
+    const int wl = V >= 8 ? (kc * HV) / 4 : 0;
+    const int replica = kc % REPL;
+    const int bcell = win0 + wl;
+    const bool cell_valid = bcell < batch;
+    float *ycol = y + (cell_valid ? static_cast<long>(bcell) * steps * kOutput : 0) +
+                  direction * kHidden + u;
+    const uint32_t hsend_off =
+        static_cast<uint32_t>(((wg * NW + wl) * HROW + (u / KLEN) * CHUNK_STRIDE + (u % KLEN)) * 4);
+
+    for (int i = tid; i < 2 * TW * HROW; i += THREADS)
+        (&hbuf[0][0][0])[i] = 0.0f;
+    // every CTA of the cluster is running and zeroed before anyone sends
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+
+    const uint32_t hbase = ptx::smem_u32(&hbuf[0][0][0]);
+    float gq[PF][HV];
+    auto gload = [&](int s, float (&dst)[HV]) {
+        const int t = direction ? steps - 1 - s : s;
+#pragma unroll
+        for (int v = 0; v < HV; ++v)
+            dst[v] = (gvalid[v] && s < steps) ? __ldg(gsrc[v] + static_cast<long>(t) * kGateColumns)
+                                              : 0.0f;
+    };
+#pragma unroll
+    for (int p = 0; p < PF; ++p)
+        gload(p, gq[p]);
+
+    float c = 0.0f;
+    for (int s0 = 0; s0 < steps; s0 += PF) {
+#pragma unroll
+        for (int p = 0; p < PF; ++p) {
+            const int s = s0 + p;
+            if (s >= steps)
+                break;
+            const int par = s & 1;
+
+            // 1. partial dot products over this lane's K chunk
+            float part[V];
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float4 *hp =
+                    reinterpret_cast<const float4 *>(&hbuf[par][wg * NW + w][kc * CHUNK_STRIDE]);
+                const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+                const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y}, {h1.z, h1.w},
+                                      {h2.x, h2.y}, {h2.z, h2.w}, {h3.x, h3.y}, {h3.z, h3.w}};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc = __ffma2_rn(r2[q][i], hh[i], acc);
+                    part[w * 4 + q] = acc.x + acc.y;
+                }
+            }
+
+            // 2. fixed butterfly over the 8 K-chunk lanes
+            float held[HV];
+            if constexpr (V >= 8) {
+                float a[V / 2], b2[V / 4];
+                reduce_level<V>(part, a, 4, (kc & 4) != 0);
+                reduce_level<V / 2>(a, b2, 2, (kc & 2) != 0);
+                reduce_level<V / 4>(b2, held, 1, (kc & 1) != 0);
+            } else {
+                float a[2], b2[1];
+                reduce_level<4>(part, a, 4, (kc & 4) != 0);
+                reduce_level<2>(a, b2, 2, (kc & 2) != 0);
+                held[0] = b2[0] + __shfl_xor_sync(0xffffffffu, b2[0], 1);
+            }
+
+            // 3. activations, gate gather, cell update
+            float act[HV];
+#pragma unroll
+            for (int v = 0; v < HV; ++v) {
+                const int idx = V >= 8 ? kc * HV + v : (kc >> 1);
+                const float z = held[v] + gq[p][v] + bias_v[v];
+                act[v] = (idx & 3) == 2 ? tanh_bounded(z) : sigmoid_bounded(z);
+            }
+            float gate[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int src = V >= 8 ? (4 * wl + q) / HV : 2 * q;
+                gate[q] = __shfl_sync(0xffffffffu, act[q % HV], src, 8);
+            }
+            c = gate[1] * c + gate[0] * gate[2];
+            const float h = gate[3] * tanh_bounded(c);
+
+            // 4. output and exchange
+            const int t = direction ? steps - 1 - s : s;
+            if (replica == 0 && cell_valid)
+                ycol[static_cast<long>(t) * kOutput] = h;
+            if (s + 1 < steps) {
+                const uint32_t dst = hbase + static_cast<uint32_t>((par ^ 1) * TW * HROW * 4) + hsend_off;
+#pragma unroll
+                for (int r = 0; r < C / REPL + (C % REPL ? 1 : 0); ++r) {
+                    const int peer = replica + r * REPL;
+                    if (peer < C)
+                        ptx::st_cluster_f32(ptx::map_to_rank(dst, peer), h);
+                }
+            }
+
+            // 5. step barrier; the next projection loads go out meanwhile
+            __syncwarp();
+            ptx::cluster_arrive_release();
+            gload(s + PF, gq[p]);
+            ptx::cluster_wait_acquire();
+        }
+    }
+}
+
+struct Variant {
+    int cluster;
+    int nw;
+    int tile;  // windows per cluster
+    const void *fn;
+};
+
+template <int C, int NW>
+Variant variant()
+{
+    return Variant{C, NW, (C / 4) * NW, reinterpret_cast<const void *>(&recurrence_kernel<C, NW>)};
+}
+
+const Variant kVariants[] = {
+    variant<16, 1>(), variant<16, 2>(), variant<16, 4>(), variant<16, 8>(),
+    variant<8, 1>(),  variant<8, 2>(),  variant<8, 4>(),  variant<8, 8>(),
+};
+
+const Variant *find_variant(int cluster, int nw)
+{
+    for (const Variant &v : kVariants)
+        if (v.cluster == cluster && v.nw == nw)
+            return &v;
+    return nullptr;
+}
+
+// The default variant for a batch: cluster 16, the narrowest tile that keeps
+// both directions' clusters within one wave where possible.
+const Variant *choose_variant(int batch)
+{
+    if (batch <= 4)
+        return find_variant(16, 1);
+    if (batch <= 32)
+        return find_variant(16, 2);
+    if (batch <= 64)
+        return find_variant(16, 4);
+    return find_variant(16, 8);
+}
+
+int launch_variant(const Variant &v, const float *g, const float *rp, const float *bias, float *y,
+                   int batch, int steps, int direction, cudaStream_t stream)
+{
+    const long tiles = (static_cast<long>(batch) + v.tile - 1) / v.tile;
+    const long blocks = tiles * v.cluster;
+    if (blocks > 0x7fffffffL)
+        return fail(LSTM_E_OVERFLOW, "recurrence: %d windows need %ld blocks", batch, blocks);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(v.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<float **>(&g), const_cast<float **>(&rp),
+                    const_cast<float **>(&bias), &y, &batch, &steps, &direction};
+    return cuda_status(cudaLaunchKernelExC(&cfg, v.fn, args), "recurrence launch");
+}
+
+} // namespace
+
+int recurrence_prepare(int)
+{
+    for (const Variant &v : kVariants) {
+        if (v.cluster > 8) {
+            int st = cuda_status(
+                cudaFuncSetAttribute(v.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+                "recurrence cluster-size attribute");
+            if (st != LSTM_OK)
+                return st;
+        }
+    }
+    return LSTM_OK;
+}
+
+int launch_recurrence(const float *g, const float *rp, const float *bias, float *y, int batch,
+                      int steps, int direction, cudaStream_t stream)
+{
+    return launch_variant(*choose_variant(batch), g, rp, bias, y, batch, steps, direction, stream);
+}
+
+int launch_recurrence_variant(const float *g, const float *rp, const float *bias, float *y,
+                              int batch, int steps, int direction, int cluster, int nw,
+                              cudaStream_t stream)
+{
+    const Variant *v = find_variant(cluster, nw);
+    if (!v)
+        return fail(LSTM_E_INVALID, "recurrence: no variant with cluster %d and %d windows per lane",
+                    cluster, nw);
+    return launch_variant(*v, g, rp, bias, y, batch, steps, direction, stream);
+}
+
+} // namespace lstm

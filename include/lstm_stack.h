@@ -1,0 +1,209 @@
+/*
+ * lstm_stack.h -- C ABI of liblstmstack.so, a GB300 (sm_103a) forward pass of
+ * the four-layer bidirectional LSTM stack (hidden size 128, input width 60 for
+ * the first layer and 256 after it, gate blocks i, f, g, o).
+ *
+ * The operation is the one the speakrs 0.6.0 pages define (docs.rs source of
+ * src/inference/cuda/candidate/lstmproj.rs and lstm.rs):
+ *  - module docs: per layer, a projection `x . W^T` for every step of each
+ *    direction with the gate columns reordered so each hidden unit's four
+ *    gates are adjacent, then one persistent recurrence per direction with
+ *    the recurrent weights on chip; the reverse direction runs beside the
+ *    forward one and the next layer waits for both;
+ *  - `PackedLayer`: W `[2, padded_input, 512]`/`[2, 512, padded_input]`,
+ *    R `[2, 512, 128]`, bias `[2, 512]` = Wb + Rb;
+ *  - `Oxide::with_recurrence`, pack closure: source lengths W = 2*512*input,
+ *    R = 2*512*128, B = 4*512;
+ *  - `Oxide::enqueue`: input `rows * 60`, output `rows * 256`, rows =
+ *    batch * steps; `check_len` / `to_u32`: exact-length and 32-bit checks;
+ *  - `recur`: the reverse direction's h goes to output columns 128..255.
+ * Cell equations (not printed on the pages; the standard LSTM):
+ *   z = W x_t + Wb + R h_prev + Rb,  i = s(z_i), f = s(z_f), g = tanh(z_g),
+ *   o = s(z_o),  c = f c + i g,  h = o tanh(c),  h and c start at zero.
+ *
+ * Conventions for every entry point below:
+ *  - All floating-point data is IEEE fp32, row-major, densely packed.
+ *  - "device" pointers are CUDA device (or managed) memory on the stack's
+ *    device; "host" pointers are CPU memory (pinned memory makes the copies
+ *    asynchronous).  Device pointers passed to a TMA-fed call must be 16-byte
+ *    aligned (cudaMalloc and torch give 256-byte alignment).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Device work is enqueued on it asynchronously; nothing
+ *    synchronises unless stated.
+ *  - The return value is LSTM_OK (0) or one of the LSTM_E_* codes;
+ *    lstm_stack_last_error() then returns a message for the calling thread.
+ *    No C++ exception crosses this boundary.
+ *  - Finite inputs give finite, bounded outputs.  How NaN or infinite inputs
+ *    surface is unspecified (the activations clamp their argument), as on the
+ *    pages (`SPECIAL_VALUES`).
+ */
+#ifndef LSTM_STACK_H
+#define LSTM_STACK_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LSTM_STACK_LAYERS 4
+#define LSTM_STACK_HIDDEN 128
+#define LSTM_STACK_FEATURES 60
+#define LSTM_STACK_GATES 512         /* 4 * HIDDEN, one direction            */
+#define LSTM_STACK_GATE_COLUMNS 1024 /* both directions' packed gate columns */
+#define LSTM_STACK_OUTPUT 256        /* 2 * HIDDEN                           */
+
+enum {
+    LSTM_OK = 0,
+    LSTM_E_INVALID = 1,  /* null pointer, non-positive or too-large size, bad direction, misaligned pointer */
+    LSTM_E_LENGTH = 2,   /* a buffer length differs from what the sizes need (message: expected/actual) */
+    LSTM_E_OVERFLOW = 3, /* a dimension does not fit the kernels' 32-bit indexing */
+    LSTM_E_DEVICE = 4,   /* the device is not sm_103 / refuses a needed attribute */
+    LSTM_E_CUDA = 5,     /* a CUDA runtime/driver call failed (message: its error string) */
+    LSTM_E_ALLOC = 6,    /* host or device allocation failed */
+    LSTM_E_FAULT = 7     /* a kernel's bounded wait ran out and it set its fault word */
+};
+
+/* ---------------------------------------------------------------------------
+ * The stack (create / forward / destroy)
+ * ------------------------------------------------------------------------- */
+
+typedef struct lstm_stack lstm_stack; /* opaque; owned by the library */
+
+/* Source weights, host fp32, read only during lstm_stack_create.  Layer l:
+ *   w[l] : [2][512][in_l]  direction d's W, gate row blocks i,f,g,o
+ *                          (row k*128 + u is gate k of unit u); in_0 = 60,
+ *                          in_l = 256 for l >= 1
+ *   r[l] : [2][512][128]   direction d's R, same row blocks
+ *   b[l] : [2][1024]       direction d's Wb[512] followed by Rb[512]
+ * Direction 0 is forward, 1 reverse. */
+typedef struct {
+    const float *w[LSTM_STACK_LAYERS];
+    const float *r[LSTM_STACK_LAYERS];
+    const float *b[LSTM_STACK_LAYERS];
+} lstm_stack_weights;
+
+/* Packs the weights (lstm_pack_layer) and copies them to `device`, allocates
+ * the device scratch for up to max_batch windows of up to max_steps steps
+ * (gate buffer [rows][1024], two ping-pong layer buffers [rows][256], host
+ * staging for lstm_stack_forward_host), creates the side stream and events.
+ * On success *out owns all of it.  Errors: LSTM_E_INVALID (null, sizes <= 0),
+ * LSTM_E_OVERFLOW (max_batch*max_steps*1024 beyond 2^31 rows*cols),
+ * LSTM_E_DEVICE (device is not compute capability 10.3 or lacks cluster
+ * launch), LSTM_E_CUDA, LSTM_E_ALLOC.  Nothing is leaked on failure. */
+int lstm_stack_create(const lstm_stack_weights *weights, int max_batch,
+                      int max_steps, int device, lstm_stack **out);
+
+/* y = stack(x) for `batch` independent windows of `steps` steps.
+ *   x : device [batch][steps][60],  x_len = batch*steps*60 floats
+ *   y : device [batch][steps][256], y_len = batch*steps*256 floats;
+ *       y[b][t][0:128] forward h, y[b][t][128:256] reverse h
+ * x and y must not overlap each other or the stack's scratch.  Enqueued on
+ * `stream`; allocates nothing and does not synchronise.  Each layer runs its
+ * projection on `stream`, then the forward recurrence on `stream` and the
+ * reverse one on the stack's side stream, joined back into `stream` before
+ * the next layer.  Calls on one stack object must not overlap (they share its
+ * scratch).  Errors: LSTM_E_INVALID (null, batch/steps <= 0 or above the
+ * create-time maxima, x not 16-byte aligned, device mismatch), LSTM_E_LENGTH,
+ * LSTM_E_CUDA. */
+int lstm_stack_forward(lstm_stack *s, const float *x, size_t x_len, float *y,
+                       size_t y_len, int batch, int steps, void *stream);
+
+/* The same forward pass from and to host memory: copies x (host, x_len
+ * floats) into the stack's device staging buffer on `stream`, runs
+ * lstm_stack_forward, copies the result back into y (host, y_len floats) and
+ * waits for `stream` before returning, so y is ready on return. */
+int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_t x_len,
+                            float *y_host, size_t y_len, int batch, int steps,
+                            void *stream);
+
+/* Opt-in per-phase timing (the pages' `LstmPhases` hooks): when enabled,
+ * every forward records CUDA events around each layer's projection (on the
+ * caller's stream) and around each direction's recurrence (on the stream it
+ * runs on).  lstm_stack_phase_times then waits for the last forward and
+ * writes 12 milliseconds into ms[12]: for layer l, ms[3l] projection,
+ * ms[3l+1] forward recurrence, ms[3l+2] reverse recurrence. */
+int lstm_stack_enable_phase_timing(lstm_stack *s, int enable);
+int lstm_stack_phase_times(lstm_stack *s, float *ms);
+
+/* Releases everything the stack owns (waits for its pending work first).
+ * NULL is ignored. */
+void lstm_stack_destroy(lstm_stack *s);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char *lstm_stack_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * The steps of the path, exposed one by one (used by the stack above; also
+ * callable on their own for testing and measurement)
+ * ------------------------------------------------------------------------- */
+
+/* Step 1, host: gate-interleaving packer of one layer (lstmproj.rs module
+ * docs and `PackedLayer`).  Host-only; needs no GPU.
+ *   w : [2][512][in_width], r : [2][512][128], b : [2][1024] (source layout)
+ *   wp_hi, wp_lo : [1024][kp]  both directions' W stacked; packed row
+ *        n = d*512 + 4u + k holds source row k*128 + u of direction d,
+ *        columns in_width..kp-1 zero; wp_hi is that value rounded to TF32
+ *        (round to nearest, ties away) and wp_lo = value - wp_hi, also
+ *        rounded to TF32, so wp_hi + wp_lo carries fp32-level precision
+ *   rp : [2][512][128]  packed row 4u + k of direction d = source row k*128+u
+ *   bias : [2][512]     bias[d][4u + k] = Wb[d][k*128+u] + Rb[d][k*128+u] (fp32)
+ * kp must be >= in_width and a multiple of 32.  Errors: LSTM_E_INVALID. */
+int lstm_pack_layer(const float *w, const float *r, const float *b,
+                    int in_width, int kp, float *wp_hi, float *wp_lo,
+                    float *rp, float *bias);
+
+/* Step 2, device: the input projection of one layer for both directions,
+ *   g[m][n] = sum_j x[m][j] * wp[n][j],  m < rows, n < 1024,
+ * computed on the tensor cores in a 3xTF32 split (x_hi*w_hi + x_hi*w_lo +
+ * x_lo*w_hi with fp32 accumulation), so the result carries fp32-level
+ * accuracy.  No bias is added.
+ *   x : device [rows][in_width], rows of in_width floats (in_width*4 bytes
+ *       must be a multiple of 16: 60 and 256 are)
+ *   wp_hi, wp_lo : device [1024][kp] from lstm_pack_layer (kp = in_width
+ *       rounded up to a multiple of 32; 64 for 60)
+ *   g : device [rows][1024]
+ * Errors: LSTM_E_INVALID (null, rows <= 0, in_width not in (0, kp], kp not a
+ * multiple of 32, misaligned pointers), LSTM_E_OVERFLOW, LSTM_E_DEVICE,
+ * LSTM_E_CUDA. */
+int lstm_projection(const float *x, int rows, int in_width,
+                    const float *wp_hi, const float *wp_lo, int kp, float *g,
+                    void *stream);
+
+/* Step 3, device: one direction's recurrence over one layer.
+ *   g    : device [batch*steps][1024] projection from lstm_projection
+ *          (row b*steps + t); this direction reads columns d*512 .. d*512+511
+ *   rp   : device [512][128]  this direction's packed R (lstm_pack_layer)
+ *   bias : device [512]       this direction's packed bias
+ *   y    : device [batch][steps][256]; writes columns d*128 .. d*128+127 only
+ *   direction : 0 forward (t = 0..steps-1), 1 reverse (t = steps-1..0)
+ * h and c start at zero for every window.  One thread-block cluster holds R
+ * in shared memory split across its blocks and exchanges h through
+ * distributed shared memory each step.  Errors: LSTM_E_INVALID,
+ * LSTM_E_OVERFLOW, LSTM_E_DEVICE, LSTM_E_CUDA. */
+int lstm_recurrence(const float *g, const float *rp, const float *bias,
+                    float *y, int batch, int steps, int direction,
+                    void *stream);
+
+/* lstm_recurrence with an explicit kernel variant, for tests and tuning:
+ * cluster_size 8 or 16 blocks per cluster, windows_per_lane 1, 2, 4 or 8
+ * (a cluster then runs cluster_size/4 * windows_per_lane windows).  Every
+ * variant computes the same sums in the same order, so all give bitwise
+ * identical y (the pages' three recurrence kernels are likewise bitwise
+ * identical, lstmproj.rs module docs).  Errors as lstm_recurrence, plus
+ * LSTM_E_INVALID for an unknown variant. */
+int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
+                            float *y, int batch, int steps, int direction,
+                            int cluster_size, int windows_per_lane,
+                            void *stream);
+
+/* Reads and clears the library's device fault word on the current device
+ * (set by a kernel whose bounded wait ran out; 0 = none).  Synchronises the
+ * device. */
+int lstm_fault_status(unsigned int *fault);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSTM_STACK_H */

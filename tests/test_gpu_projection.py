@@ -1,0 +1,65 @@
+"""Parity of the tcgen05 3xTF32 projection (through the C ABI) with the
+float64 oracle's packed-column projection, over ragged row counts and both
+layer widths."""
+import numpy as np
+import pytest
+
+import oracle
+from bidirectional_lstm_stack_gb300 import binding, synthetic
+from gpu_util import assert_within, cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def weights():
+    return synthetic.stack_weights()
+
+
+# rows: one row; a full tile; a tile plus one; several tiles with a ragged
+# tail; the small workload's 64 rows; the batch-8 workload's 4712 rows
+CASES = [(60, 1), (60, 64), (256, 128), (256, 129), (60, 300), (256, 300), (60, 4712),
+         (256, 4712)]
+
+
+@pytest.mark.parametrize("in_width,rows", CASES)
+def test_projection_matches_oracle(weights, in_width, rows):
+    import torch
+    layer = weights[0] if in_width == 60 else weights[1]
+    kp = 64 if in_width == 60 else 256
+    wp_hi, wp_lo, _, _ = binding.lstm_pack_layer(layer["w"], layer["r"], layer["b"], in_width, kp)
+    x = synthetic.random_matrix(100 + rows + in_width, (rows, in_width))
+    g = torch.full((rows, 1024), float("nan"), device="cuda")
+    binding.lstm_projection(cuda(x), rows, in_width, cuda(wp_hi), cuda(wp_lo), kp, g)
+    torch.cuda.synchronize()
+    ref = oracle.projection(x, layer["w"])
+    # 3xTF32 keeps fp32-level accuracy: a single TF32 product would miss this
+    # bound by ~100x
+    assert_within(g.cpu().numpy(), ref, atol=1e-5, rtol=1e-5, what=f"projection {in_width}x{rows}")
+    assert binding.lstm_fault_status() == 0
+
+
+def test_projection_large_inputs_exercise_the_lo_plane(weights):
+    # inputs of magnitude ~100 make the dropped lo terms visible if any product
+    # of the split were missing
+    import torch
+    layer = weights[1]
+    wp_hi, wp_lo, _, _ = binding.lstm_pack_layer(layer["w"], layer["r"], layer["b"], 256, 256)
+    rows = 257
+    x = synthetic.random_matrix(7, (rows, 256), scale=100.0)
+    g = torch.empty((rows, 1024), device="cuda")
+    binding.lstm_projection(cuda(x), rows, 256, cuda(wp_hi), cuda(wp_lo), 256, g)
+    torch.cuda.synchronize()
+    ref = oracle.projection(x, layer["w"])
+    assert_within(g.cpu().numpy(), ref, atol=5e-4, rtol=1e-5, what="projection x100")
+
+
+def test_projection_rejects_misaligned_input(weights):
+    import torch
+    layer = weights[0]
+    wp_hi, wp_lo, _, _ = binding.lstm_pack_layer(layer["w"], layer["r"], layer["b"], 60, 64)
+    x = torch.zeros(2 * 60 + 1, device="cuda")[1:]  # 4-byte offset
+    g = torch.empty((2, 1024), device="cuda")
+    with pytest.raises(binding.LSTMError) as e:
+        binding.lstm_projection(x, 2, 60, cuda(wp_hi), cuda(wp_lo), 64, g)
+    assert e.value.code == binding.LSTM_E_INVALID

@@ -1,0 +1,85 @@
+"""Parity of the cluster recurrence (through the C ABI) with the float64
+oracle's recurrence, given the same fp32 projection; and bitwise identity of
+every kernel variant."""
+import numpy as np
+import pytest
+
+import oracle
+from bidirectional_lstm_stack_gb300 import binding, synthetic
+from gpu_util import assert_within, cuda
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [(16, 1), (16, 2), (16, 4), (16, 8), (8, 1), (8, 2), (8, 4), (8, 8)]
+
+
+def _layer_inputs(batch, steps, layer_index=0, seed=21, scale=1.0):
+    layers = synthetic.stack_weights()
+    lay = layers[layer_index]
+    inw = lay["w"].shape[2]
+    x = synthetic.random_matrix(seed, (batch * steps, inw), scale=scale)
+    G = oracle.projection(x, lay["w"]).astype(np.float32)
+    _, _, rp, bias = binding.lstm_pack_layer(lay["w"], lay["r"], lay["b"], inw,
+                                            64 if inw == 60 else 256)
+    return lay, G, rp, bias
+
+
+def _run(G, rp, bias, batch, steps, variant=None):
+    import torch
+    g = cuda(G)
+    rpt, bt = cuda(rp), cuda(bias)
+    y = torch.full((batch, steps, 256), float("nan"), device="cuda")
+    for d in range(2):
+        if variant is None:
+            binding.lstm_recurrence(g, rpt[d], bt[d], y, batch, steps, d)
+        else:
+            binding.lstm_recurrence_variant(g, rpt[d], bt[d], y, batch, steps, d, *variant)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("batch,steps", [(1, 1), (1, 2), (1, 64), (3, 37), (5, 100), (9, 20),
+                                         (33, 12)])
+def test_recurrence_matches_oracle(batch, steps):
+    lay, G, rp, bias = _layer_inputs(batch, steps)
+    y = _run(G, rp, bias, batch, steps)
+    ref = oracle.recurrence(G.astype(np.float64), lay["r"], lay["b"], batch, steps)
+    assert_within(y, ref, what=f"recurrence b{batch} t{steps}")
+    assert binding.lstm_fault_status() == 0
+
+
+def test_recurrence_saturated_gates():
+    # large projections drive the gates into saturation (the x3 workload's regime)
+    lay, G, rp, bias = _layer_inputs(4, 50, layer_index=1, scale=6.0)
+    y = _run(G, rp, bias, 4, 50)
+    ref = oracle.recurrence(G.astype(np.float64), lay["r"], lay["b"], 4, 50)
+    assert_within(y, ref, what="recurrence saturated")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_every_variant_matches_oracle(variant):
+    batch, steps = 13, 29
+    lay, G, rp, bias = _layer_inputs(batch, steps, seed=22)
+    y = _run(G, rp, bias, batch, steps, variant)
+    ref = oracle.recurrence(G.astype(np.float64), lay["r"], lay["b"], batch, steps)
+    assert_within(y, ref, what=f"variant {variant}")
+
+
+def test_variants_are_bitwise_identical():
+    batch, steps = 37, 41
+    _, G, rp, bias = _layer_inputs(batch, steps, seed=23)
+    outs = [_run(G, rp, bias, batch, steps, v) for v in VARIANTS]
+    outs.append(_run(G, rp, bias, batch, steps, None))
+    for v, o in zip(VARIANTS + [None], outs):
+        assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)), v
+
+
+def test_unknown_variant_is_rejected():
+    import torch
+    g = torch.zeros((4, 1024), device="cuda")
+    rp = torch.zeros((512, 128), device="cuda")
+    b = torch.zeros(512, device="cuda")
+    y = torch.zeros((1, 4, 256), device="cuda")
+    with pytest.raises(binding.LSTMError) as e:
+        binding.lstm_recurrence_variant(g, rp, b, y, 1, 4, 0, 4, 1)
+    assert e.value.code == binding.LSTM_E_INVALID

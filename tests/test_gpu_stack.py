@@ -1,0 +1,110 @@
+"""The whole stack through the C ABI against the float64 oracle on the five
+synthetic workloads (the large ones on sampled windows, which are
+independent), plus determinism, the host-buffer entry point and argument
+errors with a live device."""
+import numpy as np
+import pytest
+
+import oracle
+from bidirectional_lstm_stack_gb300 import binding, synthetic
+from gpu_util import assert_within, cuda
+
+pytestmark = pytest.mark.gpu
+
+MAX_BATCH, MAX_STEPS = 256, 589
+
+
+@pytest.fixture(scope="module")
+def layers():
+    return synthetic.stack_weights()
+
+
+@pytest.fixture(scope="module")
+def stack(layers):
+    s = binding.LSTMStack(layers, MAX_BATCH, MAX_STEPS)
+    yield s
+    s.close()
+
+
+def _forward(stack, x):
+    import torch
+    y = stack(cuda(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+# windows compared per workload (None = all of them); the sampled sets include
+# the first and last window, so ragged cluster tiles are covered
+SAMPLES = {
+    "b1_t64": None,
+    "b1_t589": None,
+    "b8_t589_x3": None,
+    "b32_t589": [0, 5, 17, 31],
+    "b256_t589_z5": [0, 9, 128, 201, 255],
+}
+
+
+@pytest.mark.parametrize("name", list(SAMPLES))
+def test_stack_matches_oracle(stack, layers, name):
+    wl = synthetic.WORKLOADS[name]
+    x = synthetic.stack_input(wl)
+    y = _forward(stack, x)
+    idx = SAMPLES[name]
+    if idx is None:
+        idx = list(range(wl.batch))
+    ref = oracle.lstm_stack(x[idx], layers)
+    assert_within(y[idx], ref, what=name)
+    assert binding.lstm_fault_status() == 0
+
+
+def test_stack_ragged_small_shapes(stack, layers):
+    for batch, steps in [(1, 1), (2, 3), (7, 129), (19, 40)]:
+        x = synthetic.random_matrix(batch * 1000 + steps, (batch, steps, 60))
+        y = _forward(stack, x)
+        assert_within(y, oracle.lstm_stack(x, layers), what=f"stack b{batch} t{steps}")
+
+
+def test_stack_is_deterministic_and_host_path_matches(stack):
+    x = synthetic.stack_input(synthetic.WORKLOADS["b8_t589_x3"])
+    y1 = _forward(stack, x)
+    y2 = _forward(stack, x)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    yh = np.empty_like(y1)
+    binding.lstm_stack_forward_host(stack.handle, np.ascontiguousarray(x), yh, 8, 589)
+    assert np.array_equal(y1.view(np.uint32), yh.view(np.uint32))
+
+
+def test_stack_phase_timing(stack):
+    import torch
+    x = cuda(synthetic.stack_input(synthetic.WORKLOADS["b1_t64"]))
+    binding.lstm_stack_enable_phase_timing(stack.handle, True)
+    stack(x)
+    ms = binding.lstm_stack_phase_times(stack.handle)
+    binding.lstm_stack_enable_phase_timing(stack.handle, False)
+    torch.cuda.synchronize()
+    assert ms.shape == (4, 3) and np.all(ms > 0)
+
+
+def test_stack_argument_errors(stack):
+    import torch
+    x = torch.zeros((2, 10, 60), device="cuda")
+    y = torch.zeros((2, 10, 256), device="cuda")
+    h = stack.handle
+    lib = binding.load()
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.lstm_stack_forward(h, x.data_ptr(), x.numel() - 1, y.data_ptr(), y.numel(), 2, 10,
+                                  s) == binding.LSTM_E_LENGTH
+    assert "expected" in binding.lstm_stack_last_error()
+    assert lib.lstm_stack_forward(h, x.data_ptr(), x.numel(), y.data_ptr(), y.numel() + 1, 2, 10,
+                                  s) == binding.LSTM_E_LENGTH
+    big = MAX_BATCH + 1
+    assert lib.lstm_stack_forward(h, x.data_ptr(), big * 10 * 60, y.data_ptr(), big * 10 * 256,
+                                  big, 10, s) == binding.LSTM_E_INVALID
+    assert lib.lstm_stack_forward(h, x.data_ptr(), 0, y.data_ptr(), 0, 0, 10,
+                                  s) == binding.LSTM_E_INVALID
+    xm = torch.zeros(2 * 10 * 60 + 1, device="cuda")[1:]
+    assert lib.lstm_stack_forward(h, xm.data_ptr(), 1200, y.data_ptr(), y.numel(), 2, 10,
+                                  s) == binding.LSTM_E_INVALID
+    xh = np.zeros(1200, np.float32)
+    assert lib.lstm_stack_forward(h, xh.ctypes.data, 1200, y.data_ptr(), y.numel(), 2, 10,
+                                  s) == binding.LSTM_E_INVALID
