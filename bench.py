@@ -1,0 +1,383 @@
+"""Benchmark of the four-layer bidirectional LSTM stack on GB300.
+
+One step = one full forward pass of the stack (4 layers x (projection +
+forward and reverse recurrences)) over one batch of windows already resident
+in HBM.  The default workload is the batch-32 case (32 windows of 589 steps);
+the single-window latency case (batch 1, T = 589) is reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own
+stack on its own GPU with its own batch of windows (weak scaling: windows are
+independent, no data exchange); the step time is the maximum over ranks.
+
+Timing: CUDA events on the launching stream around each step; between timed
+steps a 256 MiB buffer is written to flush the 129 MB L2 (not timed).  Per-
+kernel times come from the library's phase events, recorded on the stream
+each kernel runs on.  SM clocks are sampled with nvidia-smi during the timed
+region.  ``--impl reference`` times the float64 CPU oracle on this machine's
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bidirectional_lstm_stack_gb300 import synthetic  # noqa: E402
+
+WORKLOAD = "b32_t589"
+LATENCY_WORKLOAD = "b1_t589"
+METRIC = "4-layer BiLSTM windows/s and µs/step at B=1,32 (H=128, T=589, fp32)"
+FLUSH_BYTES = 256 << 20
+LAYERS = synthetic.LAYERS
+H = synthetic.HIDDEN
+
+# roofline denominators
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal dense rates (per GPU) used to scale the measured bf16 peak to TF32
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_TF32_TFLOPS = 1100.0
+# FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop per FMA at the SM clock
+SMS = 152
+FP32_LANES = 128
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def flops_projection(rows: int) -> float:
+    """Algorithmic flops of the four projections: 2 * rows * 1024 * K_l."""
+    return sum(2.0 * rows * 1024 * (60 if l == 0 else 256) for l in range(LAYERS))
+
+
+def flops_recurrence_launch(batch: int, steps: int) -> float:
+    """Algorithmic flops of one recurrence launch (one direction, one layer):
+    the 512 x 128 matrix-vector product per window and step."""
+    return 2.0 * batch * steps * 4 * H * H
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        # "under load": samples above the idle floor
+        load = [r for r in rows if r[2] > 0.5 * max(x[2] for x in rows)] or rows
+        return {"sm_mhz": float(np.median([r[0] for r in load])),
+                "sm_max_mhz": float(max(r[1] for r in rows)),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": float(max(r[2] for r in rows))}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The float64 CPU oracle on this host's cores, on a bounded sample of the
+    workload: each step runs `sample` windows of the workload's input."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    wl = synthetic.WORKLOADS[args.workload]
+    layers = synthetic.stack_weights()
+    x = synthetic.stack_input(wl)
+    sample = min(wl.batch, args.reference_windows)
+    xs = x[:sample]
+    for _ in range(args.warmup):
+        oracle.lstm_stack(xs[:1], layers)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.lstm_stack(xs, layers)
+        times.append(time.perf_counter() - t0)
+    per_step = float(np.mean(times))
+    value = sample / per_step
+    cores = oracle.threads()
+    desc = f"{sample} of the {wl.batch} windows of {wl.name} per step (T={wl.steps}), float64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "windows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "steps": wl.steps, "hidden": H,
+                   "layers": LAYERS, "sample_windows": sample},
+        "cpu_baseline": {"value": value, "unit": "windows/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "windows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def cpu_baseline(workload: str, max_seconds: float = 20.0):
+    """The oracle as it stands on the host cores: whole windows of the
+    workload, as many as fit about `max_seconds` (at least one)."""
+    import oracle
+    wl = synthetic.WORKLOADS[workload]
+    layers = synthetic.stack_weights()
+    x = synthetic.stack_input(wl)
+    cores = oracle.threads()
+    t0 = time.perf_counter()
+    oracle.lstm_stack(x[:1], layers)
+    one = time.perf_counter() - t0
+    # windows run in parallel over (window, direction): estimate what fits
+    n = int(max(1, min(wl.batch, (max_seconds / max(one, 1e-6)) * max(1, cores // 2))))
+    t0 = time.perf_counter()
+    oracle.lstm_stack(x[:n], layers)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "windows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of the {wl.batch} windows of {wl.name} (T={wl.steps}), float64, "
+                      f"{dt:.1f} s"}
+
+
+def time_stack(stack, x, steps, warmup, flush, stream, with_phases=True):
+    """Per-step device time (ms) of stack.forward on resident inputs, L2
+    flushed between steps; and the mean per-phase times."""
+    import torch
+    from bidirectional_lstm_stack_gb300 import binding
+    y = torch.empty((x.shape[0], x.shape[1], 2 * H), device=x.device)
+    for _ in range(warmup):
+        stack.forward(x, y, stream)
+    torch.cuda.synchronize()
+    if with_phases:
+        binding.lstm_stack_enable_phase_timing(stack.handle, True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    phases = []
+    for i in range(steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(i)
+            starts[i].record(stream)
+            stack.forward(x, y, stream)
+            ends[i].record(stream)
+        if with_phases:
+            phases.append(binding.lstm_stack_phase_times(stack.handle))
+    torch.cuda.synchronize()
+    if with_phases:
+        binding.lstm_stack_enable_phase_timing(stack.handle, False)
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ph = np.mean(np.stack(phases), axis=0) if phases else None
+    return ms, ph, y
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from bidirectional_lstm_stack_gb300 import binding
+    from bidirectional_lstm_stack_gb300.sharding import max_over_ranks
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    wl = synthetic.WORKLOADS[args.workload]
+    lat = synthetic.WORKLOADS[LATENCY_WORKLOAD]
+    layers = synthetic.stack_weights()
+    stack = binding.LSTMStack(layers, max(wl.batch, lat.batch), max(wl.steps, lat.steps), dev)
+    stream = torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    # weak scaling: every rank runs its own batch of the workload's windows
+    x_host = synthetic.stack_input(wl)
+    x = torch.from_numpy(x_host).cuda()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clocks:
+        ms, phases, y = time_stack(stack, x, args.steps, args.warmup, flush, stream)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+    total_s = max_over_ranks(sum(ms) / 1e3, device=torch.device("cuda", dev))
+    ms_per_step = total_s * 1e3 / args.steps
+    value = wl.batch * world * args.steps / total_s
+
+    # latency case: one window of 589 steps
+    x1 = torch.from_numpy(synthetic.stack_input(lat)).cuda()
+    ms1, ph1, _ = time_stack(stack, x1, max(args.steps, 10), args.warmup, flush, stream)
+    ms1_step = max_over_ranks(float(np.mean(ms1)), device=torch.device("cuda", dev))
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    xp = torch.from_numpy(x_host).pin_memory()
+    yp = torch.empty((wl.batch, wl.steps, 2 * H), dtype=torch.float32).pin_memory()
+    xn, yn = xp.numpy(), yp.numpy()
+    for _ in range(args.warmup):
+        binding.lstm_stack_forward_host(stack.handle, xn, yn, wl.batch, wl.steps, stream)
+    e2e_s = []
+    for i in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(i)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        binding.lstm_stack_forward_host(stack.handle, xn, yn, wl.batch, wl.steps, stream)
+        e2e_s.append(time.perf_counter() - t0)
+    e2e_total = max_over_ranks(sum(e2e_s), device=torch.device("cuda", dev))
+    e2e_value = wl.batch * world * args.steps / e2e_total
+
+    # dominant kernel: the recurrence (per launch = one direction of one layer)
+    p, peak_kind = peaks()
+    clk = clocks.summary()
+    rec_ms = float(np.mean(phases[:, 1:]))   # mean over layers and both directions
+    proj_ms = float(np.mean(phases[:, 0]))
+    sm_mhz = clk.get("sm_mhz") or 2070.0
+    fp32_peak_tflops = SMS * FP32_LANES * 2 * (clk.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    rec_flops = flops_recurrence_launch(wl.batch, wl.steps)
+    rec_achieved = rec_flops / (rec_ms * 1e-3) / 1e12
+    tf32_peak = p["bf16_tflops"] * NOMINAL_TF32_TFLOPS / NOMINAL_BF16_TFLOPS
+    proj_peak = tf32_peak / 3.0    # 3xTF32: three TF32 products per fp32 product
+    proj_achieved = flops_projection(wl.batch * wl.steps) / LAYERS / (proj_ms * 1e-3) / 1e12
+    us_per_layer_step = ms_per_step * 1e3 / (LAYERS * wl.steps)
+    rec_us_per_step = rec_ms * 1e3 / wl.steps
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "windows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "steps": wl.steps, "hidden": H,
+                   "layers": LAYERS, "inputs": wl.description,
+                   "l2": "flushed: 256 MiB written between timed steps",
+                   "parallelism": f"windows sharded, {wl.batch} per GPU" if world > 1
+                   else "1 GPU"},
+        "us_per_step": us_per_layer_step,
+        "latency_b1": {"workload": lat.name, "ms_per_window": ms1_step,
+                       "windows_per_s": 1e3 / ms1_step,
+                       "us_per_step": ms1_step * 1e3 / (LAYERS * lat.steps),
+                       "recurrence_us_per_step": float(np.mean(ph1[:, 1:])) * 1e3 / lat.steps,
+                       "context": "pages: A100, TF32-projection stack, 3.21-4.13 ms per window"},
+        "phases_ms": {"projection": [round(float(v), 4) for v in phases[:, 0]],
+                      "recurrence_fwd": [round(float(v), 4) for v in phases[:, 1]],
+                      "recurrence_rev": [round(float(v), 4) for v in phases[:, 2]]},
+        "roofline": {"kernel": "recurrence (one direction, one layer)", "bound": "alu",
+                     "achieved": rec_achieved, "peak": fp32_peak_tflops, "unit": "TFLOP/s",
+                     "frac": rec_achieved / fp32_peak_tflops, "traffic": None,
+                     "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock",
+                     "us_per_step": rec_us_per_step},
+        "roofline_projection": {"kernel": "projection (one layer, both directions)",
+                                "bound": "tensor", "achieved": proj_achieved, "peak": proj_peak,
+                                "unit": "TFLOP/s", "frac": proj_achieved / proj_peak,
+                                "traffic": None,
+                                "peak_source": f"{peak_kind} bf16 burst {p['bf16_tflops']} x "
+                                               f"{NOMINAL_TF32_TFLOPS}/{NOMINAL_BF16_TFLOPS} "
+                                               f"(TF32) / 3 (3xTF32)"},
+        "e2e": {"value": e2e_value, "unit": "windows/s",
+                "h2d_bytes_per_step": int(xn.nbytes), "d2h_bytes_per_step": int(yn.nbytes)},
+        "gpu_launches": 12 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl.name)
+    if rank == 0:
+        print(json.dumps(line))
+    stack.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--reference-windows", type=int, default=2,
+                    help="windows per step of the --impl reference run")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
