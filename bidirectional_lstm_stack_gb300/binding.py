@@ -74,6 +74,7 @@ def load():
             "lstm_projection": (i, [_vp, i, i, _vp, _vp, i, _vp, _vp]),
             "lstm_recurrence": (i, [_vp, _vp, _vp, _vp, i, i, i, _vp]),
             "lstm_recurrence_variant": (i, [_vp, _vp, _vp, _vp, i, i, i, i, i, _vp]),
+            "lstm_recurrence_max_clusters": (i, [i, i, i, ctypes.POINTER(i)]),
             "lstm_fault_status": (i, [ctypes.POINTER(ctypes.c_uint)]),
         }
         for name, (res, args) in sig.items():
@@ -140,6 +141,14 @@ def lstm_recurrence_variant(g, rp, bias, y, batch: int, steps: int, direction: i
     _check(load().lstm_recurrence_variant(_ptr(g), _ptr(rp), _ptr(bias), _ptr(y), batch, steps,
                                           direction, cluster_size, windows_per_lane,
                                           _stream(stream, g.device)))
+
+
+def lstm_recurrence_max_clusters(cluster_size: int, windows_per_lane: int,
+                                 device: int = 0) -> int:
+    v = ctypes.c_int(0)
+    _check(load().lstm_recurrence_max_clusters(cluster_size, windows_per_lane, device,
+                                               ctypes.byref(v)))
+    return int(v.value)
 
 
 def lstm_fault_status() -> int:

@@ -424,7 +424,8 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
             return st;
         if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 1, 0), stream), "event")))
             return st;
-        st = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps, 0, stream);
+        st = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps, 0, s->fault,
+                               stream);
         if (st != LSTM_OK)
             return st;
         if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 1, 1), stream), "event")))
@@ -432,7 +433,7 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
         if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 2, 0), s->side), "event")))
             return st;
         st = launch_recurrence(s->gates, s->rp[l] + kGates * kHidden, s->bias[l] + kGates, dst,
-                               batch, steps, 1, s->side);
+                               batch, steps, 1, s->fault, s->side);
         if (st != LSTM_OK)
             return st;
         if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 2, 1), s->side), "event")))
@@ -578,7 +579,10 @@ extern "C" int lstm_recurrence(const float *g, const float *rp, const float *bia
     if (st != LSTM_OK)
         return st;
     DeviceGuard guard(dev);
-    return launch_recurrence(g, rp, bias, y, batch, steps, direction,
+    unsigned *fault = fault_word();
+    if (!fault)
+        return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
+    return launch_recurrence(g, rp, bias, y, batch, steps, direction, fault,
                              static_cast<cudaStream_t>(stream));
 }
 
@@ -591,8 +595,23 @@ extern "C" int lstm_recurrence_variant(const float *g, const float *rp, const fl
     if (st != LSTM_OK)
         return st;
     DeviceGuard guard(dev);
+    unsigned *fault = fault_word();
+    if (!fault)
+        return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
     return launch_recurrence_variant(g, rp, bias, y, batch, steps, direction, cluster_size,
-                                     windows_per_lane, static_cast<cudaStream_t>(stream));
+                                     windows_per_lane, fault, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int lstm_recurrence_max_clusters(int cluster_size, int windows_per_lane, int device,
+                                            int *max_clusters)
+{
+    if (!max_clusters)
+        return fail(LSTM_E_INVALID, "lstm_recurrence_max_clusters: null pointer");
+    int st = prepare_device(device);
+    if (st != LSTM_OK)
+        return st;
+    DeviceGuard guard(device);
+    return recurrence_max_clusters(cluster_size, windows_per_lane, max_clusters);
 }
 
 extern "C" int lstm_fault_status(unsigned int *fault)

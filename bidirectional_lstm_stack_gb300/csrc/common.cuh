@@ -31,6 +31,7 @@ enum : unsigned {
     kFaultMma = 1u << 2,
     kFaultEpilogue = 1u << 3,
     kFaultDrain = 1u << 4,
+    kFaultRecurrence = 1u << 5,
 };
 
 // The device fault word of the current device (a __device__ variable;
@@ -52,10 +53,12 @@ int projection_prepare(int device);
 // ---- recurrence (recurrence.cu) ------------------------------------------
 int launch_recurrence(const float *g, const float *rp, const float *bias,
                       float *y, int batch, int steps, int direction,
-                      cudaStream_t stream);
+                      unsigned *fault, cudaStream_t stream);
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias,
                               float *y, int batch, int steps, int direction,
-                              int cluster, int nw, cudaStream_t stream);
+                              int cluster, int nw, unsigned *fault, cudaStream_t stream);
+// Clusters of a variant the device can hold at once (0 if unknown variant).
+int recurrence_max_clusters(int cluster, int nw, int *out);
 int recurrence_prepare(int device);
 
 } // namespace lstm
@@ -239,6 +242,28 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// One-sided push of a value into a peer CTA's shared memory; on arrival the
+// peer's mbarrier at `remote_bar` is credited with 4 transaction bytes.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
+                     remote_addr),
+                 "f"(v), "r"(remote_bar)
+                 : "memory");
+}
+// try_wait with acquire semantics at cluster scope (pairs with the
+// transaction credit of st.async from peer CTAs).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
 }
 __device__ __forceinline__ void cluster_arrive_release()
 {

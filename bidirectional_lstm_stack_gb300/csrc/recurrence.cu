@@ -19,12 +19,19 @@
 //   3. add the prefetched projection value and the bias, apply the bounded
 //      activations, gather the four gates of a window (shuffles), update c
 //      and h (c stays in registers);
-//   4. write h to y, and store it into the next-step h buffer of every CTA of
-//      the cluster (distributed shared memory);
-//   5. barrier.cluster arrive.release / wait.acquire: after it, the next
-//      step's h buffer is complete in every CTA.  Two h buffers alternate by
-//      step parity, so one barrier per step suffices.
-// No global flag words and no spinning: the cluster barrier is hardware.
+//   4. write h to y, and push it into the next-step h buffer of every CTA of
+//      the cluster with st.async (distributed shared memory), which credits
+//      the receiving CTA's mbarrier for that buffer with the bytes written;
+//   5. before reading a buffer, wait on its mbarrier: the phase completes when
+//      all 128 x (tile) values of the step have landed.
+// Two h buffers alternate by step parity.  The exchange is one-sided: no
+// cluster-wide barrier per step, no global flag words, and no release fence
+// (which would also wait for the in-flight projection prefetch loads).  Data
+// dependence makes the double buffer safe: a CTA can only push step s+1's h
+// once it holds every unit's h_s, i.e. once every warp of every CTA has
+// finished reading the buffer it is about to overwrite.  Each wait is bounded
+// in time; when one runs out the kernel records a fault bit, stops waiting
+// and finishes (with wrong results) instead of hanging.
 // The arithmetic per (window, unit, gate) is the same for every cluster size
 // and tile width (same K chunks, same pairing, same reduction tree), so all
 // variants give bitwise-identical results.
@@ -41,6 +48,7 @@ constexpr int KLEN = 16;              // columns per chunk
 constexpr int CHUNK_STRIDE = 20;      // padded chunk stride (conflict-free LDS.128)
 constexpr int HROW = KC * CHUNK_STRIDE;  // floats per window in the h buffer
 constexpr int PF = 4;                 // projection prefetch depth (steps)
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
 __device__ __forceinline__ float sigmoid_bounded(float z)
 {
@@ -70,7 +78,7 @@ template <int C, int NW>
 __global__ void __launch_bounds__(THREADS, 1)
 recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                   const float *__restrict__ bias, float *__restrict__ y, int batch, int steps,
-                  int direction)
+                  int direction, unsigned *fault)
 {
     constexpr int U = kHidden / C;       // units per CTA
     constexpr int SPU = 32 / U;          // slots per unit
@@ -80,7 +88,10 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     constexpr int REPL = V >= 8 ? 4 / HV : 8;  // lanes holding one window's cell
     static_assert(U * SPU == 32 && C * U == kHidden, "cluster shape");
 
+    constexpr uint32_t STEP_BYTES = kHidden * TW * 4;  // h values a CTA receives per step
     __shared__ __align__(16) float hbuf[2][TW][HROW];
+    __shared__ __align__(8) uint64_t hbar[2];
+    __shared__ int abort_flag;
 
     const int tid = threadIdx.x;
     const int kc = tid & 7;
@@ -127,13 +138,26 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     const uint32_t hsend_off =
         static_cast<uint32_t>(((wg * NW + wl) * HROW + (u / KLEN) * CHUNK_STRIDE + (u % KLEN)) * 4);
 
-    for (int i = tid; i < 2 * TW * HROW; i += THREADS)
+    // h_{-1} = 0 in buffer 0; buffer 1 is written whole before it is read
+    for (int i = tid; i < TW * HROW; i += THREADS)
         (&hbuf[0][0][0])[i] = 0.0f;
-    // every CTA of the cluster is running and zeroed before anyone sends
+    if (tid == 0) {
+        ptx::mbar_init(&hbar[0], 1);
+        ptx::mbar_init(&hbar[1], 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+        // arm buffer 1 for h_0 and buffer 0 for h_1
+        if (steps > 1)
+            ptx::mbar_arrive_expect_tx(&hbar[1], STEP_BYTES);
+        if (steps > 2)
+            ptx::mbar_arrive_expect_tx(&hbar[0], STEP_BYTES);
+    }
+    // every CTA of the cluster is running, zeroed and armed before anyone sends
     ptx::cluster_arrive_release();
     ptx::cluster_wait_acquire();
 
     const uint32_t hbase = ptx::smem_u32(&hbuf[0][0][0]);
+    const uint32_t bar_base = ptx::smem_u32(&hbar[0]);
     float gq[PF][HV];
     auto gload = [&](int s, float (&dst)[HV]) {
         const int t = direction ? steps - 1 - s : s;
@@ -154,6 +178,27 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             if (s >= steps)
                 break;
             const int par = s & 1;
+
+            // 0. h_{s-1} complete in buffer `par`
+            if (s > 0) {
+                const uint32_t phase = ((s - 1) >> 1) & 1;
+                volatile int *abort_v = &abort_flag;
+                if (!ptx::mbar_try_wait_cluster(&hbar[par], phase) && !*abort_v) {
+                    const uint64_t start = ptx::globaltimer();
+                    while (!ptx::mbar_try_wait_cluster(&hbar[par], phase)) {
+                        if (*abort_v)
+                            break;
+                        if (ptx::globaltimer() - start > WAIT_LIMIT_NS) {
+                            atomicOr(fault, kFaultRecurrence);
+                            *abort_v = 1;
+                            break;
+                        }
+                    }
+                }
+                // re-arm this buffer for h_{s+1}
+                if (tid == 0 && s + 2 < steps)
+                    ptx::mbar_arrive_expect_tx(&hbar[par], STEP_BYTES);
+            }
 
             // 1. partial dot products over this lane's K chunk
             float part[V];
@@ -210,22 +255,26 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             if (replica == 0 && cell_valid)
                 ycol[static_cast<long>(t) * kOutput] = h;
             if (s + 1 < steps) {
-                const uint32_t dst = hbase + static_cast<uint32_t>((par ^ 1) * TW * HROW * 4) + hsend_off;
+                const uint32_t dst =
+                    hbase + static_cast<uint32_t>((par ^ 1) * TW * HROW * 4) + hsend_off;
+                const uint32_t bar = bar_base + static_cast<uint32_t>((par ^ 1) * 8);
 #pragma unroll
                 for (int r = 0; r < C / REPL + (C % REPL ? 1 : 0); ++r) {
                     const int peer = replica + r * REPL;
                     if (peer < C)
-                        ptx::st_cluster_f32(ptx::map_to_rank(dst, peer), h);
+                        ptx::st_async_f32(ptx::map_to_rank(dst, peer), h,
+                                          ptx::map_to_rank(bar, peer));
                 }
             }
 
-            // 5. step barrier; the next projection loads go out meanwhile
-            __syncwarp();
-            ptx::cluster_arrive_release();
+            // 5. projection values PF steps ahead
             gload(s + PF, gq[p]);
-            ptx::cluster_wait_acquire();
         }
     }
+    // no CTA leaves while a peer may still write into its shared memory
+    __syncwarp();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
 }
 
 struct Variant {
@@ -268,7 +317,7 @@ const Variant *choose_variant(int batch)
 }
 
 int launch_variant(const Variant &v, const float *g, const float *rp, const float *bias, float *y,
-                   int batch, int steps, int direction, cudaStream_t stream)
+                   int batch, int steps, int direction, unsigned *fault, cudaStream_t stream)
 {
     const long tiles = (static_cast<long>(batch) + v.tile - 1) / v.tile;
     const long blocks = tiles * v.cluster;
@@ -287,7 +336,7 @@ int launch_variant(const Variant &v, const float *g, const float *rp, const floa
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     void *args[] = {const_cast<float **>(&g), const_cast<float **>(&rp),
-                    const_cast<float **>(&bias), &y, &batch, &steps, &direction};
+                    const_cast<float **>(&bias), &y, &batch, &steps, &direction, &fault};
     return cuda_status(cudaLaunchKernelExC(&cfg, v.fn, args), "recurrence launch");
 }
 
@@ -308,20 +357,40 @@ int recurrence_prepare(int)
 }
 
 int launch_recurrence(const float *g, const float *rp, const float *bias, float *y, int batch,
-                      int steps, int direction, cudaStream_t stream)
+                      int steps, int direction, unsigned *fault, cudaStream_t stream)
 {
-    return launch_variant(*choose_variant(batch), g, rp, bias, y, batch, steps, direction, stream);
+    return launch_variant(*choose_variant(batch), g, rp, bias, y, batch, steps, direction, fault,
+                          stream);
 }
 
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias, float *y,
                               int batch, int steps, int direction, int cluster, int nw,
-                              cudaStream_t stream)
+                              unsigned *fault, cudaStream_t stream)
 {
     const Variant *v = find_variant(cluster, nw);
     if (!v)
         return fail(LSTM_E_INVALID, "recurrence: no variant with cluster %d and %d windows per lane",
                     cluster, nw);
-    return launch_variant(*v, g, rp, bias, y, batch, steps, direction, stream);
+    return launch_variant(*v, g, rp, bias, y, batch, steps, direction, fault, stream);
+}
+
+int recurrence_max_clusters(int cluster, int nw, int *out)
+{
+    const Variant *v = find_variant(cluster, nw);
+    if (!v)
+        return fail(LSTM_E_INVALID, "recurrence: no variant with cluster %d and %d windows per lane",
+                    cluster, nw);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(v->cluster));
+    cfg.blockDim = dim3(THREADS);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(v->cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaOccupancyMaxActiveClusters(out, v->fn, &cfg), "max active clusters");
 }
 
 } // namespace lstm

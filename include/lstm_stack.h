@@ -197,6 +197,13 @@ int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
                             int cluster_size, int windows_per_lane,
                             void *stream);
 
+/* How many clusters of a recurrence variant `device` can run at once
+ * (cudaOccupancyMaxActiveClusters); the stack picks its variant per batch
+ * so that both directions' clusters fit in one wave where they can.
+ * Errors: LSTM_E_INVALID (null, unknown variant), LSTM_E_DEVICE, LSTM_E_CUDA. */
+int lstm_recurrence_max_clusters(int cluster_size, int windows_per_lane,
+                                 int device, int *max_clusters);
+
 /* Reads and clears the library's device fault word on the current device
  * (set by a kernel whose bounded wait ran out; 0 = none).  Synchronises the
  * device. */

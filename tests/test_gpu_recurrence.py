@@ -83,3 +83,11 @@ def test_unknown_variant_is_rejected():
     with pytest.raises(binding.LSTMError) as e:
         binding.lstm_recurrence_variant(g, rp, b, y, 1, 4, 0, 4, 1)
     assert e.value.code == binding.LSTM_E_INVALID
+
+
+def test_max_clusters_query():
+    for c, nw in VARIANTS:
+        n = binding.lstm_recurrence_max_clusters(c, nw)
+        assert n >= 1, (c, nw, n)
+    with pytest.raises(binding.LSTMError):
+        binding.lstm_recurrence_max_clusters(4, 1)
