@@ -252,6 +252,15 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
                  "f"(v), "r"(remote_bar)
                  : "memory");
 }
+// 16-byte variant: four consecutive floats, 16 transaction bytes.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c,
+                                            float d, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+                 : "memory");
+}
 // try_wait with acquire semantics at cluster scope (pairs with the
 // transaction credit of st.async from peer CTAs).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)

@@ -19,9 +19,11 @@
 //   3. add the prefetched projection value and the bias, apply the bounded
 //      activations, gather the four gates of a window (shuffles), update c
 //      and h (c stays in registers);
-//   4. write h to y, and push it into the next-step h buffer of every CTA of
-//      the cluster with st.async (distributed shared memory), which credits
-//      the receiving CTA's mbarrier for that buffer with the bytes written;
+//   4. gather the h of the warp's four consecutive units, write them to y
+//      (one float4) and push them into the next-step h buffer of every CTA
+//      of the cluster with one 16-byte st.async each (distributed shared
+//      memory), which credits the receiving CTA's mbarrier for that buffer
+//      with the bytes written; padding windows past the batch send nothing;
 //   5. before reading a buffer, wait on its mbarrier: the phase completes when
 //      all 128 x (tile) values of the step have landed.
 // Two h buffers alternate by step parity.  The exchange is one-sided: no
@@ -88,7 +90,6 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     constexpr int REPL = V >= 8 ? 4 / HV : 8;  // lanes holding one window's cell
     static_assert(U * SPU == 32 && C * U == kHidden, "cluster shape");
 
-    constexpr uint32_t STEP_BYTES = kHidden * TW * 4;  // h values a CTA receives per step
     __shared__ __align__(16) float hbuf[2][TW][HROW];
     __shared__ __align__(8) uint64_t hbar[2];
     __shared__ int abort_flag;
@@ -96,12 +97,19 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     const int tid = threadIdx.x;
     const int kc = tid & 7;
     const int slot = tid >> 3;
-    const int ul = slot / SPU;
-    const int wg = slot % SPU;
+    // units vary fastest over slots, so the four 8-lane groups of a warp hold
+    // four consecutive units of the same windows
+    const int ul = slot % U;
+    const int wg = slot / U;
     const uint32_t rank = ptx::cluster_ctarank();
     const int tile = static_cast<int>(ptx::cluster_id_x());
     const int u = static_cast<int>(rank) * U + ul;  // this thread's hidden unit
     const int win0 = tile * TW + wg * NW;           // this thread's first window
+    const int u0 = u & ~3;                          // first of the warp's four units
+    // windows of this tile inside the batch; padding windows are computed but
+    // their h is neither sent nor stored
+    const int valid_tw = min(TW, batch - tile * TW);
+    const uint32_t step_bytes = static_cast<uint32_t>(kHidden * valid_tw * 4);
 
     // weights: 4 gate rows of unit u, columns kc*16 .. kc*16+15, as pairs
     float2 r2[4][KLEN / 2];
@@ -128,18 +136,20 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
         gsrc[v] = g + (gvalid[v] ? static_cast<long>(b) * steps * kGateColumns : 0) +
                   direction * kGates + 4 * u + q;
     }
-    // the window whose cell this lane updates, and its replica index
+    // the window whose cell this lane updates; after the gather below, the
+    // 4*REPL lanes of the warp that hold it share the sends to the C CTAs
     const int wl = V >= 8 ? (kc * HV) / 4 : 0;
-    const int replica = kc % REPL;
+    const int sender = (tid & 31) / 8 * REPL + kc % REPL;  // 0 .. 4*REPL-1
     const int bcell = win0 + wl;
     const bool cell_valid = bcell < batch;
     float *ycol = y + (cell_valid ? static_cast<long>(bcell) * steps * kOutput : 0) +
-                  direction * kHidden + u;
-    const uint32_t hsend_off =
-        static_cast<uint32_t>(((wg * NW + wl) * HROW + (u / KLEN) * CHUNK_STRIDE + (u % KLEN)) * 4);
+                  direction * kHidden + u0;
+    const uint32_t hsend_off = static_cast<uint32_t>(
+        ((wg * NW + wl) * HROW + (u0 / KLEN) * CHUNK_STRIDE + (u0 % KLEN)) * 4);
 
-    // h_{-1} = 0 in buffer 0; buffer 1 is written whole before it is read
-    for (int i = tid; i < TW * HROW; i += THREADS)
+    // h_{-1} = 0 in buffer 0; buffer 1 is zeroed too, so padding windows
+    // (never sent) only ever see zeros
+    for (int i = tid; i < 2 * TW * HROW; i += THREADS)
         (&hbuf[0][0][0])[i] = 0.0f;
     if (tid == 0) {
         ptx::mbar_init(&hbar[0], 1);
@@ -148,9 +158,9 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
         ptx::fence_mbar_init();
         // arm buffer 1 for h_0 and buffer 0 for h_1
         if (steps > 1)
-            ptx::mbar_arrive_expect_tx(&hbar[1], STEP_BYTES);
+            ptx::mbar_arrive_expect_tx(&hbar[1], step_bytes);
         if (steps > 2)
-            ptx::mbar_arrive_expect_tx(&hbar[0], STEP_BYTES);
+            ptx::mbar_arrive_expect_tx(&hbar[0], step_bytes);
     }
     // every CTA of the cluster is running, zeroed and armed before anyone sends
     ptx::cluster_arrive_release();
@@ -197,7 +207,7 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                 }
                 // re-arm this buffer for h_{s+1}
                 if (tid == 0 && s + 2 < steps)
-                    ptx::mbar_arrive_expect_tx(&hbar[par], STEP_BYTES);
+                    ptx::mbar_arrive_expect_tx(&hbar[par], step_bytes);
             }
 
             // 1. partial dot products over this lane's K chunk
@@ -250,20 +260,26 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             c = gate[1] * c + gate[0] * gate[2];
             const float h = gate[3] * tanh_bounded(c);
 
-            // 4. output and exchange
+            // 4. gather the warp's four units of window wl, store them to y and
+            //    push them (16 bytes) into every CTA's next h buffer
+            float h4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                h4[j] = __shfl_sync(0xffffffffu, h, 8 * j + kc);
             const int t = direction ? steps - 1 - s : s;
-            if (replica == 0 && cell_valid)
-                ycol[static_cast<long>(t) * kOutput] = h;
-            if (s + 1 < steps) {
+            if (sender == 0 && cell_valid)
+                *reinterpret_cast<float4 *>(ycol + static_cast<long>(t) * kOutput) =
+                    make_float4(h4[0], h4[1], h4[2], h4[3]);
+            if (s + 1 < steps && cell_valid) {
                 const uint32_t dst =
                     hbase + static_cast<uint32_t>((par ^ 1) * TW * HROW * 4) + hsend_off;
                 const uint32_t bar = bar_base + static_cast<uint32_t>((par ^ 1) * 8);
 #pragma unroll
-                for (int r = 0; r < C / REPL + (C % REPL ? 1 : 0); ++r) {
-                    const int peer = replica + r * REPL;
+                for (int r = 0; r < (C + 4 * REPL - 1) / (4 * REPL); ++r) {
+                    const int peer = sender + r * 4 * REPL;
                     if (peer < C)
-                        ptx::st_async_f32(ptx::map_to_rank(dst, peer), h,
-                                          ptx::map_to_rank(bar, peer));
+                        ptx::st_async_v4(ptx::map_to_rank(dst, peer), h4[0], h4[1], h4[2], h4[3],
+                                         ptx::map_to_rank(bar, peer));
                 }
             }
 
