@@ -274,6 +274,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
                  : "memory");
     return ok != 0;
 }
+// Non-blocking test of the same phase (the caller spins).
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void cluster_arrive_release()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");

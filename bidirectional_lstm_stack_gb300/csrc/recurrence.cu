@@ -123,6 +123,10 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     }
 
     // the values this lane holds after the reduction: index idx = w*4 + gate
+    // Activations are branch-free across the lanes (which hold different
+    // gates): act = m * s(m * z) + a with (m, a) = (2, -1) for the cell
+    // candidate, i.e. tanh(z) = 2 s(2z) - 1, and (1, 0) for the gates.
+    float act_m[HV], act_a[HV];
     float bias_v[HV];
     const float *gsrc[HV];
     bool gvalid[HV];
@@ -132,6 +136,8 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
         const int w = idx >> 2, q = idx & 3;
         const int b = win0 + w;
         bias_v[v] = bias[4 * u + q];
+        act_m[v] = q == 2 ? 2.0f : 1.0f;
+        act_a[v] = q == 2 ? -1.0f : 0.0f;
         gvalid[v] = b < batch;
         gsrc[v] = g + (gvalid[v] ? static_cast<long>(b) * steps * kGateColumns : 0) +
                   direction * kGates + 4 * u + q;
@@ -247,9 +253,8 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             float act[HV];
 #pragma unroll
             for (int v = 0; v < HV; ++v) {
-                const int idx = V >= 8 ? kc * HV + v : (kc >> 1);
-                const float z = held[v] + gq[p][v] + bias_v[v];
-                act[v] = (idx & 3) == 2 ? tanh_bounded(z) : sigmoid_bounded(z);
+                const float z = held[v] + (gq[p][v] + bias_v[v]);
+                act[v] = fmaf(act_m[v], sigmoid_bounded(act_m[v] * z), act_a[v]);
             }
             float gate[4];
 #pragma unroll
@@ -319,17 +324,19 @@ const Variant *find_variant(int cluster, int nw)
     return nullptr;
 }
 
-// The default variant for a batch: cluster 16, the narrowest tile that keeps
-// both directions' clusters within one wave where possible.
+// The default variant for a batch, from per-step timings of every variant
+// with both directions running (GB300, T = 589): clusters of 8 with two
+// windows each are fastest up to a few dozen windows (0.47 us/step at one
+// window, 0.65 us/step at 32, two CTAs per SM); wider tiles win once the
+// grid no longer fits one wave (batch 256: 8 windows per lane, 16 per
+// cluster).
 const Variant *choose_variant(int batch)
 {
-    if (batch <= 4)
-        return find_variant(16, 1);
-    if (batch <= 32)
-        return find_variant(16, 2);
     if (batch <= 64)
-        return find_variant(16, 4);
-    return find_variant(16, 8);
+        return find_variant(8, 1);
+    if (batch <= 128)
+        return find_variant(8, 4);
+    return find_variant(8, 8);
 }
 
 int launch_variant(const Variant &v, const float *g, const float *rp, const float *bias, float *y,
