@@ -76,6 +76,7 @@ def load():
             "lstm_recurrence_variant": (i, [_vp, _vp, _vp, _vp, i, i, i, i, i, _vp]),
             "lstm_recurrence_max_clusters": (i, [i, i, i, ctypes.POINTER(i)]),
             "lstm_fault_status": (i, [ctypes.POINTER(ctypes.c_uint)]),
+            "lstm_layer_forward_static": (i, [_vp, i, i, i, _vp, _vp, i, _vp, _vp, _vp, _vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -149,6 +150,15 @@ def lstm_recurrence_max_clusters(cluster_size: int, windows_per_lane: int,
     _check(load().lstm_recurrence_max_clusters(cluster_size, windows_per_lane, device,
                                                ctypes.byref(v)))
     return int(v.value)
+
+
+def lstm_layer_forward_static(x, batch: int, steps: int, in_width: int, wp_hi, wp_lo, kp: int,
+                              rp, bias, y, stream=None):
+    """One bidirectional layer through the entry point that allocates no
+    device memory (its gate buffer is a fixed array inside the library)."""
+    _check(load().lstm_layer_forward_static(_ptr(x), batch, steps, in_width, _ptr(wp_hi),
+                                            _ptr(wp_lo), kp, _ptr(rp), _ptr(bias), _ptr(y),
+                                            _stream(stream, x.device)))
 
 
 def lstm_fault_status() -> int:

@@ -1,0 +1,120 @@
+// One bidirectional LSTM layer that allocates no device memory.
+//
+// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
+// being captured (allocation is not a capturable operation), plug-ins whose
+// host framework owns all device memory through its own arena and forbids
+// allocations behind its back, and latency-critical loops where an
+// allocation's implicit device synchronisation is not acceptable.  Those
+// callers still pass their inputs, packed weights and outputs; the gate
+// buffer the layer needs between its projection and its recurrences lives
+// here in a fixed file-scope device array instead of a cudaMalloc'd one.
+//
+// The array holds kStaticRows rows of 1024 gate pre-activations (16 MiB).
+// Every GPU that loads the library keeps it until the process exits.  All
+// calls share it, so calls that overlap on the GPU (different streams, or
+// different host threads) race on it and must be ordered by the caller.  It
+// keeps the previous call's contents; nothing needs clearing, because each
+// call's projection writes every row its recurrences then read.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace lstm {
+namespace {
+
+constexpr long kStaticRows = 4096;
+__device__ __align__(256) float g_static_gates[kStaticRows * kGateColumns];
+
+// Per-device set-up, with that device current: resolve the array's device
+// address (a host-side name of a __device__ array is not a device address)
+// and set the kernels' launch attributes.
+int static_setup(int device, float **gates)
+{
+    static std::mutex mu;
+    static float *addr[64] = {};
+    if (device < 0 || device >= 64)
+        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: device %d out of range", device);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[device]) {
+        cudaDeviceProp prop;
+        int st = cuda_status(cudaGetDeviceProperties(&prop, device), "device properties");
+        if (st != LSTM_OK)
+            return st;
+        if (prop.major != 10 || prop.minor != 3)
+            return fail(LSTM_E_DEVICE, "device %d is compute capability %d.%d; the kernels are built for 10.3",
+                        device, prop.major, prop.minor);
+        if ((st = projection_prepare(device)) != LSTM_OK || (st = recurrence_prepare(device)) != LSTM_OK)
+            return st;
+        void *p = nullptr;
+        st = cuda_status(cudaGetSymbolAddress(&p, g_static_gates), "static gate buffer address");
+        if (st != LSTM_OK)
+            return st;
+        addr[device] = static_cast<float *>(p);
+    }
+    *gates = addr[device];
+    return LSTM_OK;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+}
+
+}  // namespace
+}  // namespace lstm
+
+using namespace lstm;
+
+extern "C" int lstm_layer_forward_static(const float *x, int batch, int steps, int in_width,
+                                         const float *wp_hi, const float *wp_lo, int kp,
+                                         const float *rp, const float *bias, float *y,
+                                         void *stream)
+{
+    if (!x || !wp_hi || !wp_lo || !rp || !bias || !y)
+        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: null pointer");
+    if (batch <= 0 || steps <= 0)
+        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: batch %d, steps %d must be positive",
+                    batch, steps);
+    const long rows = static_cast<long>(batch) * steps;
+    if (rows > kStaticRows)
+        return fail(LSTM_E_INVALID,
+                    "lstm_layer_forward_static: %d windows x %d steps = %ld rows exceed the static "
+                    "gate buffer's %ld rows; use lstm_projection/lstm_recurrence with your own buffer",
+                    batch, steps, rows, kStaticRows);
+    if (in_width <= 0 || in_width > kp || kp % 32 != 0)
+        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: in_width %d, kp %d", in_width, kp);
+    if (!aligned16(x) || !aligned16(wp_hi) || !aligned16(wp_lo) || !aligned16(rp) || !aligned16(y))
+        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: device pointers must be 16-byte aligned");
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, x) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: x is not known to CUDA");
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: x is not device memory");
+    int current = -1;
+    int st = cuda_status(cudaGetDevice(&current), "current device");
+    if (st != LSTM_OK)
+        return st;
+    if (attr.device != current)
+        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: x is on device %d, current device is %d",
+                    attr.device, current);
+    float *gates = nullptr;
+    if ((st = static_setup(current, &gates)) != LSTM_OK)
+        return st;
+    unsigned *fault = fault_word();
+    if (!fault)
+        return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
+    CUtensorMap xm, hm, lm;
+    if ((st = encode_matrix_map(&xm, x, rows, in_width, 128)) ||
+        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, 256)) ||
+        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, 256)))
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = launch_projection(xm, hm, lm, gates, static_cast<int>(rows), kp, fault, s)))
+        return st;
+    if ((st = launch_recurrence(gates, rp, bias, y, batch, steps, 0, fault, s)))
+        return st;
+    return launch_recurrence(gates, rp + kGates * kHidden, bias + kGates, y, batch, steps, 1, fault,
+                             s);
+}

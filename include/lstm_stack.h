@@ -204,6 +204,32 @@ int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
 int lstm_recurrence_max_clusters(int cluster_size, int windows_per_lane,
                                  int device, int *max_clusters);
 
+/* One bidirectional layer (projection, then the forward and the reverse
+ * recurrence, all on `stream`) that allocates no device memory.  The paper
+ * has no counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc -- code running under CUDA graph capture, plug-ins whose host
+ * framework owns all device memory, loops that cannot afford an
+ * allocation's implicit synchronisation.
+ *   x      : device [batch][steps][in_width]
+ *   wp_hi, wp_lo : device [1024][kp], rp : device [2][512][128],
+ *   bias   : device [2][512]   (lstm_pack_layer's outputs, uploaded by the caller)
+ *   y      : device [batch][steps][256] (forward h in columns 0..127,
+ *            reverse h in 128..255)
+ * The gate buffer between the projection and the recurrences is a fixed
+ * 16 MiB file-scope device array (4096 rows of 1024 floats) that every GPU
+ * loading the library holds until exit: batch*steps above 4096 is rejected
+ * with LSTM_E_INVALID.  The first call on a device resolves the array's
+ * address and sets kernel attributes, so make it before any stream
+ * capture.  All calls share the array: calls that overlap on the GPU race
+ * and must be ordered by the caller; it keeps the last call's contents, and
+ * nothing in it needs clearing (each call writes every row it reads).
+ * x must be on the current device; pointers 16-byte aligned.  Errors:
+ * LSTM_E_INVALID, LSTM_E_DEVICE, LSTM_E_CUDA. */
+int lstm_layer_forward_static(const float *x, int batch, int steps,
+                              int in_width, const float *wp_hi,
+                              const float *wp_lo, int kp, const float *rp,
+                              const float *bias, float *y, void *stream);
+
 /* Reads and clears the library's device fault word on the current device
  * (set by a kernel whose bounded wait ran out; 0 = none).  Synchronises the
  * device. */
