@@ -63,6 +63,23 @@ def peaks():
         return dict(FALLBACK), "fallback"
 
 
+def ncu_traffic(kernel: str, rows: int):
+    """DRAM bytes per launch from the committed ncu capture of `kernel`, scaled
+    to `rows` rows (the kernels' traffic grows in proportion to the rows they
+    process); None when the kernel's source changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as fh:
+            rec = json.load(fh)[kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as fh:
+            sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+    except (OSError, KeyError, ValueError):
+        return None
+    if sha != rec["sha256_16"]:
+        return None
+    return (rec["dram_read_bytes"] + rec["dram_write_bytes"]) * rows / rec["rows"]
+
+
 def flops_projection(rows: int) -> float:
     """Algorithmic flops of the four projections: 2 * rows * 1024 * K_l."""
     return sum(2.0 * rows * 1024 * (60 if l == 0 else 256) for l in range(LAYERS))
@@ -336,13 +353,15 @@ def run_ours(args):
                       "recurrence_rev": [round(float(v), 4) for v in phases[:, 2]]},
         "roofline": {"kernel": "recurrence (one direction, one layer)", "bound": "alu",
                      "achieved": rec_achieved, "peak": fp32_peak_tflops, "unit": "TFLOP/s",
-                     "frac": rec_achieved / fp32_peak_tflops, "traffic": None,
+                     "frac": rec_achieved / fp32_peak_tflops,
+                     "traffic": ncu_traffic("recurrence", wl.batch * wl.steps),
+                     "algorithmic_bytes": float(wl.batch * wl.steps * (512 + 128) * 4),
                      "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock",
                      "us_per_step": rec_us_per_step},
         "roofline_projection": {"kernel": "projection (one layer, both directions)",
                                 "bound": "tensor", "achieved": proj_achieved, "peak": proj_peak,
                                 "unit": "TFLOP/s", "frac": proj_achieved / proj_peak,
-                                "traffic": None,
+                                "traffic": ncu_traffic("projection", wl.batch * wl.steps),
                                 "peak_source": f"{peak_kind} bf16 burst {p['bf16_tflops']} x "
                                                f"{NOMINAL_TF32_TFLOPS}/{NOMINAL_BF16_TFLOPS} "
                                                f"(TF32) / 3 (3xTF32)"},
