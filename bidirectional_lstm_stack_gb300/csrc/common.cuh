@@ -40,7 +40,7 @@ unsigned *fault_word();
 
 // ---- projection (projection.cu) ------------------------------------------
 // Encodes the tensor map of a row-major fp32 matrix [rows][cols] read in
-// boxes of 32 columns x box_rows rows with the 128-byte swizzle.
+// boxes of 16 columns x box_rows rows with the 64-byte swizzle.
 int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols,
                       int box_rows);
 // G[rows][1024] = X . Wp^T in 3xTF32; the maps come from encode_matrix_map

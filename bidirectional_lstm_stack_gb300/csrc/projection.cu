@@ -5,22 +5,25 @@
 // `InputProjection::enqueue`), with the gate columns already in the packed,
 // unit-interleaved order (the packer reorders W's rows).
 //
-// Design (sm_103a):
-//  * one CTA computes a 128 x 256 tile of G; K advances in blocks of 32 fp32
-//    (128 bytes, one 128-byte-swizzle row), double-buffered;
-//  * a TMA producer warp loads the X block and the two TF32 planes of Wp
-//    (hi and lo, split on the host) into 128B-swizzled shared memory;
-//  * four converter warps split the X block in place into its TF32 hi part
-//    and a second buffer with the TF32 lo remainder;
-//  * one thread issues tcgen05.mma kind::tf32 (M=128, N=256, K=8) into a
-//    tensor-memory accumulator: x_hi*w_hi + x_hi*w_lo + x_lo*w_hi, i.e. the
-//    3xTF32 split that keeps fp32-level accuracy (the TF32 tensor fragments
-//    of the pages' `spk_lstm_projection_tf32` were not accurate enough on
-//    some parts, per `tf32_projection_accurate`);
-//  * the converter warps then read the accumulator with tcgen05.ld and store
-//    the rows of G.
+// Design (sm_103a), a persistent kernel, one CTA per SM:
+//  * a CTA walks 128 x 256 tiles of G (tile t: rows 128*(t/4), gate columns
+//    256*(t%4), so the CTAs running together share their X rows in L2);
+//  * K advances in blocks of 16 fp32 (64 bytes, 64-byte swizzle) through a
+//    4-stage shared-memory ring (48 KiB per stage);
+//  * warp 8 (TMA producer) loads the X block and the TF32 hi and lo planes of
+//    Wp (split on the host) into the ring;
+//  * warps 0-3 split the X block in place into its TF32 hi part and a second
+//    buffer with the TF32 lo remainder;
+//  * one thread of warp 9 issues tcgen05.mma kind::tf32 (M=128, N=256, K=8)
+//    into one of two tensor-memory accumulators (2 x 256 columns):
+//    x_hi*w_hi + x_hi*w_lo + x_lo*w_hi, the 3xTF32 split that keeps fp32-level
+//    accuracy (TF32 alone was not accurate enough on some parts, per the
+//    pages' `tf32_projection_accurate`);
+//  * warps 4-7 (epilogue) read a finished accumulator with tcgen05.ld and
+//    store rows of G while the MMA fills the other accumulator.
 // Every mbarrier wait is bounded in time; a wait that runs out sets a bit in
-// the fault word and the CTA drains and returns.
+// the fault word, every role stops, and the CTA drains its TMA loads and MMAs
+// before it frees tensor memory and returns.
 #include <cudaTypedefs.h>
 #include <mutex>
 
@@ -29,29 +32,34 @@
 namespace lstm {
 namespace {
 
-constexpr int BM = 128;  // rows of G per CTA (MMA M)
-constexpr int BN = 256;  // gate columns per CTA (MMA N)
-constexpr int BK = 32;   // fp32 per K block = 128 bytes
-constexpr int STAGES = 2;
-constexpr int A_BYTES = BM * BK * 4;                     // 16 KiB
-constexpr int B_BYTES = BN * BK * 4;                     // 32 KiB
+constexpr int BM = 128;  // rows of G per tile (MMA M)
+constexpr int BN = 256;  // gate columns per tile (MMA N)
+constexpr int BK = 16;   // fp32 per K block = 64 bytes
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 4;                     // 8 KiB
+constexpr int B_BYTES = BN * BK * 4;                     // 16 KiB
 constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // A hi, A lo, B hi, B lo
 constexpr uint32_t TX_BYTES = A_BYTES + 2 * B_BYTES;     // what TMA writes per stage
-constexpr uint32_t TMEM_COLS = BN;                       // fp32 accumulator columns
-constexpr int THREADS = 192;  // warps 0-3 convert + epilogue, 4 TMA, 5 MMA
-constexpr int CONVERTERS = 128;
+constexpr uint32_t ACC_COLS = BN;                        // fp32 columns per accumulator
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;             // two accumulators
+constexpr int CONVERTERS = 128;                          // warps 0-3
+constexpr int EPILOGUE = 128;                            // warps 4-7
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int THREADS = 320;
 constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+constexpr int TILES_N = kGateColumns / BN;          // 4
 
-// tcgen05 shared-memory matrix descriptor: K-major operand, 128-byte
-// swizzle, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr)
+// tcgen05 shared-memory matrix descriptor: K-major operand, 64-byte
+// swizzle, 8-row groups 512 bytes apart.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t addr)
 {
     return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
-           (static_cast<uint64_t>(1) << 16) |            // leading offset (unused, swizzled K-major)
-           (static_cast<uint64_t>(1024 >> 4) << 32) |    // stride offset: 8 rows x 128 B
-           (static_cast<uint64_t>(1) << 46) |            // descriptor version (tcgen05)
-           (static_cast<uint64_t>(2) << 61);             // 128-byte swizzle
+           (static_cast<uint64_t>(1) << 16) |           // leading offset (unused, swizzled K-major)
+           (static_cast<uint64_t>(512 >> 4) << 32) |    // stride offset: 8 rows x 64 B
+           (static_cast<uint64_t>(1) << 46) |           // descriptor version (tcgen05)
+           (static_cast<uint64_t>(4) << 61);            // 64-byte swizzle
 }
 
 // Instruction descriptor, kind::tf32: D fp32, A and B TF32, both K-major,
@@ -93,7 +101,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 projection_kernel(const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap whi_map,
                   const __grid_constant__ CUtensorMap wlo_map, float *__restrict__ g, int rows,
-                  int kblocks, unsigned *fault)
+                  int kblocks, int tiles, unsigned *fault)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -101,14 +109,13 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
     uint64_t *conv = full + STAGES;
     uint64_t *empty = conv + STAGES;
-    uint64_t *acc_full = empty + STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    uint64_t *acc_full = empty + STAGES;      // [2]
+    uint64_t *acc_empty = acc_full + 2;       // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BN;
-    const int m0 = blockIdx.y * BM;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -116,16 +123,19 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             ptx::mbar_init(&conv[s], CONVERTERS);
             ptx::mbar_init(&empty[s], 1);
         }
-        ptx::mbar_init(acc_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&acc_full[a], 1);
+            ptx::mbar_init(&acc_empty[a], EPILOGUE);
+        }
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == PRODUCER_WARP && lane == 0) {
         ptx::prefetch_tensormap(&x_map);
         ptx::prefetch_tensormap(&whi_map);
         ptx::prefetch_tensormap(&wlo_map);
     }
-    if (warp == 5) {
+    if (warp == MMA_WARP) {
         ptx::tmem_alloc(tmem_slot, TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -133,109 +143,152 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    int issued = 0;  // producer: K blocks whose loads were issued
+    long issued = 0;            // producer: K blocks whose loads were issued
+    int committed_tiles = 0;    // MMA: accumulators committed
 
-    if (warp == 4) {
+    if (warp == PRODUCER_WARP) {
         if (lane == 0) {
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t n = kb / STAGES;
-                if (n > 0 && !ptx::mbar_wait_bounded(&empty[s], (n - 1) & 1, abort_flag, fault,
-                                                     kFaultProducer, WAIT_LIMIT_NS))
-                    break;
-                uint8_t *st = smem + s * STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(&full[s], TX_BYTES);
-                ptx::tma_load_2d(st, &x_map, &full[s], kb * BK, m0);
-                ptx::tma_load_2d(st + 2 * A_BYTES, &whi_map, &full[s], kb * BK, n0);
-                ptx::tma_load_2d(st + 2 * A_BYTES + B_BYTES, &wlo_map, &full[s], kb * BK, n0);
-                issued = kb + 1;
+            long kbi = 0;
+            for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+                const int m0 = (t / TILES_N) * BM;
+                const int n0 = (t % TILES_N) * BN;
+                for (int kb = 0; kb < kblocks; ++kb, ++kbi) {
+                    const int s = static_cast<int>(kbi % STAGES);
+                    const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
+                    if (n > 0 && !ptx::mbar_wait_bounded(&empty[s], (n - 1) & 1, abort_flag, fault,
+                                                         kFaultProducer, WAIT_LIMIT_NS))
+                        break;
+                    uint8_t *st = smem + s * STAGE_BYTES;
+                    ptx::mbar_arrive_expect_tx(&full[s], TX_BYTES);
+                    ptx::tma_load_2d(st, &x_map, &full[s], kb * BK, m0);
+                    ptx::tma_load_2d(st + 2 * A_BYTES, &whi_map, &full[s], kb * BK, n0);
+                    ptx::tma_load_2d(st + 2 * A_BYTES + B_BYTES, &wlo_map, &full[s], kb * BK, n0);
+                    issued = kbi + 1;
+                }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == MMA_WARP) {
         if (lane == 0) {
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t n = kb / STAGES;
-                if (!ptx::mbar_wait_bounded(&conv[s], n & 1, abort_flag, fault, kFaultMma,
-                                            WAIT_LIMIT_NS))
+            long kbi = 0;
+            int ti = 0;
+            for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++ti) {
+                const int a = ti & 1;
+                const uint32_t use = static_cast<uint32_t>(ti >> 1);
+                if (use > 0 && !ptx::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, abort_flag,
+                                                       fault, kFaultMma, WAIT_LIMIT_NS))
                     break;
                 ptx::tc_fence_after();
-                const uint32_t a_hi = ptx::smem_u32(smem + s * STAGE_BYTES);
-                const uint32_t a_lo = a_hi + A_BYTES;
-                const uint32_t b_hi = a_hi + 2 * A_BYTES;
-                const uint32_t b_lo = b_hi + B_BYTES;
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(a) * ACC_COLS;
+                bool ok = true;
+                for (int kb = 0; kb < kblocks; ++kb, ++kbi) {
+                    const int s = static_cast<int>(kbi % STAGES);
+                    const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
+                    if (!ptx::mbar_wait_bounded(&conv[s], n & 1, abort_flag, fault, kFaultMma,
+                                                WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_hi = ptx::smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t a_lo = a_hi + A_BYTES;
+                    const uint32_t b_hi = a_hi + 2 * A_BYTES;
+                    const uint32_t b_lo = b_hi + B_BYTES;
 #pragma unroll
-                for (int j = 0; j < BK / 8; ++j) {
-                    const uint32_t off = j * 32;  // 8 TF32 = 32 bytes along K
-                    ptx::mma_tf32(tmem, sw128_desc(a_hi + off), sw128_desc(b_hi + off), IDESC,
-                                  (kb | j) != 0);
-                    ptx::mma_tf32(tmem, sw128_desc(a_hi + off), sw128_desc(b_lo + off), IDESC, 1);
-                    ptx::mma_tf32(tmem, sw128_desc(a_lo + off), sw128_desc(b_hi + off), IDESC, 1);
+                    for (int j = 0; j < BK / 8; ++j) {
+                        const uint32_t off = j * 32;  // 8 TF32 = 32 bytes along K
+                        ptx::mma_tf32(d_tmem, sw64_desc(a_hi + off), sw64_desc(b_hi + off), IDESC,
+                                      (kb | j) != 0);
+                        ptx::mma_tf32(d_tmem, sw64_desc(a_hi + off), sw64_desc(b_lo + off), IDESC, 1);
+                        ptx::mma_tf32(d_tmem, sw64_desc(a_lo + off), sw64_desc(b_hi + off), IDESC, 1);
+                    }
+                    ptx::mma_commit(&empty[s]);
                 }
-                ptx::mma_commit(&empty[s]);
+                ptx::mma_commit(&acc_full[a]);  // also when stopping early: frees the epilogue
+                committed_tiles = ti + 1;
+                if (!ok)
+                    break;
             }
-            ptx::mma_commit(acc_full);
+        }
+    } else if (warp < 4) {
+        // converters: split X into TF32 hi (in place) and lo
+        const int tid = threadIdx.x;
+        long kbi = 0;
+        for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+            bool ok = true;
+            for (int kb = 0; kb < kblocks; ++kb, ++kbi) {
+                const int s = static_cast<int>(kbi % STAGES);
+                const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
+                if (!ptx::mbar_wait_bounded(&full[s], n & 1, abort_flag, fault, kFaultConverter,
+                                            WAIT_LIMIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                float4 *a = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES);
+                float4 *alo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + A_BYTES);
+#pragma unroll
+                for (int i = 0; i < A_BYTES / 16 / CONVERTERS; ++i) {
+                    const int idx = tid + i * CONVERTERS;
+                    float4 hi, lo;
+                    split4(a[idx], hi, lo);
+                    a[idx] = hi;
+                    alo[idx] = lo;
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(&conv[s]);
+            }
+            if (!ok)
+                break;
         }
     } else {
-        // warps 0-3: split X into TF32 hi/lo, then the epilogue
-        const int tid = threadIdx.x;
-        bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t n = kb / STAGES;
-            if (!ptx::mbar_wait_bounded(&full[s], n & 1, abort_flag, fault, kFaultConverter,
-                                        WAIT_LIMIT_NS)) {
-                ok = false;
+        // epilogue: warp 4+q reads TMEM lanes 32q .. 32q+31 (warp id mod 4 = q)
+        const int q = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        int ti = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++ti) {
+            const int a = ti & 1;
+            const uint32_t use = static_cast<uint32_t>(ti >> 1);
+            bool got = ptx::mbar_wait_bounded(&acc_full[a], use & 1, abort_flag, fault,
+                                              kFaultEpilogue, WAIT_LIMIT_NS);
+            // tcgen05.ld is warp-collective: continue only if every lane may
+            if (!__all_sync(0xffffffffu, got) || *abort_flag)
                 break;
-            }
-            float4 *a = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES);
-            float4 *alo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + A_BYTES);
-#pragma unroll
-            for (int i = 0; i < A_BYTES / 16 / CONVERTERS; ++i) {
-                const int idx = tid + i * CONVERTERS;
-                float4 hi, lo;
-                split4(a[idx], hi, lo);
-                a[idx] = hi;
-                alo[idx] = lo;
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&conv[s]);
-        }
-        bool got = ok && ptx::mbar_wait_bounded(acc_full, 0, abort_flag, fault, kFaultEpilogue,
-                                                WAIT_LIMIT_NS);
-        // tcgen05.ld is warp-collective: take the epilogue only if every lane may
-        if (__all_sync(0xffffffffu, got)) {
             ptx::tc_fence_after();
-            const int row = warp * 32 + lane;
-            const long m = static_cast<long>(m0) + row;
-            const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+            const int m0 = (t / TILES_N) * BM;
+            const int n0 = (t % TILES_N) * BN;
+            const long m = static_cast<long>(m0) + q * 32 + lane;
+            const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(a) * ACC_COLS;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(tmem + lane_base + c * 32, r);
+                ptx::tmem_ld_32x32b_x32(acc + c * 32, r);
                 ptx::tmem_ld_wait();
                 if (m < rows) {
                     float4 *dst = reinterpret_cast<float4 *>(g + m * kGateColumns + n0 + c * 32);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                             __uint_as_float(r[4 * q + 2]),
-                                             __uint_as_float(r[4 * q + 3]));
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                             __uint_as_float(r[4 * v + 2]),
+                                             __uint_as_float(r[4 * v + 3]));
                 }
             }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&acc_empty[a]);
         }
     }
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 4 && lane == 0) {
+    if (warp == PRODUCER_WARP && lane == 0) {
         // every issued TMA load has landed before the CTA's shared memory goes away
-        for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
-            drain_wait(&full[kb % STAGES], (kb / STAGES) & 1, fault);
+        for (long kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
+            drain_wait(&full[kb % STAGES], static_cast<uint32_t>(kb / STAGES) & 1, fault);
     }
-    if (warp == 5) {
-        if (lane == 0)
-            drain_wait(acc_full, 0, fault);  // every MMA has completed
+    if (warp == MMA_WARP) {
+        if (lane == 0) {
+            // every MMA has completed before tensor memory is freed
+            for (int ti = committed_tiles - 2 < 0 ? 0 : committed_tiles - 2; ti < committed_tiles; ++ti)
+                drain_wait(&acc_full[ti & 1], static_cast<uint32_t>(ti >> 1) & 1, fault);
+        }
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
@@ -257,6 +310,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+int g_sm_count[64] = {};
+
 } // namespace
 
 int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols, int box_rows)
@@ -274,7 +329,7 @@ int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols, 
     cuuint32_t estr[2] = {1, 1};
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(LSTM_E_CUDA, "cuTensorMapEncodeTiled failed (%d) for %ld x %d", (int)r, rows,
@@ -282,8 +337,16 @@ int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols, 
     return LSTM_OK;
 }
 
-int projection_prepare(int)
+int projection_prepare(int device)
 {
+    if (device < 0 || device >= 64)
+        return fail(LSTM_E_INVALID, "device %d out of range", device);
+    int sms = 0;
+    int st = cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
+                         "SM count");
+    if (st != LSTM_OK)
+        return st;
+    g_sm_count[device] = sms;
     return cuda_status(cudaFuncSetAttribute(projection_kernel,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(SMEM_BYTES)),
@@ -294,14 +357,20 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
                       const CUtensorMap &wlo_map, float *g, int rows, int kp, unsigned *fault,
                       cudaStream_t stream)
 {
-    if (rows <= 0 || kp <= 0 || kp % BK != 0)
+    if (rows <= 0 || kp <= 0 || kp % 32 != 0)
         return fail(LSTM_E_INVALID, "projection: rows %d, kp %d", rows, kp);
     const long mtiles = (static_cast<long>(rows) + BM - 1) / BM;
-    if (mtiles > 65535)
-        return fail(LSTM_E_OVERFLOW, "projection: %d rows exceed %d", rows, 65535 * BM);
-    dim3 grid(kGateColumns / BN, static_cast<unsigned>(mtiles));
+    const long tiles = mtiles * TILES_N;
+    if (tiles > 0x7fffffffL)
+        return fail(LSTM_E_OVERFLOW, "projection: %d rows", rows);
+    int dev = 0;
+    int st = cuda_status(cudaGetDevice(&dev), "current device");
+    if (st != LSTM_OK)
+        return st;
+    const int sms = (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) ? g_sm_count[dev] : 148;
+    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
     projection_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(x_map, whi_map, wlo_map, g, rows,
-                                                             kp / BK, fault);
+                                                             kp / BK, static_cast<int>(tiles), fault);
     return cuda_status(cudaGetLastError(), "projection launch");
 }
 
