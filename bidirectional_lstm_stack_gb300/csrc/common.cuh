@@ -56,9 +56,10 @@ int launch_recurrence(const float *g, const float *rp, const float *bias,
                       unsigned *fault, cudaStream_t stream);
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias,
                               float *y, int batch, int steps, int direction,
-                              int cluster, int nw, unsigned *fault, cudaStream_t stream);
-// Clusters of a variant the device can hold at once (0 if unknown variant).
-int recurrence_max_clusters(int cluster, int nw, int *out);
+                              int cluster, int nw, int nch, unsigned *fault,
+                              cudaStream_t stream);
+// Clusters of a variant the device can hold at once.
+int recurrence_max_clusters(int cluster, int nw, int nch, int *out);
 int recurrence_prepare(int device);
 
 } // namespace lstm
@@ -256,10 +257,12 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
 __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c,
                                             float d, uint32_t remote_bar)
 {
+    // No "memory" clobber: the pushed buffer is read only after a wait on
+    // its mbarrier, and that wait is the compiler barrier; leaving this store
+    // unordered lets independent work be scheduled around it.
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      remote_addr),
-                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-                 : "memory");
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar));
 }
 // try_wait with acquire semantics at cluster scope (pairs with the
 // transaction credit of st.async from peer CTAs).

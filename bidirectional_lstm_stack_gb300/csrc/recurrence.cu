@@ -39,12 +39,20 @@
 // variants give bitwise-identical results.
 #include <stdio.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace lstm {
 namespace {
 
-constexpr int THREADS = 256;
+// Threads per CTA: 256 (8 warps); clusters of 2 use 512 so that a CTA's
+// half of R (64 units) still fits in registers at 64 per thread.
+template <int C>
+constexpr int threads_for()
+{
+    return C == 2 ? 512 : 256;
+}
 constexpr int KC = 8;                 // K chunks = lanes per reduction group
 constexpr int KLEN = 16;              // columns per chunk
 constexpr int CHUNK_STRIDE = 20;      // padded chunk stride (conflict-free LDS.128)
@@ -76,19 +84,22 @@ __device__ __forceinline__ void reduce_level(const float (&in)[N], float (&out)[
     }
 }
 
-template <int C, int NW>
+template <int C, int NW, int NCH = 1, int THREADS = threads_for<C>()>
 __global__ void __launch_bounds__(THREADS, 1)
 recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                   const float *__restrict__ bias, float *__restrict__ y, int batch, int steps,
                   int direction, unsigned *fault)
 {
     constexpr int U = kHidden / C;       // units per CTA
-    constexpr int SPU = 32 / U;          // slots per unit
-    constexpr int TW = SPU * NW;         // windows per tile (per cluster)
-    constexpr int V = 4 * NW;            // partial sums per thread
+    constexpr int SLOTS = THREADS / 8;   // 8-lane groups per CTA
+    constexpr int SPU = SLOTS / U;       // slots per unit
+    constexpr int LW = NW * NCH;         // windows per slot: NCH chunks of NW
+    constexpr int TW = SPU * LW;         // windows per tile (per cluster)
+    constexpr int V = 4 * NW;            // partial sums per thread and chunk
     constexpr int HV = V >= 8 ? V / 8 : 1;  // values a lane holds after the reduction
     constexpr int REPL = V >= 8 ? 4 / HV : 8;  // lanes holding one window's cell
-    static_assert(U * SPU == 32 && C * U == kHidden, "cluster shape");
+    constexpr int PFD = NCH >= 4 ? 2 : PF;     // projection prefetch depth (steps)
+    static_assert(U * SPU == SLOTS && C * U == kHidden && U % 4 == 0, "cluster shape");
 
     __shared__ __align__(16) float hbuf[2][TW][HROW];
     __shared__ __align__(8) uint64_t hbar[2];
@@ -104,7 +115,7 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     const uint32_t rank = ptx::cluster_ctarank();
     const int tile = static_cast<int>(ptx::cluster_id_x());
     const int u = static_cast<int>(rank) * U + ul;  // this thread's hidden unit
-    const int win0 = tile * TW + wg * NW;           // this thread's first window
+    const int wbase = wg * LW;                      // this slot's first window in the tile
     const int u0 = u & ~3;                          // first of the warp's four units
     // windows of this tile inside the batch; padding windows are computed but
     // their h is neither sent nor stored
@@ -122,36 +133,29 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             r2[q][i] = src[i];
     }
 
-    // the values this lane holds after the reduction: index idx = w*4 + gate
+    // The values this lane holds after each chunk's reduction: index
+    // idx = w*4 + gate within the chunk (the same for every chunk).
     // Activations are branch-free across the lanes (which hold different
     // gates): act = m * s(m * z) + a with (m, a) = (2, -1) for the cell
     // candidate, i.e. tanh(z) = 2 s(2z) - 1, and (1, 0) for the gates.
-    float act_m[HV], act_a[HV];
-    float bias_v[HV];
-    const float *gsrc[HV];
-    bool gvalid[HV];
+    float act_m[HV], act_a[HV], bias_v[HV];
+    int wv[HV];
+    const float *gcol[HV];
 #pragma unroll
     for (int v = 0; v < HV; ++v) {
         const int idx = V >= 8 ? kc * HV + v : (kc >> 1);
-        const int w = idx >> 2, q = idx & 3;
-        const int b = win0 + w;
+        const int q = idx & 3;
+        wv[v] = idx >> 2;
         bias_v[v] = bias[4 * u + q];
         act_m[v] = q == 2 ? 2.0f : 1.0f;
         act_a[v] = q == 2 ? -1.0f : 0.0f;
-        gvalid[v] = b < batch;
-        gsrc[v] = g + (gvalid[v] ? static_cast<long>(b) * steps * kGateColumns : 0) +
-                  direction * kGates + 4 * u + q;
+        gcol[v] = g + direction * kGates + 4 * u + q;
     }
-    // the window whose cell this lane updates; after the gather below, the
-    // 4*REPL lanes of the warp that hold it share the sends to the C CTAs
+    // the window (within a chunk) whose cell this lane updates; after the
+    // gather below, the 4*REPL lanes of the warp that hold it share the sends
+    // to the C CTAs
     const int wl = V >= 8 ? (kc * HV) / 4 : 0;
     const int sender = (tid & 31) / 8 * REPL + kc % REPL;  // 0 .. 4*REPL-1
-    const int bcell = win0 + wl;
-    const bool cell_valid = bcell < batch;
-    float *ycol = y + (cell_valid ? static_cast<long>(bcell) * steps * kOutput : 0) +
-                  direction * kHidden + u0;
-    const uint32_t hsend_off = static_cast<uint32_t>(
-        ((wg * NW + wl) * HROW + (u0 / KLEN) * CHUNK_STRIDE + (u0 % KLEN)) * 4);
 
     // h_{-1} = 0 in buffer 0; buffer 1 is zeroed too, so padding windows
     // (never sent) only ever see zeros
@@ -174,26 +178,47 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
 
     const uint32_t hbase = ptx::smem_u32(&hbuf[0][0][0]);
     const uint32_t bar_base = ptx::smem_u32(&hbar[0]);
-    float gq[PF][HV];
-    auto gload = [&](int s, float (&dst)[HV]) {
-        const int t = direction ? steps - 1 - s : s;
+    const int tile_w0 = tile * TW;
+    // chunk 0's projection column and output row; chunk ch is ch*NW windows on
+    const long row_stride = static_cast<long>(NW) * steps;  // rows between chunks
+    const float *gch0[HV];
 #pragma unroll
-        for (int v = 0; v < HV; ++v)
-            dst[v] = (gvalid[v] && s < steps) ? __ldg(gsrc[v] + static_cast<long>(t) * kGateColumns)
-                                              : 0.0f;
+    for (int v = 0; v < HV; ++v)
+        gch0[v] = gcol[v] + static_cast<long>(tile_w0 + wbase + wv[v]) * steps * kGateColumns;
+    float *ych0 = y + static_cast<long>(tile_w0 + wbase + wl) * steps * kOutput +
+                  direction * kHidden + u0;
+    const int bch0 = tile_w0 + wbase;  // window of chunk 0, w = 0
+    const uint32_t send_off0 = static_cast<uint32_t>(
+        ((wbase + wl) * HROW + (u0 / KLEN) * CHUNK_STRIDE + (u0 % KLEN)) * 4);
+
+    float gq[PFD][NCH][HV];
+    auto gload = [&](int s, float (&dst)[NCH][HV]) {
+        const long t = direction ? steps - 1 - s : s;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+#pragma unroll
+            for (int v = 0; v < HV; ++v) {
+                const bool ok = bch0 + ch * NW + wv[v] < batch && s < steps;
+                dst[ch][v] = ok ? __ldg(gch0[v] + (ch * row_stride + t) * kGateColumns) : 0.0f;
+            }
+        }
     };
 #pragma unroll
-    for (int p = 0; p < PF; ++p)
+    for (int p = 0; p < PFD; ++p)
         gload(p, gq[p]);
 
-    float c = 0.0f;
-    for (int s0 = 0; s0 < steps; s0 += PF) {
+    float c[NCH];
 #pragma unroll
-        for (int p = 0; p < PF; ++p) {
+    for (int ch = 0; ch < NCH; ++ch)
+        c[ch] = 0.0f;
+    for (int s0 = 0; s0 < steps; s0 += PFD) {
+#pragma unroll
+        for (int p = 0; p < PFD; ++p) {
             const int s = s0 + p;
             if (s >= steps)
                 break;
             const int par = s & 1;
+            const int t = direction ? steps - 1 - s : s;
 
             // 0. h_{s-1} complete in buffer `par`
             if (s > 0) {
@@ -216,80 +241,98 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                     ptx::mbar_arrive_expect_tx(&hbar[par], step_bytes);
             }
 
+            // The chunks are independent: each phase below runs over all of
+            // them, so their latencies overlap.
             // 1. partial dot products over this lane's K chunk
-            float part[V];
+            float part[NCH][V];
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float4 *hp =
-                    reinterpret_cast<const float4 *>(&hbuf[par][wg * NW + w][kc * CHUNK_STRIDE]);
-                const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
-                const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y}, {h1.z, h1.w},
-                                      {h2.x, h2.y}, {h2.z, h2.w}, {h3.x, h3.y}, {h3.z, h3.w}};
+            for (int ch = 0; ch < NCH; ++ch) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float2 acc = make_float2(0.0f, 0.0f);
+                for (int w = 0; w < NW; ++w) {
+                    const float4 *hp = reinterpret_cast<const float4 *>(
+                        &hbuf[par][wbase + ch * NW + w][kc * CHUNK_STRIDE]);
+                    const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+                    const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y},
+                                          {h1.z, h1.w}, {h2.x, h2.y}, {h2.z, h2.w},
+                                          {h3.x, h3.y}, {h3.z, h3.w}};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        acc = __ffma2_rn(r2[q][i], hh[i], acc);
-                    part[w * 4 + q] = acc.x + acc.y;
+                    for (int q = 0; q < 4; ++q) {
+                        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            acc = __ffma2_rn(r2[q][i], hh[i], acc);
+                        part[ch][w * 4 + q] = acc.x + acc.y;
+                    }
                 }
             }
 
             // 2. fixed butterfly over the 8 K-chunk lanes
-            float held[HV];
-            if constexpr (V >= 8) {
-                float a[V / 2], b2[V / 4];
-                reduce_level<V>(part, a, 4, (kc & 4) != 0);
-                reduce_level<V / 2>(a, b2, 2, (kc & 2) != 0);
-                reduce_level<V / 4>(b2, held, 1, (kc & 1) != 0);
-            } else {
-                float a[2], b2[1];
-                reduce_level<4>(part, a, 4, (kc & 4) != 0);
-                reduce_level<2>(a, b2, 2, (kc & 2) != 0);
-                held[0] = b2[0] + __shfl_xor_sync(0xffffffffu, b2[0], 1);
-            }
-
-            // 3. activations, gate gather, cell update
-            float act[HV];
+            float held[NCH][HV];
 #pragma unroll
-            for (int v = 0; v < HV; ++v) {
-                const float z = held[v] + (gq[p][v] + bias_v[v]);
-                act[v] = fmaf(act_m[v], sigmoid_bounded(act_m[v] * z), act_a[v]);
-            }
-            float gate[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int src = V >= 8 ? (4 * wl + q) / HV : 2 * q;
-                gate[q] = __shfl_sync(0xffffffffu, act[q % HV], src, 8);
-            }
-            c = gate[1] * c + gate[0] * gate[2];
-            const float h = gate[3] * tanh_bounded(c);
-
-            // 4. gather the warp's four units of window wl, store them to y and
-            //    push them (16 bytes) into every CTA's next h buffer
-            float h4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                h4[j] = __shfl_sync(0xffffffffu, h, 8 * j + kc);
-            const int t = direction ? steps - 1 - s : s;
-            if (sender == 0 && cell_valid)
-                *reinterpret_cast<float4 *>(ycol + static_cast<long>(t) * kOutput) =
-                    make_float4(h4[0], h4[1], h4[2], h4[3]);
-            if (s + 1 < steps && cell_valid) {
-                const uint32_t dst =
-                    hbase + static_cast<uint32_t>((par ^ 1) * TW * HROW * 4) + hsend_off;
-                const uint32_t bar = bar_base + static_cast<uint32_t>((par ^ 1) * 8);
-#pragma unroll
-                for (int r = 0; r < (C + 4 * REPL - 1) / (4 * REPL); ++r) {
-                    const int peer = sender + r * 4 * REPL;
-                    if (peer < C)
-                        ptx::st_async_v4(ptx::map_to_rank(dst, peer), h4[0], h4[1], h4[2], h4[3],
-                                         ptx::map_to_rank(bar, peer));
+            for (int ch = 0; ch < NCH; ++ch) {
+                if constexpr (V >= 8) {
+                    float a[V / 2], b2[V / 4];
+                    reduce_level<V>(part[ch], a, 4, (kc & 4) != 0);
+                    reduce_level<V / 2>(a, b2, 2, (kc & 2) != 0);
+                    reduce_level<V / 4>(b2, held[ch], 1, (kc & 1) != 0);
+                } else {
+                    float a[2], b2[1];
+                    reduce_level<4>(part[ch], a, 4, (kc & 4) != 0);
+                    reduce_level<2>(a, b2, 2, (kc & 2) != 0);
+                    held[ch][0] = b2[0] + __shfl_xor_sync(0xffffffffu, b2[0], 1);
                 }
             }
 
-            // 5. projection values PF steps ahead
-            gload(s + PF, gq[p]);
+            // 3. activations, gate gather, cell update
+            float h[NCH];
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                float act[HV];
+#pragma unroll
+                for (int v = 0; v < HV; ++v) {
+                    const float z = held[ch][v] + (gq[p][ch][v] + bias_v[v]);
+                    act[v] = fmaf(act_m[v], sigmoid_bounded(act_m[v] * z), act_a[v]);
+                }
+                float gate[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int src = V >= 8 ? (4 * wl + q) / HV : 2 * q;
+                    gate[q] = __shfl_sync(0xffffffffu, act[q % HV], src, 8);
+                }
+                c[ch] = gate[1] * c[ch] + gate[0] * gate[2];
+                h[ch] = gate[3] * tanh_bounded(c[ch]);
+            }
+
+            // 4. gather the warp's four units of window wl, store them to y and
+            //    push them (16 bytes) into every CTA's next h buffer
+            const uint32_t dst_par = hbase + static_cast<uint32_t>((par ^ 1) * TW * HROW * 4);
+            const uint32_t bar = bar_base + static_cast<uint32_t>((par ^ 1) * 8);
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                float h4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    h4[j] = __shfl_sync(0xffffffffu, h[ch], 8 * j + kc);
+                if (bch0 + ch * NW + wl < batch) {
+                    if (sender == 0)
+                        *reinterpret_cast<float4 *>(ych0 + (ch * row_stride + t) * kOutput) =
+                            make_float4(h4[0], h4[1], h4[2], h4[3]);
+                    if (s + 1 < steps) {
+                        const uint32_t dst =
+                            dst_par + send_off0 + static_cast<uint32_t>(ch * NW * HROW * 4);
+#pragma unroll
+                        for (int r = 0; r < (C + 4 * REPL - 1) / (4 * REPL); ++r) {
+                            const int peer = sender + r * 4 * REPL;
+                            if (peer < C)
+                                ptx::st_async_v4(ptx::map_to_rank(dst, peer), h4[0], h4[1], h4[2],
+                                                 h4[3], ptx::map_to_rank(bar, peer));
+                        }
+                    }
+                }
+            }
+
+            // 5. projection values PFD steps ahead
+            gload(s + PFD, gq[p]);
         }
     }
     // no CTA leaves while a peer may still write into its shared memory
@@ -300,43 +343,73 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
 
 struct Variant {
     int cluster;
-    int nw;
-    int tile;  // windows per cluster
+    int nw;       // windows per chunk
+    int nch;      // chunks per lane
+    int tile;     // windows per cluster
+    int threads;  // per CTA
     const void *fn;
 };
 
-template <int C, int NW>
+template <int C, int NW, int NCH = 1>
 Variant variant()
 {
-    return Variant{C, NW, (C / 4) * NW, reinterpret_cast<const void *>(&recurrence_kernel<C, NW>)};
+    constexpr int threads = threads_for<C>();
+    return Variant{C, NW, NCH, threads / 8 / (kHidden / C) * NW * NCH, threads,
+                   reinterpret_cast<const void *>(&recurrence_kernel<C, NW, NCH>)};
 }
 
 const Variant kVariants[] = {
-    variant<16, 1>(), variant<16, 2>(), variant<16, 4>(), variant<16, 8>(),
-    variant<8, 1>(),  variant<8, 2>(),  variant<8, 4>(),  variant<8, 8>(),
+    variant<16, 1>(),   variant<16, 2>(),   variant<16, 4>(),   variant<16, 8>(),
+    variant<8, 1>(),    variant<8, 2>(),    variant<8, 4>(),    variant<8, 8>(),
+    variant<4, 1>(),    variant<4, 2>(),    variant<2, 1>(),
+    variant<4, 1, 2>(), variant<4, 1, 4>(), variant<4, 1, 8>(), variant<4, 2, 2>(),
+    variant<4, 2, 4>(), variant<4, 2, 8>(), variant<8, 2, 4>(),
 };
 
-const Variant *find_variant(int cluster, int nw)
+const Variant *find_variant(int cluster, int nw, int nch)
 {
     for (const Variant &v : kVariants)
-        if (v.cluster == cluster && v.nw == nw)
+        if (v.cluster == cluster && v.nw == nw && v.nch == nch)
             return &v;
     return nullptr;
 }
 
-// The default variant for a batch, from per-step timings of every variant
-// with both directions running (GB300, T = 589): clusters of 8 with two
-// windows each are fastest up to a few dozen windows (0.47 us/step at one
-// window, 0.65 us/step at 32, two CTAs per SM); wider tiles win once the
-// grid no longer fits one wave (batch 256: 8 windows per lane, 16 per
-// cluster).
+int max_active_clusters(const Variant &v, int *out);
+
+// The default variant for a batch.  Candidates in order of preference, from
+// per-step timings of every variant with both directions running (GB300,
+// T = 589): clusters of 4 with one window per 8-lane group (0.51 us/step from
+// 1 to 16 windows, 0.65 at 32; two CTAs per SM), then 2, 4 and 8 chunks of
+// two windows per lane (0.95 us/step at 64 windows, 1.58 at 128, 2.91 at 256).
+// The first whose clusters for both directions fit the device at once wins;
+// past that, the widest tile.
 const Variant *choose_variant(int batch)
 {
-    if (batch <= 64)
-        return find_variant(8, 1);
-    if (batch <= 128)
-        return find_variant(8, 4);
-    return find_variant(8, 8);
+    static const int order[][3] = {{4, 1, 1}, {4, 2, 2}, {4, 2, 4}, {4, 2, 8}};
+    static std::mutex mu;
+    static int fits[64][4];
+    static bool known[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        dev = -1;
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!known[dev]) {
+            for (int i = 0; i < 4; ++i) {
+                int n = 0;
+                const Variant *v = find_variant(order[i][0], order[i][1], order[i][2]);
+                fits[dev][i] = (v && max_active_clusters(*v, &n) == LSTM_OK) ? n : 0;
+            }
+            known[dev] = true;
+        }
+    }
+    for (int i = 0; i < 4; ++i) {
+        const Variant *v = find_variant(order[i][0], order[i][1], order[i][2]);
+        const long tiles = (static_cast<long>(batch) + v->tile - 1) / v->tile;
+        if (dev >= 0 && 2 * tiles <= fits[dev][i])
+            return v;
+    }
+    return find_variant(4, 2, 8);
 }
 
 int launch_variant(const Variant &v, const float *g, const float *rp, const float *bias, float *y,
@@ -348,7 +421,7 @@ int launch_variant(const Variant &v, const float *g, const float *rp, const floa
         return fail(LSTM_E_OVERFLOW, "recurrence: %d windows need %ld blocks", batch, blocks);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(static_cast<unsigned>(v.threads));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -387,25 +460,34 @@ int launch_recurrence(const float *g, const float *rp, const float *bias, float 
 }
 
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias, float *y,
-                              int batch, int steps, int direction, int cluster, int nw,
+                              int batch, int steps, int direction, int cluster, int nw, int nch,
                               unsigned *fault, cudaStream_t stream)
 {
-    const Variant *v = find_variant(cluster, nw);
+    const Variant *v = find_variant(cluster, nw, nch);
     if (!v)
-        return fail(LSTM_E_INVALID, "recurrence: no variant with cluster %d and %d windows per lane",
-                    cluster, nw);
+        return fail(LSTM_E_INVALID,
+                    "recurrence: no variant with cluster %d, %d windows per chunk, %d chunks",
+                    cluster, nw, nch);
     return launch_variant(*v, g, rp, bias, y, batch, steps, direction, fault, stream);
 }
 
-int recurrence_max_clusters(int cluster, int nw, int *out)
+int recurrence_max_clusters(int cluster, int nw, int nch, int *out)
 {
-    const Variant *v = find_variant(cluster, nw);
+    const Variant *v = find_variant(cluster, nw, nch);
     if (!v)
-        return fail(LSTM_E_INVALID, "recurrence: no variant with cluster %d and %d windows per lane",
-                    cluster, nw);
+        return fail(LSTM_E_INVALID,
+                    "recurrence: no variant with cluster %d, %d windows per chunk, %d chunks",
+                    cluster, nw, nch);
+    return max_active_clusters(*v, out);
+}
+
+namespace {
+int max_active_clusters(const Variant &vr, int *out)
+{
+    const Variant *v = &vr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(v->cluster));
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(static_cast<unsigned>(v->threads));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(v->cluster);
@@ -415,5 +497,6 @@ int recurrence_max_clusters(int cluster, int nw, int *out)
     cfg.numAttrs = 1;
     return cuda_status(cudaOccupancyMaxActiveClusters(out, v->fn, &cfg), "max active clusters");
 }
+}  // namespace
 
 } // namespace lstm

@@ -10,7 +10,9 @@ from gpu_util import assert_within, cuda
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [(16, 1), (16, 2), (16, 4), (16, 8), (8, 1), (8, 2), (8, 4), (8, 8)]
+VARIANTS = [(16, 1, 1), (16, 2, 1), (16, 4, 1), (16, 8, 1), (8, 1, 1), (8, 2, 1), (8, 4, 1),
+            (8, 8, 1), (4, 1, 1), (4, 2, 1), (2, 1, 1), (4, 1, 2), (4, 1, 4), (4, 1, 8),
+            (4, 2, 2), (4, 2, 4), (4, 2, 8), (8, 2, 4)]
 
 
 def _layer_inputs(batch, steps, layer_index=0, seed=21, scale=1.0):
@@ -81,13 +83,13 @@ def test_unknown_variant_is_rejected():
     b = torch.zeros(512, device="cuda")
     y = torch.zeros((1, 4, 256), device="cuda")
     with pytest.raises(binding.LSTMError) as e:
-        binding.lstm_recurrence_variant(g, rp, b, y, 1, 4, 0, 4, 1)
+        binding.lstm_recurrence_variant(g, rp, b, y, 1, 4, 0, 3, 1, 1)
     assert e.value.code == binding.LSTM_E_INVALID
 
 
 def test_max_clusters_query():
-    for c, nw in VARIANTS:
-        n = binding.lstm_recurrence_max_clusters(c, nw)
-        assert n >= 1, (c, nw, n)
+    for v in VARIANTS:
+        n = binding.lstm_recurrence_max_clusters(*v)
+        assert n >= 1, (v, n)
     with pytest.raises(binding.LSTMError):
-        binding.lstm_recurrence_max_clusters(4, 1)
+        binding.lstm_recurrence_max_clusters(3, 1, 1)
