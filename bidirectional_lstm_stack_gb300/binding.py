@@ -67,6 +67,7 @@ def load():
             "lstm_stack_forward": (i, [_vp, _vp, sz, _vp, sz, i, i, _vp]),
             "lstm_stack_forward_host": (i, [_vp, _vp, sz, _vp, sz, i, i, _vp]),
             "lstm_stack_enable_phase_timing": (i, [_vp, i]),
+            "lstm_stack_set_graphs": (i, [_vp, i]),
             "lstm_stack_phase_times": (i, [_vp, _c_float_p]),
             "lstm_stack_destroy": (None, [_vp]),
             "lstm_stack_last_error": (ctypes.c_char_p, []),
@@ -198,6 +199,10 @@ def lstm_stack_forward_host(handle, x: np.ndarray, y: np.ndarray, batch: int, st
     assert x.flags.c_contiguous and y.flags.c_contiguous
     _check(load().lstm_stack_forward_host(handle, x.ctypes.data, x.size, y.ctypes.data, y.size,
                                           batch, steps, _stream(stream)))
+
+
+def lstm_stack_set_graphs(handle, enable: bool = True):
+    _check(load().lstm_stack_set_graphs(handle, int(bool(enable))))
 
 
 def lstm_stack_enable_phase_timing(handle, enable: bool = True):

@@ -191,6 +191,21 @@ struct lstm_stack {
     bool timed_once = false;
     cudaEvent_t phase[kPhaseEvents] = {};
     unsigned *fault = nullptr;
+    // CUDA-graph replay of the forward pass, one instantiated graph per
+    // argument set (least recently used evicted)
+    struct Graph {
+        const float *x = nullptr;
+        float *y = nullptr;
+        int batch = 0, steps = 0;
+        bool timing = false;
+        cudaGraphExec_t exec = nullptr;
+        unsigned long long used = 0;
+    };
+    static constexpr int kGraphs = 8;
+    Graph graphs[kGraphs];
+    unsigned long long uses = 0;
+    bool use_graphs = true;
+    cudaStream_t capture = nullptr;
 };
 
 extern "C" const char *lstm_stack_last_error(void)
@@ -249,6 +264,11 @@ extern "C" void lstm_stack_destroy(lstm_stack *s)
     for (int i = 0; i < kPhaseEvents; ++i)
         if (s->phase[i])
             cudaEventDestroy(s->phase[i]);
+    for (auto &gr : s->graphs)
+        if (gr.exec)
+            cudaGraphExecDestroy(gr.exec);
+    if (s->capture)
+        cudaStreamDestroy(s->capture);
     if (s->side)
         cudaStreamDestroy(s->side);
     delete s;
@@ -356,6 +376,9 @@ extern "C" int lstm_stack_create(const lstm_stack_weights *weights, int max_batc
         st = encode_matrix_map(&s->map_ping[i], s->ping[i], max_rows, kOutput, 128);
     if (st == LSTM_OK)
         st = cuda_status(cudaStreamCreateWithFlags(&s->side, cudaStreamNonBlocking), "side stream");
+    if (st == LSTM_OK)
+        st = cuda_status(cudaStreamCreateWithFlags(&s->capture, cudaStreamNonBlocking),
+                         "capture stream");
     for (int l = 0; l < kLayers && st == LSTM_OK; ++l) {
         st = cuda_status(cudaEventCreateWithFlags(&s->fork[l], cudaEventDisableTiming), "event");
         if (st == LSTM_OK)
@@ -407,36 +430,38 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
         s->map_x_base = x;
         s->map_x_rows = rows;
     }
+    // phase events are recorded as external events, so they also fire when the
+    // pass is replayed from a captured graph
     auto ev = [&](int layer, int part, int end) { return s->phase[(layer * 3 + part) * 2 + end]; };
     for (int l = 0; l < kLayers; ++l) {
         const CUtensorMap &src = l == 0 ? s->map_x : s->map_ping[(l - 1) & 1];
         float *dst = l == kLayers - 1 ? y : s->ping[l & 1];
-        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 0, 0), stream), "event")))
+        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 0, 0), stream, cudaEventRecordExternal), "event")))
             return st;
         st = launch_projection(src, s->map_whi[l], s->map_wlo[l], s->gates, static_cast<int>(rows),
                                s->kp[l], s->fault, stream);
         if (st != LSTM_OK)
             return st;
-        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 0, 1), stream), "event")))
+        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 0, 1), stream, cudaEventRecordExternal), "event")))
             return st;
         if ((st = cuda_status(cudaEventRecord(s->fork[l], stream), "fork record")) ||
             (st = cuda_status(cudaStreamWaitEvent(s->side, s->fork[l], 0), "fork wait")))
             return st;
-        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 1, 0), stream), "event")))
+        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 1, 0), stream, cudaEventRecordExternal), "event")))
             return st;
         st = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps, 0, s->fault,
                                stream);
         if (st != LSTM_OK)
             return st;
-        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 1, 1), stream), "event")))
+        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 1, 1), stream, cudaEventRecordExternal), "event")))
             return st;
-        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 2, 0), s->side), "event")))
+        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 2, 0), s->side, cudaEventRecordExternal), "event")))
             return st;
         st = launch_recurrence(s->gates, s->rp[l] + kGates * kHidden, s->bias[l] + kGates, dst,
                                batch, steps, 1, s->fault, s->side);
         if (st != LSTM_OK)
             return st;
-        if (s->timing && (st = cuda_status(cudaEventRecord(ev(l, 2, 1), s->side), "event")))
+        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 2, 1), s->side, cudaEventRecordExternal), "event")))
             return st;
         if ((st = cuda_status(cudaEventRecord(s->join[l], s->side), "join record")) ||
             (st = cuda_status(cudaStreamWaitEvent(stream, s->join[l], 0), "join wait")))
@@ -448,6 +473,72 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
 }
 
 }  // namespace
+
+namespace {
+
+// Runs the forward pass on `stream` by replaying a CUDA graph of it: the
+// first call with a given (x, y, batch, steps, timing) records the launches
+// and the fork/join events on a private stream and instantiates the graph;
+// later calls only launch it.  When `stream` is itself being captured (the
+// caller is building a graph) or replay is off, the launches are enqueued
+// directly.
+int forward_replay(lstm_stack *s, const float *x, float *y, int batch, int steps,
+                   cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    int st = cuda_status(cudaStreamIsCapturing(stream, &cs), "stream capture status");
+    if (st != LSTM_OK)
+        return st;
+    if (!s->use_graphs || cs != cudaStreamCaptureStatusNone)
+        return forward_device(s, x, y, batch, steps, stream);
+    lstm_stack::Graph *hit = nullptr, *victim = &s->graphs[0];
+    for (auto &gr : s->graphs) {
+        if (gr.exec && gr.x == x && gr.y == y && gr.batch == batch && gr.steps == steps &&
+            gr.timing == s->timing) {
+            hit = &gr;
+            break;
+        }
+        if (!gr.exec || (victim->exec && gr.used < victim->used))
+            victim = &gr;
+    }
+    if (!hit) {
+        if (victim->exec) {
+            cudaGraphExecDestroy(victim->exec);
+            victim->exec = nullptr;
+        }
+        st = cuda_status(cudaStreamBeginCapture(s->capture, cudaStreamCaptureModeThreadLocal),
+                         "begin capture");
+        if (st != LSTM_OK)
+            return st;
+        const int fst = forward_device(s, x, y, batch, steps, s->capture);
+        cudaGraph_t graph = nullptr;
+        st = cuda_status(cudaStreamEndCapture(s->capture, &graph), "end capture");
+        if (fst != LSTM_OK || st != LSTM_OK) {
+            if (graph)
+                cudaGraphDestroy(graph);
+            return fst != LSTM_OK ? fst : st;
+        }
+        cudaGraphExec_t exec = nullptr;
+        st = cuda_status(cudaGraphInstantiate(&exec, graph, 0), "graph instantiate");
+        cudaGraphDestroy(graph);
+        if (st != LSTM_OK)
+            return st;
+        *victim = lstm_stack::Graph{x, y, batch, steps, s->timing, exec, 0};
+        hit = victim;
+    }
+    hit->used = ++s->uses;
+    return cuda_status(cudaGraphLaunch(hit->exec, stream), "graph launch");
+}
+
+}  // namespace
+
+extern "C" int lstm_stack_set_graphs(lstm_stack *s, int enable)
+{
+    if (!s)
+        return fail(LSTM_E_INVALID, "set_graphs: null stack");
+    s->use_graphs = enable != 0;
+    return LSTM_OK;
+}
 
 extern "C" int lstm_stack_forward(lstm_stack *s, const float *x, size_t x_len, float *y,
                                   size_t y_len, int batch, int steps, void *stream)
@@ -468,7 +559,7 @@ extern "C" int lstm_stack_forward(lstm_stack *s, const float *x, size_t x_len, f
     if (dx != s->device || dy != s->device)
         return fail(LSTM_E_INVALID, "forward: buffers on devices %d/%d, stack on device %d", dx, dy,
                     s->device);
-    return forward_device(s, x, y, batch, steps, static_cast<cudaStream_t>(stream));
+    return forward_replay(s, x, y, batch, steps, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_t x_len,
@@ -486,7 +577,7 @@ extern "C" int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_
                                           cudaMemcpyHostToDevice, st_),
                           "input copy")))
         return st;
-    if ((st = forward_device(s, s->x_stage, s->y_stage, batch, steps, st_)))
+    if ((st = forward_replay(s, s->x_stage, s->y_stage, batch, steps, st_)))
         return st;
     if ((st = cuda_status(cudaMemcpyAsync(y_host, s->y_stage, y_len * sizeof(float),
                                           cudaMemcpyDeviceToHost, st_),

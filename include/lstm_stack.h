@@ -99,13 +99,18 @@ int lstm_stack_create(const lstm_stack_weights *weights, int max_batch,
  *   y : device [batch][steps][256], y_len = batch*steps*256 floats;
  *       y[b][t][0:128] forward h, y[b][t][128:256] reverse h
  * x and y must not overlap each other or the stack's scratch.  Enqueued on
- * `stream`; allocates nothing and does not synchronise.  Each layer runs its
- * projection on `stream`, then the forward recurrence on `stream` and the
- * reverse one on the stack's side stream, joined back into `stream` before
- * the next layer.  Calls on one stack object must not overlap (they share its
- * scratch).  Errors: LSTM_E_INVALID (null, batch/steps <= 0 or above the
- * create-time maxima, x not 16-byte aligned, device mismatch), LSTM_E_LENGTH,
- * LSTM_E_CUDA. */
+ * `stream`; never allocates device memory and does not synchronise.  Each
+ * layer runs its projection, then the forward recurrence and, concurrently,
+ * the reverse one (forked onto the stack's side stream and joined back
+ * before the next layer).  The work is replayed from a CUDA graph: the first
+ * call with a given (x, y, batch, steps) records and instantiates the graph
+ * (driver-side host resources; up to 8 argument sets are kept, least
+ * recently used evicted), later calls launch it.  If `stream` is being
+ * captured by the caller, the launches are enqueued directly into the
+ * caller's capture instead.  Calls on one stack object must not overlap
+ * (they share its scratch).  Errors: LSTM_E_INVALID (null, batch/steps <= 0
+ * or above the create-time maxima, x not 16-byte aligned, device mismatch),
+ * LSTM_E_LENGTH, LSTM_E_CUDA. */
 int lstm_stack_forward(lstm_stack *s, const float *x, size_t x_len, float *y,
                        size_t y_len, int batch, int steps, void *stream);
 
@@ -125,6 +130,10 @@ int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_t x_len,
  * ms[3l+1] forward recurrence, ms[3l+2] reverse recurrence. */
 int lstm_stack_enable_phase_timing(lstm_stack *s, int enable);
 int lstm_stack_phase_times(lstm_stack *s, float *ms);
+
+/* Turns graph replay in lstm_stack_forward(_host) on (default) or off
+ * (direct launches every call); results are identical either way. */
+int lstm_stack_set_graphs(lstm_stack *s, int enable);
 
 /* Releases everything the stack owns (waits for its pending work first).
  * NULL is ignored. */

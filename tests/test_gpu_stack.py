@@ -108,3 +108,37 @@ def test_stack_argument_errors(stack):
     xh = np.zeros(1200, np.float32)
     assert lib.lstm_stack_forward(h, xh.ctypes.data, 1200, y.data_ptr(), y.numel(), 2, 10,
                                   s) == binding.LSTM_E_INVALID
+
+
+def test_graph_replay_matches_direct_launches(stack):
+    import torch
+    x = cuda(synthetic.stack_input(synthetic.WORKLOADS["b8_t589_x3"]))
+    outs = []
+    for graphs in (False, True, True):
+        binding.lstm_stack_set_graphs(stack.handle, graphs)
+        y = torch.full((8, 589, 256), float("nan"), device="cuda")
+        stack(x, y)
+        torch.cuda.synchronize()
+        outs.append(y.cpu().numpy())
+    binding.lstm_stack_set_graphs(stack.handle, True)
+    for o in outs[1:]:
+        assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32))
+
+
+def test_forward_inside_a_caller_graph_capture(stack, layers):
+    # the forward is capturable: a caller's CUDA graph records its launches
+    import torch
+    x_np = synthetic.random_matrix(77, (3, 50, 60))
+    x = cuda(x_np)
+    y = torch.full((3, 50, 256), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        stack(x, y, s)  # warm-up outside capture (variant tables, tensor maps)
+    torch.cuda.synchronize()
+    y.fill_(float("nan"))
+    with torch.cuda.graph(g, stream=s):
+        stack(x, y, s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_within(y.cpu().numpy(), oracle.lstm_stack(x_np, layers), what="captured forward")
