@@ -368,12 +368,12 @@ extern "C" int lstm_stack_create(const lstm_stack_weights *weights, int max_batc
         s->wp_lo[l] = s->weights + offs[l][1];
         s->rp[l] = s->weights + offs[l][2];
         s->bias[l] = s->weights + offs[l][3];
-        st = encode_matrix_map(&s->map_whi[l], s->wp_hi[l], kGateColumns, s->kp[l], 256);
+        st = encode_matrix_map(&s->map_whi[l], s->wp_hi[l], kGateColumns, s->kp[l], kProjectionBoxRows);
         if (st == LSTM_OK)
-            st = encode_matrix_map(&s->map_wlo[l], s->wp_lo[l], kGateColumns, s->kp[l], 256);
+            st = encode_matrix_map(&s->map_wlo[l], s->wp_lo[l], kGateColumns, s->kp[l], kProjectionBoxRows);
     }
     for (int i = 0; i < 2 && st == LSTM_OK; ++i)
-        st = encode_matrix_map(&s->map_ping[i], s->ping[i], max_rows, kOutput, 128);
+        st = encode_matrix_map(&s->map_ping[i], s->ping[i], max_rows, kOutput, kProjectionBoxRows);
     if (st == LSTM_OK)
         st = cuda_status(cudaStreamCreateWithFlags(&s->side, cudaStreamNonBlocking), "side stream");
     if (st == LSTM_OK)
@@ -424,7 +424,7 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
     const long rows = static_cast<long>(batch) * steps;
     int st;
     if (x != s->map_x_base || rows != s->map_x_rows) {
-        st = encode_matrix_map(&s->map_x, x, rows, kFeatures, 128);
+        st = encode_matrix_map(&s->map_x, x, rows, kFeatures, kProjectionBoxRows);
         if (st != LSTM_OK)
             return st;
         s->map_x_base = x;
@@ -635,9 +635,9 @@ extern "C" int lstm_projection(const float *x, int rows, int in_width, const flo
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
     CUtensorMap xm, hm, lm;
-    if ((st = encode_matrix_map(&xm, x, rows, in_width, 128)) ||
-        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, 256)) ||
-        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, 256)))
+    if ((st = encode_matrix_map(&xm, x, rows, in_width, kProjectionBoxRows)) ||
+        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionBoxRows)) ||
+        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionBoxRows)))
         return st;
     return launch_projection(xm, hm, lm, g, rows, kp, fault, static_cast<cudaStream_t>(stream));
 }

@@ -39,12 +39,13 @@ enum : unsigned {
 unsigned *fault_word();
 
 // ---- projection (projection.cu) ------------------------------------------
+// Rows per TMA box of the projection's operands (X rows and W gate rows).
+constexpr int kProjectionBoxRows = 128;
 // Encodes the tensor map of a row-major fp32 matrix [rows][cols] read in
 // boxes of 16 columns x box_rows rows with the 64-byte swizzle.
 int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols,
                       int box_rows);
-// G[rows][1024] = X . Wp^T in 3xTF32; the maps come from encode_matrix_map
-// (X: box_rows 128; Wp planes: box_rows 256).
+// G[rows][1024] = X . Wp^T in 3xTF32; the maps come from encode_matrix_map.
 int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
                       const CUtensorMap &wlo_map, float *g, int rows, int kp,
                       unsigned *fault, cudaStream_t stream);
@@ -74,6 +75,14 @@ namespace ptx {
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// fp32 rounded to TF32 (10 mantissa bits), nearest with ties away from zero.
+__device__ __forceinline__ float tf32_rna(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
 }
 
 __device__ __forceinline__ uint64_t globaltimer()
@@ -147,6 +156,18 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
                  : "memory");
 }
+// The same load delivered to the same shared-memory offset (and mbarrier
+// offset) of every CTA in `cta_mask` of this cluster.
+__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map,
+                                                      uint64_t *bar, int x, int y,
+                                                      uint16_t cta_mask)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y),
+                 "h"(cta_mask)
+                 : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -198,6 +219,21 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+// Arrives once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
+// when this thread's earlier tcgen05 operations have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;" ::"r"(smem_u32(bar)),
+                 "h"(cta_mask)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_nid_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
 }
 // 32 lanes x 32 consecutive 32-bit columns: thread (lane) gets its lane's row.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])

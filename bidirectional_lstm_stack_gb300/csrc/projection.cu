@@ -5,13 +5,17 @@
 // `InputProjection::enqueue`), with the gate columns already in the packed,
 // unit-interleaved order (the packer reorders W's rows).
 //
-// Design (sm_103a), a persistent kernel, one CTA per SM:
-//  * a CTA walks 128 x 256 tiles of G (tile t: rows 128*(t/4), gate columns
-//    256*(t%4), so the CTAs running together share their X rows in L2);
+// Design (sm_103a), a persistent kernel, one CTA per SM, CTAs paired in
+// clusters of two along the rows:
+//  * a cluster walks pairs of 128 x 256 tiles of G (pair p: rows
+//    256*(p/4) + 128*rank, gate columns 256*(p%4)); both CTAs of a pair use
+//    the same W tile, so each loads half of it and multicasts that half into
+//    both CTAs' shared memory (half the W traffic from L2 per tile);
 //  * K advances in blocks of 16 fp32 (64 bytes, 64-byte swizzle) through a
 //    4-stage shared-memory ring (48 KiB per stage);
-//  * warp 8 (TMA producer) loads the X block and the TF32 hi and lo planes of
-//    Wp (split on the host) into the ring;
+//  * warp 8 (TMA producer) loads the X block and its half of the TF32 hi and
+//    lo planes of Wp (split on the host) into the ring; a stage is reused
+//    only once the MMAs of both CTAs have released it;
 //  * warps 0-3 split the X block in place into its TF32 hi part and a second
 //    buffer with the TF32 lo remainder;
 //  * one thread of warp 9 issues tcgen05.mma kind::tf32 (M=128, N=256, K=8)
@@ -50,6 +54,10 @@ constexpr int THREADS = 320;
 constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 constexpr int TILES_N = kGateColumns / BN;          // 4
+constexpr int CLUSTER = 2;                          // CTAs sharing a W tile
+constexpr uint16_t PAIR_MASK = 0x3;
+constexpr int B_HALF_BYTES = B_BYTES / CLUSTER;     // W rows one CTA loads
+static_assert(BN / CLUSTER == kProjectionBoxRows && BM == kProjectionBoxRows, "TMA boxes");
 
 // tcgen05 shared-memory matrix descriptor: K-major operand, 64-byte
 // swizzle, 8-row groups 512 bytes apart.
@@ -68,19 +76,12 @@ constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
                            (static_cast<uint32_t>(BN >> 3) << 17) |
                            (static_cast<uint32_t>(BM >> 4) << 24);
 
-__device__ __forceinline__ float tf32_rna(float x)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
 __device__ __forceinline__ void split4(float4 v, float4 &hi, float4 &lo)
 {
-    hi.x = tf32_rna(v.x); lo.x = tf32_rna(v.x - hi.x);
-    hi.y = tf32_rna(v.y); lo.y = tf32_rna(v.y - hi.y);
-    hi.z = tf32_rna(v.z); lo.z = tf32_rna(v.z - hi.z);
-    hi.w = tf32_rna(v.w); lo.w = tf32_rna(v.w - hi.w);
+    hi.x = ptx::tf32_rna(v.x); lo.x = ptx::tf32_rna(v.x - hi.x);
+    hi.y = ptx::tf32_rna(v.y); lo.y = ptx::tf32_rna(v.y - hi.y);
+    hi.z = ptx::tf32_rna(v.z); lo.z = ptx::tf32_rna(v.z - hi.z);
+    hi.w = ptx::tf32_rna(v.w); lo.w = ptx::tf32_rna(v.w - hi.w);
 }
 
 // Waits without regard to the abort flag (used to drain in-flight work).
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 projection_kernel(const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap whi_map,
                   const __grid_constant__ CUtensorMap wlo_map, float *__restrict__ g, int rows,
-                  int kblocks, int tiles, unsigned *fault)
+                  int kblocks, int pairs, unsigned *fault)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -121,7 +122,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&conv[s], CONVERTERS);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&empty[s], CLUSTER);  // both CTAs' MMAs release a stage
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&acc_full[a], 1);
@@ -141,17 +142,24 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     }
     ptx::tc_fence_before();
     __syncthreads();
+    // the peer's barriers are initialised before any multicast reaches them
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int rank = static_cast<int>(ptx::cluster_ctarank());
+    const int first = static_cast<int>(ptx::cluster_id_x());
+    const int stride = static_cast<int>(ptx::cluster_nid_x());
     long issued = 0;            // producer: K blocks whose loads were issued
     int committed_tiles = 0;    // MMA: accumulators committed
 
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             long kbi = 0;
-            for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-                const int m0 = (t / TILES_N) * BM;
+            for (int t = first; t < pairs && !*abort_flag; t += stride) {
+                const int m0 = ((t / TILES_N) * CLUSTER + rank) * BM;
                 const int n0 = (t % TILES_N) * BN;
+                const int nh = n0 + rank * (BN / CLUSTER);  // this CTA's half of the W tile
                 for (int kb = 0; kb < kblocks; ++kb, ++kbi) {
                     const int s = static_cast<int>(kbi % STAGES);
                     const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
@@ -161,8 +169,10 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     uint8_t *st = smem + s * STAGE_BYTES;
                     ptx::mbar_arrive_expect_tx(&full[s], TX_BYTES);
                     ptx::tma_load_2d(st, &x_map, &full[s], kb * BK, m0);
-                    ptx::tma_load_2d(st + 2 * A_BYTES, &whi_map, &full[s], kb * BK, n0);
-                    ptx::tma_load_2d(st + 2 * A_BYTES + B_BYTES, &wlo_map, &full[s], kb * BK, n0);
+                    ptx::tma_load_2d_multicast(st + 2 * A_BYTES + rank * B_HALF_BYTES, &whi_map,
+                                               &full[s], kb * BK, nh, PAIR_MASK);
+                    ptx::tma_load_2d_multicast(st + 2 * A_BYTES + B_BYTES + rank * B_HALF_BYTES,
+                                               &wlo_map, &full[s], kb * BK, nh, PAIR_MASK);
                     issued = kbi + 1;
                 }
             }
@@ -171,7 +181,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         if (lane == 0) {
             long kbi = 0;
             int ti = 0;
-            for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++ti) {
+            for (int t = first; t < pairs && !*abort_flag; t += stride, ++ti) {
                 const int a = ti & 1;
                 const uint32_t use = static_cast<uint32_t>(ti >> 1);
                 if (use > 0 && !ptx::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, abort_flag,
@@ -201,7 +211,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                         ptx::mma_tf32(d_tmem, sw64_desc(a_hi + off), sw64_desc(b_lo + off), IDESC, 1);
                         ptx::mma_tf32(d_tmem, sw64_desc(a_lo + off), sw64_desc(b_hi + off), IDESC, 1);
                     }
-                    ptx::mma_commit(&empty[s]);
+                    ptx::mma_commit_multicast(&empty[s], PAIR_MASK);
                 }
                 ptx::mma_commit(&acc_full[a]);  // also when stopping early: frees the epilogue
                 committed_tiles = ti + 1;
@@ -213,7 +223,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         // converters: split X into TF32 hi (in place) and lo
         const int tid = threadIdx.x;
         long kbi = 0;
-        for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+        for (int t = first; t < pairs && !*abort_flag; t += stride) {
             bool ok = true;
             for (int kb = 0; kb < kblocks; ++kb, ++kbi) {
                 const int s = static_cast<int>(kbi % STAGES);
@@ -239,12 +249,12 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             if (!ok)
                 break;
         }
-    } else {
+    } else if (warp >= 4) {
         // epilogue: warp 4+q reads TMEM lanes 32q .. 32q+31 (warp id mod 4 = q)
         const int q = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         int ti = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++ti) {
+        for (int t = first; t < pairs; t += stride, ++ti) {
             const int a = ti & 1;
             const uint32_t use = static_cast<uint32_t>(ti >> 1);
             bool got = ptx::mbar_wait_bounded(&acc_full[a], use & 1, abort_flag, fault,
@@ -253,7 +263,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             if (!__all_sync(0xffffffffu, got) || *abort_flag)
                 break;
             ptx::tc_fence_after();
-            const int m0 = (t / TILES_N) * BM;
+            const int m0 = ((t / TILES_N) * CLUSTER + rank) * BM;
             const int n0 = (t % TILES_N) * BN;
             const long m = static_cast<long>(m0) + q * 32 + lane;
             const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(a) * ACC_COLS;
@@ -293,6 +303,11 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
+    // neither CTA leaves while the other may still multicast into it or
+    // release its stages
+    __syncwarp();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -360,18 +375,32 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     if (rows <= 0 || kp <= 0 || kp % 32 != 0)
         return fail(LSTM_E_INVALID, "projection: rows %d, kp %d", rows, kp);
     const long mtiles = (static_cast<long>(rows) + BM - 1) / BM;
-    const long tiles = mtiles * TILES_N;
-    if (tiles > 0x7fffffffL)
+    const long pairs = (mtiles + CLUSTER - 1) / CLUSTER * TILES_N;
+    if (pairs > 0x7fffffffL)
         return fail(LSTM_E_OVERFLOW, "projection: %d rows", rows);
     int dev = 0;
     int st = cuda_status(cudaGetDevice(&dev), "current device");
     if (st != LSTM_OK)
         return st;
     const int sms = (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) ? g_sm_count[dev] : 148;
-    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    projection_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(x_map, whi_map, wlo_map, g, rows,
-                                                             kp / BK, static_cast<int>(tiles), fault);
-    return cuda_status(cudaGetLastError(), "projection launch");
+    const long clusters = pairs < sms / CLUSTER ? pairs : sms / CLUSTER;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int kblocks = kp / BK;
+    const int npairs = static_cast<int>(pairs);
+    return cuda_status(cudaLaunchKernelEx(&cfg, projection_kernel, x_map, whi_map, wlo_map, g, rows,
+                                          kblocks, npairs, fault),
+                       "projection launch");
 }
 
 } // namespace lstm

@@ -106,9 +106,9 @@ extern "C" int lstm_layer_forward_static(const float *x, int batch, int steps, i
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
     CUtensorMap xm, hm, lm;
-    if ((st = encode_matrix_map(&xm, x, rows, in_width, 128)) ||
-        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, 256)) ||
-        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, 256)))
+    if ((st = encode_matrix_map(&xm, x, rows, in_width, kProjectionBoxRows)) ||
+        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionBoxRows)) ||
+        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionBoxRows)))
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = launch_projection(xm, hm, lm, gates, static_cast<int>(rows), kp, fault, s)))
