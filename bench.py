@@ -49,6 +49,9 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # nominal dense rates (per GPU) used to scale the measured bf16 peak to TF32
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_TF32_TFLOPS = 1100.0
+# tcgen05 kind::tf32 rate measured on this GPU model by a microbenchmark
+# (back-to-back M128 N256 K8 MMAs on every SM: 128 cycles each), TF/s
+TF32_MICROBENCHMARK_TFLOPS = 1210.0
 # FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop per FMA at the SM clock
 SMS = 152
 FP32_LANES = 128
@@ -364,7 +367,9 @@ def run_ours(args):
                                 "traffic": ncu_traffic("projection", wl.batch * wl.steps),
                                 "peak_source": f"{peak_kind} bf16 burst {p['bf16_tflops']} x "
                                                f"{NOMINAL_TF32_TFLOPS}/{NOMINAL_BF16_TFLOPS} "
-                                               f"(TF32) / 3 (3xTF32)"},
+                                               f"(TF32) / 3 (3xTF32)",
+                                "frac_of_tf32_microbenchmark":
+                                    proj_achieved / (TF32_MICROBENCHMARK_TFLOPS / 3.0)},
         "e2e": {"value": e2e_value, "unit": "windows/s",
                 "h2d_bytes_per_step": int(xn.nbytes), "d2h_bytes_per_step": int(yn.nbytes)},
         "gpu_launches": 12 * args.steps,
