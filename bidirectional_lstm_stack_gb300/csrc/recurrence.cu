@@ -60,9 +60,10 @@ constexpr int HROW = KC * CHUNK_STRIDE;  // floats per window in the h buffer
 constexpr int PF = 4;                 // projection prefetch depth (steps)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
+// s(z) = 1 / (1 + e^-z), in [0, 1] for every finite z without a clamp:
+// e^-z overflows to +inf for z < about -88 and __fdividef(1, inf) is 0.
 __device__ __forceinline__ float sigmoid_bounded(float z)
 {
-    z = fminf(fmaxf(z, -80.0f), 80.0f);
     return __fdividef(1.0f, 1.0f + __expf(-z));
 }
 __device__ __forceinline__ float tanh_bounded(float z)
