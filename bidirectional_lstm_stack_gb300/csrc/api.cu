@@ -123,6 +123,9 @@ int prepare_device(int device)
     std::lock_guard<std::mutex> lock(mu);
     if (done[device])
         return LSTM_OK;
+    DeviceGuard guard(device);  // occupancy queries below use the current device
+    if (!guard.ok)
+        return fail(LSTM_E_CUDA, "cannot make device %d current", device);
     int st = check_device(device);
     if (st == LSTM_OK)
         st = projection_prepare(device);
@@ -368,9 +371,9 @@ extern "C" int lstm_stack_create(const lstm_stack_weights *weights, int max_batc
         s->wp_lo[l] = s->weights + offs[l][1];
         s->rp[l] = s->weights + offs[l][2];
         s->bias[l] = s->weights + offs[l][3];
-        st = encode_matrix_map(&s->map_whi[l], s->wp_hi[l], kGateColumns, s->kp[l], kProjectionBoxRows);
+        st = encode_matrix_map(&s->map_whi[l], s->wp_hi[l], kGateColumns, s->kp[l], kProjectionWBoxRows);
         if (st == LSTM_OK)
-            st = encode_matrix_map(&s->map_wlo[l], s->wp_lo[l], kGateColumns, s->kp[l], kProjectionBoxRows);
+            st = encode_matrix_map(&s->map_wlo[l], s->wp_lo[l], kGateColumns, s->kp[l], kProjectionWBoxRows);
     }
     for (int i = 0; i < 2 && st == LSTM_OK; ++i)
         st = encode_matrix_map(&s->map_ping[i], s->ping[i], max_rows, kOutput, kProjectionBoxRows);
@@ -636,8 +639,8 @@ extern "C" int lstm_projection(const float *x, int rows, int in_width, const flo
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
     CUtensorMap xm, hm, lm;
     if ((st = encode_matrix_map(&xm, x, rows, in_width, kProjectionBoxRows)) ||
-        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionBoxRows)) ||
-        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionBoxRows)))
+        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionWBoxRows)) ||
+        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionWBoxRows)))
         return st;
     return launch_projection(xm, hm, lm, g, rows, kp, fault, static_cast<cudaStream_t>(stream));
 }

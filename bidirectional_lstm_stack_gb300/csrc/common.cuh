@@ -39,8 +39,10 @@ enum : unsigned {
 unsigned *fault_word();
 
 // ---- projection (projection.cu) ------------------------------------------
-// Rows per TMA box of the projection's operands (X rows and W gate rows).
+// Rows per TMA box of the projection's operands: X rows, and the W gate rows
+// one CTA of a 2-CTA cluster loads (half of a 256-row W tile).
 constexpr int kProjectionBoxRows = 128;
+constexpr int kProjectionWBoxRows = 128;
 // Encodes the tensor map of a row-major fp32 matrix [rows][cols] read in
 // boxes of 16 columns x box_rows rows with the 64-byte swizzle.
 int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols,

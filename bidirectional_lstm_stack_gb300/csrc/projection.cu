@@ -10,7 +10,8 @@
 //  * a cluster walks pairs of 128 x 256 tiles of G (pair p: rows
 //    256*(p/4) + 128*rank, gate columns 256*(p%4)); both CTAs of a pair use
 //    the same W tile, so each loads half of it and multicasts that half into
-//    both CTAs' shared memory (half the W traffic from L2 per tile);
+//    both CTAs' shared memory (half the W traffic from L2 per tile; clusters
+//    of four were measured slower);
 //  * K advances in blocks of 16 fp32 (64 bytes, 64-byte swizzle) through a
 //    4-stage shared-memory ring (48 KiB per stage);
 //  * warp 8 (TMA producer) loads the X block and its half of the TF32 hi and
@@ -24,7 +25,8 @@
 //    accuracy (TF32 alone was not accurate enough on some parts, per the
 //    pages' `tf32_projection_accurate`);
 //  * warps 4-7 (epilogue) read a finished accumulator with tcgen05.ld and
-//    store rows of G while the MMA fills the other accumulator.
+//    store rows of G while the MMA fills the other accumulator, paced by the
+//    MMA's progress through the next tile.
 // Every mbarrier wait is bounded in time; a wait that runs out sets a bit in
 // the fault word, every role stops, and the CTA drains its TMA loads and MMAs
 // before it frees tensor memory and returns.
@@ -55,9 +57,9 @@ constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 constexpr int TILES_N = kGateColumns / BN;          // 4
 constexpr int CLUSTER = 2;                          // CTAs sharing a W tile
-constexpr uint16_t PAIR_MASK = 0x3;
+constexpr uint16_t PAIR_MASK = (1u << CLUSTER) - 1;
 constexpr int B_HALF_BYTES = B_BYTES / CLUSTER;     // W rows one CTA loads
-static_assert(BN / CLUSTER == kProjectionBoxRows && BM == kProjectionBoxRows, "TMA boxes");
+static_assert(BN / CLUSTER == kProjectionWBoxRows && BM == kProjectionBoxRows, "TMA boxes");
 
 // tcgen05 shared-memory matrix descriptor: K-major operand, 64-byte
 // swizzle, 8-row groups 512 bytes apart.
@@ -114,6 +116,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     uint64_t *acc_empty = acc_full + 2;       // [2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *progress = abort_flag + 1;  // K blocks whose MMAs were issued
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -129,6 +132,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             ptx::mbar_init(&acc_empty[a], EPILOGUE);
         }
         *abort_flag = 0;
+        *progress = 0;
         ptx::fence_mbar_init();
     }
     if (warp == PRODUCER_WARP && lane == 0) {
@@ -212,6 +216,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                         ptx::mma_tf32(d_tmem, sw64_desc(a_lo + off), sw64_desc(b_hi + off), IDESC, 1);
                     }
                     ptx::mma_commit_multicast(&empty[s], PAIR_MASK);
+                    *progress = static_cast<int>(kbi + 1);
                 }
                 ptx::mma_commit(&acc_full[a]);  // also when stopping early: frees the epilogue
                 committed_tiles = ti + 1;
@@ -267,8 +272,23 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             const int n0 = (t % TILES_N) * BN;
             const long m = static_cast<long>(m0) + q * 32 + lane;
             const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(a) * ACC_COLS;
+            // Pace the stores: chunk c of this tile goes out once the next
+            // tile's mainloop has issued c/8 of its K blocks, so G streams to
+            // memory under the next tile's compute instead of every CTA
+            // writing its whole tile at once and stalling the loads.
+            const bool paced = t + stride < pairs;
+            const long next_kb = static_cast<long>(ti + 1) * kblocks;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
+                if (paced) {
+                    const long want = next_kb + (static_cast<long>(c) * kblocks) / (BN / 32);
+                    if (*progress < want && !*abort_flag) {
+                        const uint64_t start = ptx::globaltimer();
+                        while (*progress < want && !*abort_flag &&
+                               ptx::globaltimer() - start < WAIT_LIMIT_NS)
+                            __nanosleep(64);
+                    }
+                }
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(acc + c * 32, r);
                 ptx::tmem_ld_wait();
@@ -326,6 +346,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 int g_sm_count[64] = {};
+int g_max_clusters[64] = {};  // clusters of the projection a device runs at once
 
 } // namespace
 
@@ -362,10 +383,31 @@ int projection_prepare(int device)
     if (st != LSTM_OK)
         return st;
     g_sm_count[device] = sms;
-    return cuda_status(cudaFuncSetAttribute(projection_kernel,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(SMEM_BYTES)),
-                       "projection shared-memory attribute");
+    st = cuda_status(cudaFuncSetAttribute(projection_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(SMEM_BYTES)),
+                     "projection shared-memory attribute");
+    if (st != LSTM_OK)
+        return st;
+    // the persistent grid is no larger than what runs at once
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CLUSTER);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    st = cuda_status(cudaOccupancyMaxActiveClusters(&n, projection_kernel, &cfg),
+                     "projection max active clusters");
+    if (st != LSTM_OK)
+        return st;
+    g_max_clusters[device] = n > 0 ? n : sms / CLUSTER;
+    return LSTM_OK;
 }
 
 int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
@@ -382,8 +424,9 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     int st = cuda_status(cudaGetDevice(&dev), "current device");
     if (st != LSTM_OK)
         return st;
-    const int sms = (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) ? g_sm_count[dev] : 148;
-    const long clusters = pairs < sms / CLUSTER ? pairs : sms / CLUSTER;
+    const int fit = (dev >= 0 && dev < 64 && g_max_clusters[dev] > 0) ? g_max_clusters[dev]
+                                                                      : 148 / CLUSTER;
+    const long clusters = pairs < fit ? pairs : fit;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
     cfg.blockDim = dim3(THREADS);

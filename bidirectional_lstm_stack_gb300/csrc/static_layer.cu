@@ -107,8 +107,8 @@ extern "C" int lstm_layer_forward_static(const float *x, int batch, int steps, i
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
     CUtensorMap xm, hm, lm;
     if ((st = encode_matrix_map(&xm, x, rows, in_width, kProjectionBoxRows)) ||
-        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionBoxRows)) ||
-        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionBoxRows)))
+        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionWBoxRows)) ||
+        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionWBoxRows)))
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = launch_projection(xm, hm, lm, gates, static_cast<int>(rows), kp, fault, s)))
