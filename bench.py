@@ -350,7 +350,14 @@ def run_ours(args):
                        "windows_per_s": 1e3 / ms1_step,
                        "us_per_step": ms1_step * 1e3 / (LAYERS * lat.steps),
                        "recurrence_us_per_step": float(np.mean(ph1[:, 1:])) * 1e3 / lat.steps,
+                       "phases_ms": {"projection": [round(float(v), 4) for v in ph1[:, 0]],
+                                     "recurrence_fwd": [round(float(v), 4) for v in ph1[:, 1]],
+                                     "recurrence_rev": [round(float(v), 4) for v in ph1[:, 2]]},
+                       "gaps_ms": ms1_step - float(np.sum(ph1[:, 0]) +
+                                                  np.sum(np.maximum(ph1[:, 1], ph1[:, 2]))),
                        "context": "pages: A100, TF32-projection stack, 3.21-4.13 ms per window"},
+        "gaps_ms": ms_per_step - float(np.sum(phases[:, 0]) +
+                                       np.sum(np.maximum(phases[:, 1], phases[:, 2]))),
         "phases_ms": {"projection": [round(float(v), 4) for v in phases[:, 0]],
                       "recurrence_fwd": [round(float(v), 4) for v in phases[:, 1]],
                       "recurrence_rev": [round(float(v), 4) for v in phases[:, 2]]},

@@ -74,8 +74,8 @@ def load():
             "lstm_pack_layer": (i, [_vp, _vp, _vp, i, i, _vp, _vp, _vp, _vp]),
             "lstm_projection": (i, [_vp, i, i, _vp, _vp, i, _vp, _vp]),
             "lstm_recurrence": (i, [_vp, _vp, _vp, _vp, i, i, i, _vp]),
-            "lstm_recurrence_variant": (i, [_vp, _vp, _vp, _vp, i, i, i, i, i, i, _vp]),
-            "lstm_recurrence_max_clusters": (i, [i, i, i, i, ctypes.POINTER(i)]),
+            "lstm_recurrence_variant": (i, [_vp, _vp, _vp, _vp, i, i, i, i, i, i, i, _vp]),
+            "lstm_recurrence_max_clusters": (i, [i, i, i, i, i, ctypes.POINTER(i)]),
             "lstm_fault_status": (i, [ctypes.POINTER(ctypes.c_uint)]),
             "lstm_layer_forward_static": (i, [_vp, i, i, i, _vp, _vp, i, _vp, _vp, _vp, _vp]),
         }
@@ -140,17 +140,17 @@ def lstm_recurrence(g, rp, bias, y, batch: int, steps: int, direction: int, stre
 
 def lstm_recurrence_variant(g, rp, bias, y, batch: int, steps: int, direction: int,
                             cluster_size: int, windows_per_chunk: int, chunks: int = 1,
-                            stream=None):
+                            threads_per_block: int = 0, stream=None):
     _check(load().lstm_recurrence_variant(_ptr(g), _ptr(rp), _ptr(bias), _ptr(y), batch, steps,
                                           direction, cluster_size, windows_per_chunk, chunks,
-                                          _stream(stream, g.device)))
+                                          threads_per_block, _stream(stream, g.device)))
 
 
 def lstm_recurrence_max_clusters(cluster_size: int, windows_per_chunk: int, chunks: int = 1,
-                                 device: int = 0) -> int:
+                                 threads_per_block: int = 0, device: int = 0) -> int:
     v = ctypes.c_int(0)
-    _check(load().lstm_recurrence_max_clusters(cluster_size, windows_per_chunk, chunks, device,
-                                               ctypes.byref(v)))
+    _check(load().lstm_recurrence_max_clusters(cluster_size, windows_per_chunk, chunks,
+                                               threads_per_block, device, ctypes.byref(v)))
     return int(v.value)
 
 

@@ -683,7 +683,7 @@ extern "C" int lstm_recurrence(const float *g, const float *rp, const float *bia
 extern "C" int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
                                        float *y, int batch, int steps, int direction,
                                        int cluster_size, int windows_per_chunk, int chunks,
-                                       void *stream)
+                                       int threads_per_block, void *stream)
 {
     int dev = 0;
     int st = recurrence_args(g, rp, bias, y, batch, steps, direction, &dev);
@@ -694,12 +694,13 @@ extern "C" int lstm_recurrence_variant(const float *g, const float *rp, const fl
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
     return launch_recurrence_variant(g, rp, bias, y, batch, steps, direction, cluster_size,
-                                     windows_per_chunk, chunks, fault,
+                                     windows_per_chunk, chunks, threads_per_block, fault,
                                      static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int lstm_recurrence_max_clusters(int cluster_size, int windows_per_chunk, int chunks,
-                                            int device, int *max_clusters)
+                                            int threads_per_block, int device,
+                                            int *max_clusters)
 {
     if (!max_clusters)
         return fail(LSTM_E_INVALID, "lstm_recurrence_max_clusters: null pointer");
@@ -707,7 +708,8 @@ extern "C" int lstm_recurrence_max_clusters(int cluster_size, int windows_per_ch
     if (st != LSTM_OK)
         return st;
     DeviceGuard guard(device);
-    return recurrence_max_clusters(cluster_size, windows_per_chunk, chunks, max_clusters);
+    return recurrence_max_clusters(cluster_size, windows_per_chunk, chunks, threads_per_block,
+                                   max_clusters);
 }
 
 extern "C" int lstm_fault_status(unsigned int *fault)

@@ -59,10 +59,10 @@ int launch_recurrence(const float *g, const float *rp, const float *bias,
                       unsigned *fault, cudaStream_t stream);
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias,
                               float *y, int batch, int steps, int direction,
-                              int cluster, int nw, int nch, unsigned *fault,
+                              int cluster, int nw, int nch, int threads, unsigned *fault,
                               cudaStream_t stream);
 // Clusters of a variant the device can hold at once.
-int recurrence_max_clusters(int cluster, int nw, int nch, int *out);
+int recurrence_max_clusters(int cluster, int nw, int nch, int threads, int *out);
 int recurrence_prepare(int device);
 
 } // namespace lstm

@@ -351,26 +351,32 @@ struct Variant {
     const void *fn;
 };
 
-template <int C, int NW, int NCH = 1>
+template <int C, int NW, int NCH = 1, int THREADS = threads_for<C>()>
 Variant variant()
 {
-    constexpr int threads = threads_for<C>();
-    return Variant{C, NW, NCH, threads / 8 / (kHidden / C) * NW * NCH, threads,
-                   reinterpret_cast<const void *>(&recurrence_kernel<C, NW, NCH>)};
+    return Variant{C, NW, NCH, THREADS / 8 / (kHidden / C) * NW * NCH, THREADS,
+                   reinterpret_cast<const void *>(&recurrence_kernel<C, NW, NCH, THREADS>)};
 }
 
+// "Narrow" variants (one window group per CTA: 128 threads for clusters of
+// 8, 64 for clusters of 16) give each SM sub-partition fewer warps, for small
+// batches where wider CTAs would mostly compute padding windows.
 const Variant kVariants[] = {
-    variant<16, 1>(),   variant<16, 2>(),   variant<16, 4>(),   variant<16, 8>(),
-    variant<8, 1>(),    variant<8, 2>(),    variant<8, 4>(),    variant<8, 8>(),
-    variant<4, 1>(),    variant<4, 2>(),    variant<2, 1>(),
-    variant<4, 1, 2>(), variant<4, 1, 4>(), variant<4, 1, 8>(), variant<4, 2, 2>(),
-    variant<4, 2, 4>(), variant<4, 2, 8>(), variant<8, 2, 4>(),
+    variant<16, 1>(),           variant<16, 2>(),   variant<16, 4>(),   variant<16, 8>(),
+    variant<8, 1>(),            variant<8, 2>(),    variant<8, 4>(),    variant<8, 8>(),
+    variant<4, 1>(),            variant<4, 2>(),    variant<2, 1>(),
+    variant<4, 1, 2>(),         variant<4, 1, 4>(), variant<4, 1, 8>(), variant<4, 2, 2>(),
+    variant<4, 2, 4>(),         variant<4, 2, 8>(), variant<8, 2, 4>(),
+    variant<8, 1, 1, 128>(),    variant<8, 2, 1, 128>(), variant<16, 1, 1, 64>(),
+    variant<16, 2, 1, 64>(),
 };
 
-const Variant *find_variant(int cluster, int nw, int nch)
+// threads == 0: the variant's default block size
+const Variant *find_variant(int cluster, int nw, int nch, int threads = 0)
 {
     for (const Variant &v : kVariants)
-        if (v.cluster == cluster && v.nw == nw && v.nch == nch)
+        if (v.cluster == cluster && v.nw == nw && v.nch == nch &&
+            (threads ? v.threads == threads : v.threads == (cluster == 2 ? 512 : 256)))
             return &v;
     return nullptr;
 }
@@ -379,16 +385,20 @@ int max_active_clusters(const Variant &v, int *out);
 
 // The default variant for a batch.  Candidates in order of preference, from
 // per-step timings of every variant with both directions running (GB300,
-// T = 589): clusters of 4 with one window per 8-lane group (0.51 us/step from
-// 1 to 16 windows, 0.65 at 32; two CTAs per SM), then 2, 4 and 8 chunks of
-// two windows per lane (0.95 us/step at 64 windows, 1.58 at 128, 2.91 at 256).
-// The first whose clusters for both directions fit the device at once wins;
-// past that, the widest tile.
+// T = 589): up to 8 windows, narrow clusters of 8 (128 threads, one window
+// per 8-lane group: 0.47 us/step at one window); then clusters of 4 with one
+// window per group (0.51 us/step up to 16 windows, 0.65 at 32; two CTAs per
+// SM), then 2, 4 and 8 chunks of two windows per lane (0.94 us/step at 64
+// windows, 1.58 at 128, 2.91 at 256).  The first whose clusters for both
+// directions fit the device at once wins; past that, the widest tile.
 const Variant *choose_variant(int batch)
 {
-    static const int order[][3] = {{4, 1, 1}, {4, 2, 2}, {4, 2, 4}, {4, 2, 8}};
+    static const int order[][4] = {{8, 1, 1, 128}, {4, 1, 1, 0}, {4, 2, 2, 0}, {4, 2, 4, 0},
+                                   {4, 2, 8, 0}};
+    constexpr int N = sizeof(order) / sizeof(order[0]);
+    constexpr int NARROW_MAX_BATCH = 8;
     static std::mutex mu;
-    static int fits[64][4];
+    static int fits[64][N];
     static bool known[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
@@ -396,16 +406,18 @@ const Variant *choose_variant(int batch)
     if (dev >= 0) {
         std::lock_guard<std::mutex> lock(mu);
         if (!known[dev]) {
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < N; ++i) {
                 int n = 0;
-                const Variant *v = find_variant(order[i][0], order[i][1], order[i][2]);
+                const Variant *v = find_variant(order[i][0], order[i][1], order[i][2], order[i][3]);
                 fits[dev][i] = (v && max_active_clusters(*v, &n) == LSTM_OK) ? n : 0;
             }
             known[dev] = true;
         }
     }
-    for (int i = 0; i < 4; ++i) {
-        const Variant *v = find_variant(order[i][0], order[i][1], order[i][2]);
+    for (int i = 0; i < N; ++i) {
+        if (i == 0 && batch > NARROW_MAX_BATCH)
+            continue;
+        const Variant *v = find_variant(order[i][0], order[i][1], order[i][2], order[i][3]);
         const long tiles = (static_cast<long>(batch) + v->tile - 1) / v->tile;
         if (dev >= 0 && 2 * tiles <= fits[dev][i])
             return v;
@@ -462,23 +474,25 @@ int launch_recurrence(const float *g, const float *rp, const float *bias, float 
 
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias, float *y,
                               int batch, int steps, int direction, int cluster, int nw, int nch,
-                              unsigned *fault, cudaStream_t stream)
+                              int threads, unsigned *fault, cudaStream_t stream)
 {
-    const Variant *v = find_variant(cluster, nw, nch);
+    const Variant *v = find_variant(cluster, nw, nch, threads);
     if (!v)
         return fail(LSTM_E_INVALID,
-                    "recurrence: no variant with cluster %d, %d windows per chunk, %d chunks",
-                    cluster, nw, nch);
+                    "recurrence: no variant with cluster %d, %d windows per chunk, %d chunks, "
+                    "%d threads",
+                    cluster, nw, nch, threads);
     return launch_variant(*v, g, rp, bias, y, batch, steps, direction, fault, stream);
 }
 
-int recurrence_max_clusters(int cluster, int nw, int nch, int *out)
+int recurrence_max_clusters(int cluster, int nw, int nch, int threads, int *out)
 {
-    const Variant *v = find_variant(cluster, nw, nch);
+    const Variant *v = find_variant(cluster, nw, nch, threads);
     if (!v)
         return fail(LSTM_E_INVALID,
-                    "recurrence: no variant with cluster %d, %d windows per chunk, %d chunks",
-                    cluster, nw, nch);
+                    "recurrence: no variant with cluster %d, %d windows per chunk, %d chunks, "
+                    "%d threads",
+                    cluster, nw, nch, threads);
     return max_active_clusters(*v, out);
 }
 

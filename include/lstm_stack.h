@@ -198,23 +198,26 @@ int lstm_recurrence(const float *g, const float *rp, const float *bias,
  * A cluster of cluster_size blocks splits the 128 hidden units; each 8-lane
  * group of a block holds one unit's weights for a K chunk and runs `chunks`
  * independent chunks of windows_per_chunk windows.  Windows per cluster =
- * (block threads / 8) / (128 / cluster_size) * windows_per_chunk * chunks
- * (256 threads per block, 512 for clusters of 2).  Variants:
- * (16|8, 1|2|4|8, 1), (4, 1|2, 1), (2, 1, 1), (4, 1, 2|4|8), (4, 2, 2|4|8),
- * (8, 2, 4).  Every variant computes the same sums in the same order, so all
- * give bitwise identical y (the pages' three recurrence kernels are likewise
- * bitwise identical, lstmproj.rs module docs).  Errors as lstm_recurrence,
- * plus LSTM_E_INVALID for an unknown variant. */
+ * (threads_per_block / 8) / (128 / cluster_size) * windows_per_chunk * chunks.
+ * threads_per_block 0 selects the default (256; 512 for clusters of 2).
+ * Variants (cluster, windows_per_chunk, chunks, threads): (16|8, 1|2|4|8, 1,
+ * 0), (4, 1|2, 1, 0), (2, 1, 1, 0), (4, 1, 2|4|8, 0), (4, 2, 2|4|8, 0),
+ * (8, 2, 4, 0), and the narrow (8, 1|2, 1, 128), (16, 1|2, 1, 64).  Every
+ * variant computes the same sums in the same order, so all give bitwise
+ * identical y (the pages' three recurrence kernels are likewise bitwise
+ * identical, lstmproj.rs module docs).  Errors as lstm_recurrence, plus
+ * LSTM_E_INVALID for an unknown variant. */
 int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
                             float *y, int batch, int steps, int direction,
                             int cluster_size, int windows_per_chunk, int chunks,
-                            void *stream);
+                            int threads_per_block, void *stream);
 
-/* How many clusters of a recurrence variant `device` can run at once
- * (cudaOccupancyMaxActiveClusters).  Errors: LSTM_E_INVALID (null, unknown
- * variant), LSTM_E_DEVICE, LSTM_E_CUDA. */
+/* How many clusters of a recurrence variant (as above) `device` can run at
+ * once (cudaOccupancyMaxActiveClusters).  Errors: LSTM_E_INVALID (null,
+ * unknown variant), LSTM_E_DEVICE, LSTM_E_CUDA. */
 int lstm_recurrence_max_clusters(int cluster_size, int windows_per_chunk,
-                                 int chunks, int device, int *max_clusters);
+                                 int chunks, int threads_per_block, int device,
+                                 int *max_clusters);
 
 /* One bidirectional layer (projection, then the forward and the reverse
  * recurrence, all on `stream`) that allocates no device memory.  The paper

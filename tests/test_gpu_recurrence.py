@@ -10,9 +10,10 @@ from gpu_util import assert_within, cuda
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [(16, 1, 1), (16, 2, 1), (16, 4, 1), (16, 8, 1), (8, 1, 1), (8, 2, 1), (8, 4, 1),
-            (8, 8, 1), (4, 1, 1), (4, 2, 1), (2, 1, 1), (4, 1, 2), (4, 1, 4), (4, 1, 8),
-            (4, 2, 2), (4, 2, 4), (4, 2, 8), (8, 2, 4)]
+VARIANTS = [(16, 1, 1, 0), (16, 2, 1, 0), (16, 4, 1, 0), (16, 8, 1, 0), (8, 1, 1, 0),
+            (8, 2, 1, 0), (8, 4, 1, 0), (8, 8, 1, 0), (4, 1, 1, 0), (4, 2, 1, 0), (2, 1, 1, 0),
+            (4, 1, 2, 0), (4, 1, 4, 0), (4, 1, 8, 0), (4, 2, 2, 0), (4, 2, 4, 0), (4, 2, 8, 0),
+            (8, 2, 4, 0), (8, 1, 1, 128), (8, 2, 1, 128), (16, 1, 1, 64), (16, 2, 1, 64)]
 
 
 def _layer_inputs(batch, steps, layer_index=0, seed=21, scale=1.0):
@@ -83,7 +84,7 @@ def test_unknown_variant_is_rejected():
     b = torch.zeros(512, device="cuda")
     y = torch.zeros((1, 4, 256), device="cuda")
     with pytest.raises(binding.LSTMError) as e:
-        binding.lstm_recurrence_variant(g, rp, b, y, 1, 4, 0, 3, 1, 1)
+        binding.lstm_recurrence_variant(g, rp, b, y, 1, 4, 0, 3, 1, 1, 0)
     assert e.value.code == binding.LSTM_E_INVALID
 
 
@@ -92,4 +93,4 @@ def test_max_clusters_query():
         n = binding.lstm_recurrence_max_clusters(*v)
         assert n >= 1, (v, n)
     with pytest.raises(binding.LSTMError):
-        binding.lstm_recurrence_max_clusters(3, 1, 1)
+        binding.lstm_recurrence_max_clusters(3, 1, 1, 0)
