@@ -19,11 +19,12 @@
 //   3. add the prefetched projection value and the bias, apply the bounded
 //      activations, gather the four gates of a window (shuffles), update c
 //      and h (c stays in registers);
-//   4. gather the h of the warp's four consecutive units, write them to y
-//      (one float4) and push them into the next-step h buffer of every CTA
-//      of the cluster with one 16-byte st.async each (distributed shared
-//      memory), which credits the receiving CTA's mbarrier for that buffer
-//      with the bytes written; padding windows past the batch send nothing;
+//   4. gather the h of the warp's four consecutive units, push them into the
+//      next-step h buffer of every CTA of the cluster with one 16-byte
+//      st.async each (distributed shared memory), which credits the
+//      receiving CTA's mbarrier for that buffer with the bytes written, then
+//      write them to y (one float4); padding windows past the batch send
+//      nothing;
 //   5. before reading a buffer, wait on its mbarrier: the phase completes when
 //      all 128 x (tile) values of the step have landed.
 // Two h buffers alternate by step parity.  The exchange is one-sided: no
@@ -191,6 +192,21 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     const int bch0 = tile_w0 + wbase;  // window of chunk 0, w = 0
     const uint32_t send_off0 = static_cast<uint32_t>(
         ((wbase + wl) * HROW + (u0 / KLEN) * CHUNK_STRIDE + (u0 % KLEN)) * 4);
+    // the peers this lane sends to, and their h buffers and mbarriers for
+    // both parities, as cluster addresses (a peer's shared memory is one
+    // contiguous window, so offsets within it carry over)
+    constexpr int NPEER = (C + 4 * REPL - 1) / (4 * REPL);
+    uint32_t rdst[NPEER][2], rbar[NPEER][2];
+#pragma unroll
+    for (int r = 0; r < NPEER; ++r) {
+        const int peer = min(sender + r * 4 * REPL, C - 1);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            rdst[r][q] = ptx::map_to_rank(
+                hbase + static_cast<uint32_t>(q * TW * HROW * 4) + send_off0, peer);
+            rbar[r][q] = ptx::map_to_rank(bar_base + static_cast<uint32_t>(q * 8), peer);
+        }
+    }
 
     float gq[PFD][NCH][HV];
     auto gload = [&](int s, float (&dst)[NCH][HV]) {
@@ -304,10 +320,8 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                 h[ch] = gate[3] * tanh_bounded(c[ch]);
             }
 
-            // 4. gather the warp's four units of window wl, store them to y and
-            //    push them (16 bytes) into every CTA's next h buffer
-            const uint32_t dst_par = hbase + static_cast<uint32_t>((par ^ 1) * TW * HROW * 4);
-            const uint32_t bar = bar_base + static_cast<uint32_t>((par ^ 1) * 8);
+            // 4. gather the warp's four units of window wl, push them (16
+            //    bytes) into every CTA's next h buffer and store them to y
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
                 float h4[4];
@@ -315,20 +329,18 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                 for (int j = 0; j < 4; ++j)
                     h4[j] = __shfl_sync(0xffffffffu, h[ch], 8 * j + kc);
                 if (bch0 + ch * NW + wl < batch) {
+                    if (s + 1 < steps) {
+                        const uint32_t off = static_cast<uint32_t>(ch * NW * HROW * 4);
+#pragma unroll
+                        for (int r = 0; r < NPEER; ++r) {
+                            if (sender + r * 4 * REPL < C)
+                                ptx::st_async_v4(rdst[r][par ^ 1] + off, h4[0], h4[1], h4[2],
+                                                 h4[3], rbar[r][par ^ 1]);
+                        }
+                    }
                     if (sender == 0)
                         *reinterpret_cast<float4 *>(ych0 + (ch * row_stride + t) * kOutput) =
                             make_float4(h4[0], h4[1], h4[2], h4[3]);
-                    if (s + 1 < steps) {
-                        const uint32_t dst =
-                            dst_par + send_off0 + static_cast<uint32_t>(ch * NW * HROW * 4);
-#pragma unroll
-                        for (int r = 0; r < (C + 4 * REPL - 1) / (4 * REPL); ++r) {
-                            const int peer = sender + r * 4 * REPL;
-                            if (peer < C)
-                                ptx::st_async_v4(ptx::map_to_rank(dst, peer), h4[0], h4[1], h4[2],
-                                                 h4[3], ptx::map_to_rank(bar, peer));
-                        }
-                    }
                 }
             }
 
