@@ -47,7 +47,8 @@ constexpr int kProjectionWBoxRows = 128;
 // boxes of 16 columns x box_rows rows with the 64-byte swizzle.
 int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols,
                       int box_rows);
-// G[rows][1024] = X . Wp^T in 3xTF32; the maps come from encode_matrix_map.
+// G[rows][1024] = X . Wp^T in 3xTF32; the maps come from encode_matrix_map
+// (G's own store map is encoded per launch).
 int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
                       const CUtensorMap &wlo_map, float *g, int rows, int kp,
                       unsigned *fault, cudaStream_t stream);
@@ -169,6 +170,31 @@ __device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorM
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y),
                  "h"(cta_mask)
                  : "memory");
+}
+// Shared memory -> global through the tensor map; the TMA engine writes only
+// the part of the box inside the tensor.  Tracked by bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// At most N of this thread's bulk groups still reading their shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// At most N of this thread's bulk groups not yet complete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {

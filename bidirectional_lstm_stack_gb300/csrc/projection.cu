@@ -24,9 +24,12 @@
 //    x_hi*w_hi + x_hi*w_lo + x_lo*w_hi, the 3xTF32 split that keeps fp32-level
 //    accuracy (TF32 alone was not accurate enough on some parts, per the
 //    pages' `tf32_projection_accurate`);
-//  * warps 4-7 (epilogue) read a finished accumulator with tcgen05.ld and
-//    store rows of G while the MMA fills the other accumulator, paced by the
-//    MMA's progress through the next tile.
+//  * warps 4-7 (epilogue) read a finished accumulator with tcgen05.ld, write
+//    32-column slices of their 32 rows into a double-buffered shared-memory
+//    staging area (128-byte swizzle, conflict-free) and hand each 4 KiB
+//    slice to the TMA engine as one bulk tensor store, while the MMA fills
+//    the other accumulator; the slices go out paced by the MMA's progress
+//    through the next tile.
 // Every mbarrier wait is bounded in time; a wait that runs out sets a bit in
 // the fault word, every role stops, and the CTA drains its TMA loads and MMAs
 // before it frees tensor memory and returns.
@@ -53,7 +56,10 @@ constexpr int EPILOGUE = 128;                            // warps 4-7
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
-constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int OUT_COLS = 32;                             // G columns per store slice
+constexpr int OUT_BYTES = 32 * OUT_COLS * 4;             // one warp's 32 rows: 4 KiB
+constexpr int OUT_OFFSET = STAGES * STAGE_BYTES;         // staging: 4 warps x 2 slices
+constexpr size_t SMEM_BYTES = OUT_OFFSET + 4 * 2 * OUT_BYTES + 1024 + 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 constexpr int TILES_N = kGateColumns / BN;          // 4
 constexpr int CLUSTER = 2;                          // CTAs sharing a W tile
@@ -103,13 +109,14 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, unsig
 __global__ void __launch_bounds__(THREADS, 1)
 projection_kernel(const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap whi_map,
-                  const __grid_constant__ CUtensorMap wlo_map, float *__restrict__ g, int rows,
+                  const __grid_constant__ CUtensorMap wlo_map,
+                  const __grid_constant__ CUtensorMap g_map, int rows,
                   int kblocks, int pairs, unsigned *fault)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + OUT_OFFSET + 4 * 2 * OUT_BYTES);
     uint64_t *conv = full + STAGES;
     uint64_t *empty = conv + STAGES;
     uint64_t *acc_full = empty + STAGES;      // [2]
@@ -139,6 +146,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         ptx::prefetch_tensormap(&x_map);
         ptx::prefetch_tensormap(&whi_map);
         ptx::prefetch_tensormap(&wlo_map);
+        ptx::prefetch_tensormap(&g_map);
     }
     if (warp == MMA_WARP) {
         ptx::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -258,6 +266,8 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         // epilogue: warp 4+q reads TMEM lanes 32q .. 32q+31 (warp id mod 4 = q)
         const int q = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        uint8_t *out = smem + OUT_OFFSET + q * 2 * OUT_BYTES;
+        int slices = 0;  // store slices this warp issued
         int ti = 0;
         for (int t = first; t < pairs; t += stride, ++ti) {
             const int a = ti & 1;
@@ -268,20 +278,19 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             if (!__all_sync(0xffffffffu, got) || *abort_flag)
                 break;
             ptx::tc_fence_after();
-            const int m0 = ((t / TILES_N) * CLUSTER + rank) * BM;
+            const int m0 = ((t / TILES_N) * CLUSTER + rank) * BM + q * 32;  // this warp's rows
             const int n0 = (t % TILES_N) * BN;
-            const long m = static_cast<long>(m0) + q * 32 + lane;
             const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(a) * ACC_COLS;
-            // Pace the stores: chunk c of this tile goes out once the next
+            // Pace the stores: slice c of this tile goes out once the next
             // tile's mainloop has issued c/8 of its K blocks, so G streams to
             // memory under the next tile's compute instead of every CTA
             // writing its whole tile at once and stalling the loads.
             const bool paced = t + stride < pairs;
             const long next_kb = static_cast<long>(ti + 1) * kblocks;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < BN / OUT_COLS; ++c, ++slices) {
                 if (paced) {
-                    const long want = next_kb + (static_cast<long>(c) * kblocks) / (BN / 32);
+                    const long want = next_kb + (static_cast<long>(c) * kblocks) / (BN / OUT_COLS);
                     if (*progress < want && !*abort_flag) {
                         const uint64_t start = ptx::globaltimer();
                         while (*progress < want && !*abort_flag &&
@@ -290,20 +299,35 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     }
                 }
                 uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(acc + c * 32, r);
+                ptx::tmem_ld_32x32b_x32(acc + c * OUT_COLS, r);
                 ptx::tmem_ld_wait();
-                if (m < rows) {
-                    float4 *dst = reinterpret_cast<float4 *>(g + m * kGateColumns + n0 + c * 32);
+                // the store that last used this buffer (two slices ago) has read it
+                uint8_t *buf = out + (slices & 1) * OUT_BYTES;
+                if (lane == 0)
+                    ptx::bulk_wait_group_read<1>();
+                __syncwarp();
+                // lane = row; 16-byte chunk v of the row goes to chunk v ^ (row % 8)
+                float4 *row = reinterpret_cast<float4 *>(buf + lane * (OUT_COLS * 4));
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                             __uint_as_float(r[4 * v + 2]),
-                                             __uint_as_float(r[4 * v + 3]));
+                for (int v = 0; v < 8; ++v)
+                    row[v ^ (lane & 7)] =
+                        make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (m0 < rows)
+                        ptx::tma_store_2d(&g_map, buf, n0 + c * OUT_COLS, m0);
+                    ptx::bulk_commit_group();
                 }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&acc_empty[a]);
         }
+        // the staging buffers stay valid until the stores have completed
+        if (lane == 0)
+            ptx::bulk_wait_group<0>();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -350,7 +374,9 @@ int g_max_clusters[64] = {};  // clusters of the projection a device runs at onc
 
 } // namespace
 
-int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols, int box_rows)
+namespace {
+int encode_map(CUtensorMap *map, const float *base, long rows, int cols, int box_cols,
+               int box_rows, CUtensorMapSwizzle swizzle)
 {
     auto encode = encode_fn();
     if (!encode)
@@ -361,16 +387,21 @@ int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols, 
         return fail(LSTM_E_INVALID, "row pitch %d bytes is not a multiple of 16", cols * 4);
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(LSTM_E_CUDA, "cuTensorMapEncodeTiled failed (%d) for %ld x %d", (int)r, rows,
                     cols);
     return LSTM_OK;
+}
+}  // namespace
+
+int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols, int box_rows)
+{
+    return encode_map(map, base, rows, cols, BK, box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int projection_prepare(int device)
@@ -439,10 +470,14 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // G is written in 32 x 32 slices (one epilogue warp's rows), 128-byte swizzle
+    CUtensorMap g_map;
+    if ((st = encode_map(&g_map, g, rows, kGateColumns, OUT_COLS, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
     const int kblocks = kp / BK;
     const int npairs = static_cast<int>(pairs);
-    return cuda_status(cudaLaunchKernelEx(&cfg, projection_kernel, x_map, whi_map, wlo_map, g, rows,
-                                          kblocks, npairs, fault),
+    return cuda_status(cudaLaunchKernelEx(&cfg, projection_kernel, x_map, whi_map, wlo_map, g_map,
+                                          rows, kblocks, npairs, fault),
                        "projection launch");
 }
 

@@ -29,9 +29,13 @@ def test_projection_matches_oracle(weights, in_width, rows):
     kp = 64 if in_width == 60 else 256
     wp_hi, wp_lo, _, _ = binding.lstm_pack_layer(layer["w"], layer["r"], layer["b"], in_width, kp)
     x = synthetic.random_matrix(100 + rows + in_width, (rows, in_width))
-    g = torch.full((rows, 1024), float("nan"), device="cuda")
+    # guard rows past the end must stay untouched (the ragged last tile)
+    guard = 37
+    g_all = torch.full((rows + guard, 1024), float("nan"), device="cuda")
+    g = g_all[:rows]
     binding.lstm_projection(cuda(x), rows, in_width, cuda(wp_hi), cuda(wp_lo), kp, g)
     torch.cuda.synchronize()
+    assert torch.isnan(g_all[rows:]).all()
     ref = oracle.projection(x, layer["w"])
     # 3xTF32 keeps fp32-level accuracy: a single TF32 product would miss this
     # bound by ~100x
