@@ -16,8 +16,10 @@ Pins (the checks that tie the oracle to something other than itself) live in
 ``tests/test_oracle_pins.py``: zero weights, the R = 0 closed form, reverse
 equals forward on time-reversed input, a saturated-gate counter whose outputs
 are tanh of integers (``tests/golden/saturated_counter.json``), a one-hot
-projection, and agreement with ``torch.nn.LSTM`` in float64.  No oracle
-function is "parity unpinned".
+projection, and agreement with ``torch.nn.LSTM`` in float64; for the TF32
+projection mode, the rounding against a bit-level definition and the TF32
+stack against the float64 stack on pre-rounded operands.  No oracle function
+is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -61,12 +63,15 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _dptr, ctypes.c_long, _dptr, _dptr, _dptr, _dptr,
                 ctypes.c_int, _dptr, ctypes.c_long]
-            lib.oracle_lstm_stack.argtypes = [
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                ctypes.c_int, _dptr, ctypes.POINTER(_dptr),
-                ctypes.POINTER(_dptr), ctypes.POINTER(_dptr), _dptr]
-            lib.oracle_projection.argtypes = [
-                ctypes.c_long, ctypes.c_int, ctypes.c_int, _dptr, _dptr, _dptr]
+            for f in (lib.oracle_lstm_stack, lib.oracle_lstm_stack_tf32):
+                f.argtypes = [
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                    ctypes.c_int, _dptr, ctypes.POINTER(_dptr),
+                    ctypes.POINTER(_dptr), ctypes.POINTER(_dptr), _dptr]
+            for f in (lib.oracle_projection, lib.oracle_projection_tf32):
+                f.argtypes = [
+                    ctypes.c_long, ctypes.c_int, ctypes.c_int, _dptr, _dptr, _dptr]
+            lib.oracle_tf32_array.argtypes = [ctypes.c_long, _dptr, _dptr]
             lib.oracle_recurrence.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, _dptr, _dptr, _dptr,
                 _dptr]
@@ -105,14 +110,26 @@ def lstm_direction(x, W, R, Wb, Rb, reverse: bool) -> np.ndarray:
     return h
 
 
-def lstm_stack(x, layers) -> np.ndarray:
+def tf32(v) -> np.ndarray:
+    """``v`` rounded to TF32 (10 stored mantissa bits, to nearest, ties away
+    from zero), as float64."""
+    v = _f64(v)
+    out = np.empty_like(v)
+    _load().oracle_tf32_array(v.size, _p(v), _p(out))
+    return out
+
+
+def lstm_stack(x, layers, projection: str = "f64") -> np.ndarray:
     """The bidirectional stack.
 
     x ``[B, T, in0]``; ``layers`` is a sequence of dicts with ``w``
     ``[2, 4H, in_l]``, ``r`` ``[2, 4H, H]`` and ``b`` ``[2, 8H]`` (per
     direction Wb then Rb).  Returns y ``[B, T, 2H]`` =
-    concat(forward h, reverse h) of the last layer.
+    concat(forward h, reverse h) of the last layer.  ``projection="tf32"``
+    rounds both factors of every input-projection product to TF32 (the
+    method's TF32 projection mode); everything else stays float64.
     """
+    assert projection in ("f64", "tf32"), projection
     x = _f64(x)
     B, T, in0 = x.shape
     L = len(layers)
@@ -127,25 +144,26 @@ def lstm_stack(x, layers) -> np.ndarray:
         assert b.shape == (2, 8 * H), (i, b.shape)
     y = np.zeros((B, T, 2 * H), dtype=np.float64)
     arr = _dptr * L
-    _load().oracle_lstm_stack(B, T, in0, H, L, _p(x),
-                              arr(*[_p(w) for w in ws]),
-                              arr(*[_p(r) for r in rs]),
-                              arr(*[_p(b) for b in bs]), _p(y))
+    fn = _load().oracle_lstm_stack if projection == "f64" else _load().oracle_lstm_stack_tf32
+    fn(B, T, in0, H, L, _p(x), arr(*[_p(w) for w in ws]), arr(*[_p(r) for r in rs]),
+       arr(*[_p(b) for b in bs]), _p(y))
     return y
 
 
-def projection(X, W) -> np.ndarray:
+def projection(X, W, tf32: bool = False) -> np.ndarray:
     """Packed-column input projection of one layer, both directions.
 
     X ``[M, in]``, W ``[2, 4H, in]``.  Returns G ``[M, 8H]`` with
-    ``G[m, d*4H + 4u + k] = sum_j X[m, j] * W[d, k*H + u, j]`` (no bias).
+    ``G[m, d*4H + 4u + k] = sum_j X[m, j] * W[d, k*H + u, j]`` (no bias);
+    with ``tf32`` both factors of each product are rounded to TF32 first.
     """
     X, W = _f64(X), _f64(W)
     M, inw = X.shape
     H = W.shape[1] // 4
     assert W.shape == (2, 4 * H, inw)
     G = np.zeros((M, 8 * H), dtype=np.float64)
-    _load().oracle_projection(M, inw, H, _p(X), _p(W), _p(G))
+    fn = _load().oracle_projection_tf32 if tf32 else _load().oracle_projection
+    fn(M, inw, H, _p(X), _p(W), _p(G))
     return G
 
 

@@ -28,7 +28,16 @@
  *  - the reverse direction at time t writes output row t (not time-flipped).
  *
  * Everything is plain float64 with libm exp/tanh; loops follow the
- * definition with no blocking or reordering.  Windows are independent, so the
+ * definition with no blocking or reordering.
+ *
+ * TF32 projection mode (lstmproj.rs `CudaMath::Tf32` and `projection_rule`:
+ * the projection's products on TF32 tensor cores, the recurrence in FP32):
+ * the `_tf32` entry points round both factors of every input-projection
+ * product, W and the layer input, to TF32 before multiplying; the sums, the
+ * recurrent term and the cell stay float64.  TF32 keeps fp32's sign and
+ * 8-bit exponent and 10 explicit mantissa bits.  The pages do not say how
+ * values are rounded to it; the reading taken is round to nearest with ties
+ * away from zero, the rounding of the fp32-to-TF32 conversion instruction.  Windows are independent, so the
  * stack loop runs them (and the two directions) in parallel with OpenMP.
  */
 #include <math.h>
@@ -39,6 +48,26 @@
 #endif
 
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/*
+ * v rounded to TF32 (11 significant bits: the implicit one and 10 stored),
+ * to nearest, ties away from zero.  For zero and for finite values in the
+ * normal fp32 range; the LSTM's weights, inputs and hidden states are.
+ */
+double oracle_tf32(double v)
+{
+    if (v == 0.0 || !isfinite(v))
+        return v;
+    int e;
+    double m = frexp(v, &e);                   /* v = m * 2^e, 0.5 <= |m| < 1 */
+    return ldexp(round(ldexp(m, 11)), e - 11); /* round(): halves away from 0 */
+}
+
+void oracle_tf32_array(long n, const double *v, double *out)
+{
+    for (long i = 0; i < n; ++i)
+        out[i] = oracle_tf32(v[i]);
+}
 
 int oracle_threads(void)
 {
@@ -77,11 +106,11 @@ static void cell_update(int H, const double *z, double *c, double *h)
  * The forward direction visits t = 0..T-1, the reverse one t = T-1..0;
  * each visit uses the hidden state of the previously visited step.
  */
-void oracle_lstm_direction(int T, int in, int H,
-                           const double *x, long x_stride,
-                           const double *W, const double *R,
-                           const double *Wb, const double *Rb,
-                           int reverse, double *h_out, long h_stride)
+static void direction(int T, int in, int H,
+                      const double *x, long x_stride,
+                      const double *W, const double *R,
+                      const double *Wb, const double *Rb,
+                      int reverse, double *h_out, long h_stride, int tf32)
 {
     double *z = malloc(sizeof(double) * 4 * H);
     double *h = calloc(H, sizeof(double));
@@ -92,7 +121,8 @@ void oracle_lstm_direction(int T, int in, int H,
         for (int r = 0; r < 4 * H; ++r) {
             double acc = Wb[r] + Rb[r];
             for (int j = 0; j < in; ++j)
-                acc += W[(long)r * in + j] * xt[j];
+                acc += tf32 ? oracle_tf32(W[(long)r * in + j]) * oracle_tf32(xt[j])
+                            : W[(long)r * in + j] * xt[j];
             for (int j = 0; j < H; ++j)
                 acc += R[(long)r * H + j] * h[j];
             z[r] = acc;
@@ -105,6 +135,15 @@ void oracle_lstm_direction(int T, int in, int H,
     free(c);
 }
 
+void oracle_lstm_direction(int T, int in, int H,
+                           const double *x, long x_stride,
+                           const double *W, const double *R,
+                           const double *Wb, const double *Rb,
+                           int reverse, double *h_out, long h_stride)
+{
+    direction(T, in, H, x, x_stride, W, R, Wb, Rb, reverse, h_out, h_stride, 0);
+}
+
 /*
  * The whole bidirectional stack.
  *   x      : [B][T][in0]
@@ -114,10 +153,10 @@ void oracle_lstm_direction(int T, int in, int H,
  *   y      : [B][T][2H]      last layer's concat(forward h, reverse h)
  * Layer l+1 reads layer l's [B][T][2H] output.
  */
-void oracle_lstm_stack(int B, int T, int in0, int H, int L,
-                       const double *x,
-                       const double *const *w, const double *const *r,
-                       const double *const *b, double *y)
+static void stack(int B, int T, int in0, int H, int L,
+                  const double *x,
+                  const double *const *w, const double *const *r,
+                  const double *const *b, double *y, int tf32)
 {
     long plane = (long)B * T * 2 * H;
     double *cur = malloc(sizeof(double) * plane);
@@ -129,20 +168,35 @@ void oracle_lstm_stack(int B, int T, int in0, int H, int L,
         #pragma omp parallel for collapse(2) schedule(dynamic, 1)
         for (int bb = 0; bb < B; ++bb) {
             for (int d = 0; d < 2; ++d) {
-                oracle_lstm_direction(
+                direction(
                     T, in, H,
                     src + (long)bb * T * in, in,
                     w[l] + (long)d * 4 * H * in,
                     r[l] + (long)d * 4 * H * H,
                     b[l] + (long)d * 8 * H,
                     b[l] + (long)d * 8 * H + 4 * H,
-                    d, dst + (long)bb * T * 2 * H + d * H, 2 * H);
+                    d, dst + (long)bb * T * 2 * H + d * H, 2 * H, tf32);
             }
         }
         double *t = cur; cur = nxt; nxt = t;
     }
     free(cur);
     free(nxt);
+}
+
+void oracle_lstm_stack(int B, int T, int in0, int H, int L, const double *x,
+                       const double *const *w, const double *const *r,
+                       const double *const *b, double *y)
+{
+    stack(B, T, in0, H, L, x, w, r, b, y, 0);
+}
+
+/* The stack with TF32 input-projection products (see the header). */
+void oracle_lstm_stack_tf32(int B, int T, int in0, int H, int L, const double *x,
+                            const double *const *w, const double *const *r,
+                            const double *const *b, double *y)
+{
+    stack(B, T, in0, H, L, x, w, r, b, y, 1);
 }
 
 /*
@@ -154,8 +208,8 @@ void oracle_lstm_stack(int B, int T, int in0, int H, int L,
  * No bias is added here.
  *   X : [M][in],  W : [2][4H][in],  G : [M][8H]
  */
-void oracle_projection(long M, int in, int H, const double *X,
-                       const double *W, double *G)
+static void projection(long M, int in, int H, const double *X,
+                       const double *W, double *G, int tf32)
 {
     #pragma omp parallel for schedule(static)
     for (long m = 0; m < M; ++m) {
@@ -165,12 +219,25 @@ void oracle_projection(long M, int in, int H, const double *X,
                     const double *wr = W + ((long)d * 4 * H + (long)k * H + u) * in;
                     double acc = 0.0;
                     for (int j = 0; j < in; ++j)
-                        acc += X[m * in + j] * wr[j];
+                        acc += tf32 ? oracle_tf32(X[m * in + j]) * oracle_tf32(wr[j])
+                                    : X[m * in + j] * wr[j];
                     G[m * 8 * H + d * 4 * H + 4 * u + k] = acc;
                 }
             }
         }
     }
+}
+
+void oracle_projection(long M, int in, int H, const double *X, const double *W, double *G)
+{
+    projection(M, in, H, X, W, G, 0);
+}
+
+/* The projection with both factors of each product rounded to TF32. */
+void oracle_projection_tf32(long M, int in, int H, const double *X, const double *W,
+                            double *G)
+{
+    projection(M, in, H, X, W, G, 1);
 }
 
 /*

@@ -15,7 +15,11 @@ packed column) fails at least one of them:
   integers (tests/golden/saturated_counter.json);
 * agreement with torch.nn.LSTM in float64 (a library routine with the same
   i,f,g,o gate blocks and separate input/recurrent biases);
-* the packed projection against a one-hot W and against numpy's matmul.
+* the packed projection against a one-hot W and against numpy's matmul;
+* TF32 projection mode: the oracle's rounding against a definition written
+  on the bit layout (keep sign, exponent and the top 10 mantissa bits; the
+  dropped bits at or above half round the magnitude up), and the TF32 stack
+  against the float64 stack run layer by layer on operands rounded that way.
 """
 import json
 import os
@@ -277,3 +281,60 @@ def test_recurrence_of_projection_is_the_layer():
 
 def test_oracle_threads_positive():
     assert oracle.threads() >= 1
+
+
+# ---- TF32 projection mode -------------------------------------------------
+
+def _tf32_bits(v):
+    """TF32 rounding of float64 values from their bit layout: keep the sign,
+    the exponent and the top 10 of the 52 mantissa bits; if the 42 dropped
+    bits are at least half of the kept unit, add one kept unit to the
+    magnitude (the carry may run into the exponent).  Ties go away from 0."""
+    b = np.ascontiguousarray(v, dtype=np.float64).view(np.uint64)
+    unit = np.uint64(1) << np.uint64(42)
+    low = b & (unit - np.uint64(1))
+    kept = b - low
+    out = np.where(low >= (unit >> np.uint64(1)), kept + unit, kept)
+    return out.view(np.float64)
+
+
+def test_tf32_rounding_against_bit_definition():
+    rng = np.random.default_rng(31)
+    # fp32 values over many binades, plus exact ties and values a hair off them
+    v = (rng.standard_normal(20000) * np.exp2(rng.integers(-60, 60, 20000))).astype(np.float32)
+    base = rng.integers(1 << 10, 1 << 11, 500).astype(np.float64)
+    ties = np.concatenate([(base + 0.5) * 2.0 ** -10, -(base + 0.5) * 2.0 ** -3,
+                           (base + 0.5 - 2.0 ** -20) * 2.0 ** 4, (base + 0.5 + 2.0 ** -20)])
+    for vals in (v.astype(np.float64), ties, rng.standard_normal(5000)):
+        got = oracle.tf32(vals)
+        np.testing.assert_array_equal(got, _tf32_bits(vals))
+    # hand cases: 1 + 2^-11 is a tie (away: 1 + 2^-10); 1 + 2^-12 rounds down
+    np.testing.assert_array_equal(
+        oracle.tf32([1 + 2.0 ** -11, 1 + 2.0 ** -12, -(1 + 2.0 ** -11), 2 - 2.0 ** -12, 0.0]),
+        [1 + 2.0 ** -10, 1.0, -(1 + 2.0 ** -10), 2.0, 0.0])
+
+
+def test_tf32_projection_is_projection_of_rounded_operands():
+    rng = np.random.default_rng(32)
+    H, inw, M = 8, 20, 17
+    X = rng.standard_normal((M, inw)).astype(np.float32).astype(np.float64)
+    W = rng.uniform(-0.2, 0.2, (2, 4 * H, inw)).astype(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(oracle.projection(X, W, tf32=True),
+                                  oracle.projection(_tf32_bits(X), _tf32_bits(W)))
+    assert np.abs(oracle.projection(X, W, tf32=True) - oracle.projection(X, W)).max() > 1e-6
+
+
+def test_tf32_stack_is_float64_stack_on_rounded_operands():
+    # layer by layer: each layer's TF32 products equal the float64 layer run
+    # on its input and W rounded to TF32 (R and the biases untouched)
+    rng = np.random.default_rng(33)
+    H, in0, B, T = 6, 5, 2, 7
+    lays = _layers(rng, H, in0, 3)
+    x = rng.standard_normal((B, T, in0))
+    cur = x
+    for lay in lays:
+        rounded = dict(lay, w=_tf32_bits(lay["w"]))
+        cur = oracle.lstm_stack(_tf32_bits(cur), [rounded])
+    y = oracle.lstm_stack(x, lays, projection="tf32")
+    np.testing.assert_array_equal(y, cur)
+    assert np.abs(y - oracle.lstm_stack(x, lays)).max() > 1e-6
