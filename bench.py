@@ -295,6 +295,13 @@ def run_ours(args):
     ms1, ph1, _ = time_stack(stack, x1, max(args.steps, 10), args.warmup, flush, stream)
     ms1_step = max_over_ranks(float(np.mean(ms1)), device=torch.device("cuda", dev))
 
+    # the opt-in single-product TF32 projection mode on the same workload (the
+    # fp32-accurate 3xTF32 mode above is the headline)
+    binding.lstm_stack_set_math(stack.handle, binding.LSTM_MATH_TF32)
+    ms_t, ph_t, _ = time_stack(stack, x, args.steps, args.warmup, flush, stream)
+    binding.lstm_stack_set_math(stack.handle, binding.LSTM_MATH_3XTF32)
+    tf32_s = max_over_ranks(sum(ms_t) / 1e3, device=torch.device("cuda", dev))
+
     # end to end through the host-buffer entry point (pinned host memory)
     xp = torch.from_numpy(x_host).pin_memory()
     yp = torch.empty((wl.batch, wl.steps, 2 * H), dtype=torch.float32).pin_memory()
@@ -377,6 +384,9 @@ def run_ours(args):
                                                f"(TF32) / 3 (3xTF32)",
                                 "frac_of_tf32_microbenchmark":
                                     proj_achieved / (TF32_MICROBENCHMARK_TFLOPS / 3.0)},
+        "tf32_mode": {"windows_per_s": wl.batch * world * args.steps / tf32_s,
+                      "ms_per_step": tf32_s * 1e3 / args.steps,
+                      "projection_ms": [round(float(v), 4) for v in ph_t[:, 0]]},
         "e2e": {"value": e2e_value, "unit": "windows/s",
                 "h2d_bytes_per_step": int(xn.nbytes), "d2h_bytes_per_step": int(yn.nbytes)},
         "gpu_launches": 12 * args.steps,

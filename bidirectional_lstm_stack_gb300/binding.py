@@ -29,6 +29,8 @@ LSTM_E_DEVICE = 4
 LSTM_E_CUDA = 5
 LSTM_E_ALLOC = 6
 LSTM_E_FAULT = 7
+LSTM_MATH_3XTF32 = 0
+LSTM_MATH_TF32 = 1
 
 _c_float_p = ctypes.POINTER(ctypes.c_float)
 _vp = ctypes.c_void_p
@@ -68,11 +70,13 @@ def load():
             "lstm_stack_forward_host": (i, [_vp, _vp, sz, _vp, sz, i, i, _vp]),
             "lstm_stack_enable_phase_timing": (i, [_vp, i]),
             "lstm_stack_set_graphs": (i, [_vp, i]),
+            "lstm_stack_set_math": (i, [_vp, i]),
             "lstm_stack_phase_times": (i, [_vp, _c_float_p]),
             "lstm_stack_destroy": (None, [_vp]),
             "lstm_stack_last_error": (ctypes.c_char_p, []),
             "lstm_pack_layer": (i, [_vp, _vp, _vp, i, i, _vp, _vp, _vp, _vp]),
             "lstm_projection": (i, [_vp, i, i, _vp, _vp, i, _vp, _vp]),
+            "lstm_projection_math": (i, [_vp, i, i, _vp, _vp, i, _vp, i, _vp]),
             "lstm_recurrence": (i, [_vp, _vp, _vp, _vp, i, i, i, _vp]),
             "lstm_recurrence_variant": (i, [_vp, _vp, _vp, _vp, i, i, i, i, i, i, i, _vp]),
             "lstm_recurrence_max_clusters": (i, [i, i, i, i, i, ctypes.POINTER(i)]),
@@ -131,6 +135,15 @@ def lstm_projection(x, rows: int, in_width: int, wp_hi, wp_lo, kp: int, g, strea
     """G = X . Wp^T on the device (torch CUDA tensors)."""
     _check(load().lstm_projection(_ptr(x), rows, in_width, _ptr(wp_hi), _ptr(wp_lo), kp, _ptr(g),
                                   _stream(stream, x.device)))
+
+
+def lstm_projection_math(x, rows: int, in_width: int, wp_hi, wp_lo, kp: int, g, math: int,
+                         stream=None):
+    """G = X . Wp^T with the chosen products (LSTM_MATH_*); wp_lo may be None
+    for LSTM_MATH_TF32."""
+    _check(load().lstm_projection_math(_ptr(x), rows, in_width, _ptr(wp_hi),
+                                       _ptr(wp_lo), kp, _ptr(g), math,
+                                       _stream(stream, x.device)))
 
 
 def lstm_recurrence(g, rp, bias, y, batch: int, steps: int, direction: int, stream=None):
@@ -203,6 +216,10 @@ def lstm_stack_forward_host(handle, x: np.ndarray, y: np.ndarray, batch: int, st
 
 def lstm_stack_set_graphs(handle, enable: bool = True):
     _check(load().lstm_stack_set_graphs(handle, int(bool(enable))))
+
+
+def lstm_stack_set_math(handle, math: int):
+    _check(load().lstm_stack_set_math(handle, math))
 
 
 def lstm_stack_enable_phase_timing(handle, enable: bool = True):

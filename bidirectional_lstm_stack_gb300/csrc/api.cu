@@ -201,6 +201,7 @@ struct lstm_stack {
         float *y = nullptr;
         int batch = 0, steps = 0;
         bool timing = false;
+        int math = LSTM_MATH_3XTF32;
         cudaGraphExec_t exec = nullptr;
         unsigned long long used = 0;
     };
@@ -209,6 +210,7 @@ struct lstm_stack {
     unsigned long long uses = 0;
     bool use_graphs = true;
     cudaStream_t capture = nullptr;
+    int math = LSTM_MATH_3XTF32;  // projection products
 };
 
 extern "C" const char *lstm_stack_last_error(void)
@@ -442,7 +444,7 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
         if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 0, 0), stream, cudaEventRecordExternal), "event")))
             return st;
         st = launch_projection(src, s->map_whi[l], s->map_wlo[l], s->gates, static_cast<int>(rows),
-                               s->kp[l], s->fault, stream);
+                               s->kp[l], s->math, s->fault, stream);
         if (st != LSTM_OK)
             return st;
         if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 0, 1), stream, cudaEventRecordExternal), "event")))
@@ -480,7 +482,7 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
 namespace {
 
 // Runs the forward pass on `stream` by replaying a CUDA graph of it: the
-// first call with a given (x, y, batch, steps, timing) records the launches
+// first call with a given (x, y, batch, steps, timing, math) records the launches
 // and the fork/join events on a private stream and instantiates the graph;
 // later calls only launch it.  When `stream` is itself being captured (the
 // caller is building a graph) or replay is off, the launches are enqueued
@@ -497,7 +499,7 @@ int forward_replay(lstm_stack *s, const float *x, float *y, int batch, int steps
     lstm_stack::Graph *hit = nullptr, *victim = &s->graphs[0];
     for (auto &gr : s->graphs) {
         if (gr.exec && gr.x == x && gr.y == y && gr.batch == batch && gr.steps == steps &&
-            gr.timing == s->timing) {
+            gr.timing == s->timing && gr.math == s->math) {
             hit = &gr;
             break;
         }
@@ -526,7 +528,7 @@ int forward_replay(lstm_stack *s, const float *x, float *y, int batch, int steps
         cudaGraphDestroy(graph);
         if (st != LSTM_OK)
             return st;
-        *victim = lstm_stack::Graph{x, y, batch, steps, s->timing, exec, 0};
+        *victim = lstm_stack::Graph{x, y, batch, steps, s->timing, s->math, exec, 0};
         hit = victim;
     }
     hit->used = ++s->uses;
@@ -540,6 +542,16 @@ extern "C" int lstm_stack_set_graphs(lstm_stack *s, int enable)
     if (!s)
         return fail(LSTM_E_INVALID, "set_graphs: null stack");
     s->use_graphs = enable != 0;
+    return LSTM_OK;
+}
+
+extern "C" int lstm_stack_set_math(lstm_stack *s, int math)
+{
+    if (!s)
+        return fail(LSTM_E_INVALID, "set_math: null stack");
+    if (math != LSTM_MATH_3XTF32 && math != LSTM_MATH_TF32)
+        return fail(LSTM_E_INVALID, "set_math: unknown math mode %d", math);
+    s->math = math;
     return LSTM_OK;
 }
 
@@ -619,6 +631,17 @@ extern "C" int lstm_stack_phase_times(lstm_stack *s, float *ms)
 extern "C" int lstm_projection(const float *x, int rows, int in_width, const float *wp_hi,
                                const float *wp_lo, int kp, float *g, void *stream)
 {
+    return lstm_projection_math(x, rows, in_width, wp_hi, wp_lo, kp, g, LSTM_MATH_3XTF32, stream);
+}
+
+extern "C" int lstm_projection_math(const float *x, int rows, int in_width, const float *wp_hi,
+                                    const float *wp_lo, int kp, float *g, int math, void *stream)
+{
+    if (math != LSTM_MATH_3XTF32 && math != LSTM_MATH_TF32)
+        return fail(LSTM_E_INVALID, "lstm_projection: unknown math mode %d", math);
+    // the single-product mode never reads the lo plane
+    if (math == LSTM_MATH_TF32 && !wp_lo)
+        wp_lo = wp_hi;
     if (!x || !wp_hi || !wp_lo || !g)
         return fail(LSTM_E_INVALID, "lstm_projection: null pointer");
     if (rows <= 0 || in_width <= 0 || in_width > kp || kp % 32 != 0)
@@ -642,7 +665,8 @@ extern "C" int lstm_projection(const float *x, int rows, int in_width, const flo
         (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionWBoxRows)) ||
         (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionWBoxRows)))
         return st;
-    return launch_projection(xm, hm, lm, g, rows, kp, fault, static_cast<cudaStream_t>(stream));
+    return launch_projection(xm, hm, lm, g, rows, kp, math, fault,
+                             static_cast<cudaStream_t>(stream));
 }
 
 namespace {

@@ -47,10 +47,11 @@ constexpr int kProjectionWBoxRows = 128;
 // boxes of 16 columns x box_rows rows with the 64-byte swizzle.
 int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols,
                       int box_rows);
-// G[rows][1024] = X . Wp^T in 3xTF32; the maps come from encode_matrix_map
-// (G's own store map is encoded per launch).
+// G[rows][1024] = X . Wp^T in 3xTF32 (math LSTM_MATH_3XTF32) or with single
+// TF32 products (LSTM_MATH_TF32, wlo_map unused); the maps come from
+// encode_matrix_map (G's own store map is encoded per launch).
 int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                      const CUtensorMap &wlo_map, float *g, int rows, int kp,
+                      const CUtensorMap &wlo_map, float *g, int rows, int kp, int math,
                       unsigned *fault, cudaStream_t stream);
 int projection_prepare(int device);
 

@@ -23,7 +23,9 @@
 //    into one of two tensor-memory accumulators (2 x 256 columns):
 //    x_hi*w_hi + x_hi*w_lo + x_lo*w_hi, the 3xTF32 split that keeps fp32-level
 //    accuracy (TF32 alone was not accurate enough on some parts, per the
-//    pages' `tf32_projection_accurate`);
+//    pages' `tf32_projection_accurate`).  The single-product TF32 mode (the
+//    pages' `CudaMath::Tf32`) issues x_hi*w_hi alone: the lo plane of W is
+//    neither loaded nor used and the converters only round X to TF32;
 //  * warps 4-7 (epilogue) read a finished accumulator with tcgen05.ld, write
 //    32-column slices of their 32 rows into a double-buffered shared-memory
 //    staging area (128-byte swizzle, conflict-free) and hand each 4 KiB
@@ -44,11 +46,23 @@ namespace {
 constexpr int BM = 128;  // rows of G per tile (MMA M)
 constexpr int BN = 256;  // gate columns per tile (MMA N)
 constexpr int BK = 16;   // fp32 per K block = 64 bytes
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 4;                     // 8 KiB
 constexpr int B_BYTES = BN * BK * 4;                     // 16 KiB
-constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // A hi, A lo, B hi, B lo
-constexpr uint32_t TX_BYTES = A_BYTES + 2 * B_BYTES;     // what TMA writes per stage
+constexpr int RING_BYTES = 4 * (2 * A_BYTES + 2 * B_BYTES);  // 192 KiB of stages
+
+// The stage ring of each mode: 3xTF32 keeps A hi, A lo, B hi, B lo per stage
+// (48 KiB, 4 stages); the single-product mode only A hi and B hi (24 KiB), so
+// the same ring holds 8 stages and twice the K blocks in flight.
+template <bool SINGLE>
+struct Ring {
+    static constexpr int STAGE_BYTES = SINGLE ? A_BYTES + B_BYTES : 2 * A_BYTES + 2 * B_BYTES;
+    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;
+    static constexpr int A_LO = A_BYTES;                         // 3xTF32 only
+    static constexpr int B_HI = SINGLE ? A_BYTES : 2 * A_BYTES;
+    static constexpr int B_LO = B_HI + B_BYTES;                  // 3xTF32 only
+    static constexpr uint32_t TX_BYTES = SINGLE ? A_BYTES + B_BYTES : A_BYTES + 2 * B_BYTES;
+};
+constexpr int MAX_STAGES = Ring<true>::STAGES;
 constexpr uint32_t ACC_COLS = BN;                        // fp32 columns per accumulator
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;             // two accumulators
 constexpr int CONVERTERS = 128;                          // warps 0-3
@@ -58,7 +72,7 @@ constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
 constexpr int OUT_COLS = 32;                             // G columns per store slice
 constexpr int OUT_BYTES = 32 * OUT_COLS * 4;             // one warp's 32 rows: 4 KiB
-constexpr int OUT_OFFSET = STAGES * STAGE_BYTES;         // staging: 4 warps x 2 slices
+constexpr int OUT_OFFSET = RING_BYTES;                   // staging: 4 warps x 2 slices
 constexpr size_t SMEM_BYTES = OUT_OFFSET + 4 * 2 * OUT_BYTES + 1024 + 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 constexpr int TILES_N = kGateColumns / BN;          // 4
@@ -106,6 +120,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, unsig
     }
 }
 
+template <bool SINGLE>
 __global__ void __launch_bounds__(THREADS, 1)
 projection_kernel(const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap whi_map,
@@ -113,13 +128,16 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap g_map, int rows,
                   int kblocks, int pairs, unsigned *fault)
 {
+    using RG = Ring<SINGLE>;
+    constexpr int STAGES = RG::STAGES;
+    constexpr int STAGE_BYTES = RG::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + OUT_OFFSET + 4 * 2 * OUT_BYTES);
-    uint64_t *conv = full + STAGES;
-    uint64_t *empty = conv + STAGES;
-    uint64_t *acc_full = empty + STAGES;      // [2]
+    uint64_t *conv = full + MAX_STAGES;
+    uint64_t *empty = conv + MAX_STAGES;
+    uint64_t *acc_full = empty + MAX_STAGES;  // [2]
     uint64_t *acc_empty = acc_full + 2;       // [2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -179,12 +197,13 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                                                          kFaultProducer, WAIT_LIMIT_NS))
                         break;
                     uint8_t *st = smem + s * STAGE_BYTES;
-                    ptx::mbar_arrive_expect_tx(&full[s], TX_BYTES);
+                    ptx::mbar_arrive_expect_tx(&full[s], RG::TX_BYTES);
                     ptx::tma_load_2d(st, &x_map, &full[s], kb * BK, m0);
-                    ptx::tma_load_2d_multicast(st + 2 * A_BYTES + rank * B_HALF_BYTES, &whi_map,
+                    ptx::tma_load_2d_multicast(st + RG::B_HI + rank * B_HALF_BYTES, &whi_map,
                                                &full[s], kb * BK, nh, PAIR_MASK);
-                    ptx::tma_load_2d_multicast(st + 2 * A_BYTES + B_BYTES + rank * B_HALF_BYTES,
-                                               &wlo_map, &full[s], kb * BK, nh, PAIR_MASK);
+                    if constexpr (!SINGLE)
+                        ptx::tma_load_2d_multicast(st + RG::B_LO + rank * B_HALF_BYTES, &wlo_map,
+                                                   &full[s], kb * BK, nh, PAIR_MASK);
                     issued = kbi + 1;
                 }
             }
@@ -212,16 +231,20 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     }
                     ptx::tc_fence_after();
                     const uint32_t a_hi = ptx::smem_u32(smem + s * STAGE_BYTES);
-                    const uint32_t a_lo = a_hi + A_BYTES;
-                    const uint32_t b_hi = a_hi + 2 * A_BYTES;
-                    const uint32_t b_lo = b_hi + B_BYTES;
+                    const uint32_t a_lo = a_hi + RG::A_LO;
+                    const uint32_t b_hi = a_hi + RG::B_HI;
+                    const uint32_t b_lo = a_hi + RG::B_LO;
 #pragma unroll
                     for (int j = 0; j < BK / 8; ++j) {
                         const uint32_t off = j * 32;  // 8 TF32 = 32 bytes along K
                         ptx::mma_tf32(d_tmem, sw64_desc(a_hi + off), sw64_desc(b_hi + off), IDESC,
                                       (kb | j) != 0);
-                        ptx::mma_tf32(d_tmem, sw64_desc(a_hi + off), sw64_desc(b_lo + off), IDESC, 1);
-                        ptx::mma_tf32(d_tmem, sw64_desc(a_lo + off), sw64_desc(b_hi + off), IDESC, 1);
+                        if constexpr (!SINGLE) {
+                            ptx::mma_tf32(d_tmem, sw64_desc(a_hi + off), sw64_desc(b_lo + off),
+                                          IDESC, 1);
+                            ptx::mma_tf32(d_tmem, sw64_desc(a_lo + off), sw64_desc(b_hi + off),
+                                          IDESC, 1);
+                        }
                     }
                     ptx::mma_commit_multicast(&empty[s], PAIR_MASK);
                     *progress = static_cast<int>(kbi + 1);
@@ -233,7 +256,8 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             }
         }
     } else if (warp < 4) {
-        // converters: split X into TF32 hi (in place) and lo
+        // converters: split X into TF32 hi (in place) and lo; the
+        // single-product mode only rounds X to TF32 in place
         const int tid = threadIdx.x;
         long kbi = 0;
         for (int t = first; t < pairs && !*abort_flag; t += stride) {
@@ -247,14 +271,24 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     break;
                 }
                 float4 *a = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES);
-                float4 *alo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + A_BYTES);
+                float4 *alo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + RG::A_LO);
+                if constexpr (SINGLE) {
 #pragma unroll
-                for (int i = 0; i < A_BYTES / 16 / CONVERTERS; ++i) {
-                    const int idx = tid + i * CONVERTERS;
-                    float4 hi, lo;
-                    split4(a[idx], hi, lo);
-                    a[idx] = hi;
-                    alo[idx] = lo;
+                    for (int i = 0; i < A_BYTES / 16 / CONVERTERS; ++i) {
+                        const int idx = tid + i * CONVERTERS;
+                        const float4 v = a[idx];
+                        a[idx] = make_float4(ptx::tf32_rna(v.x), ptx::tf32_rna(v.y),
+                                             ptx::tf32_rna(v.z), ptx::tf32_rna(v.w));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < A_BYTES / 16 / CONVERTERS; ++i) {
+                        const int idx = tid + i * CONVERTERS;
+                        float4 hi, lo;
+                        split4(a[idx], hi, lo);
+                        a[idx] = hi;
+                        alo[idx] = lo;
+                    }
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&conv[s]);
@@ -414,13 +448,16 @@ int projection_prepare(int device)
     if (st != LSTM_OK)
         return st;
     g_sm_count[device] = sms;
-    st = cuda_status(cudaFuncSetAttribute(projection_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(SMEM_BYTES)),
-                     "projection shared-memory attribute");
-    if (st != LSTM_OK)
-        return st;
-    // the persistent grid is no larger than what runs at once
+    for (const void *fn : {reinterpret_cast<const void *>(&projection_kernel<false>),
+                           reinterpret_cast<const void *>(&projection_kernel<true>)}) {
+        st = cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(SMEM_BYTES)),
+                         "projection shared-memory attribute");
+        if (st != LSTM_OK)
+            return st;
+    }
+    // the persistent grid is no larger than what runs at once (both modes
+    // have the same block and shared-memory size)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CLUSTER);
     cfg.blockDim = dim3(THREADS);
@@ -433,7 +470,7 @@ int projection_prepare(int device)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    st = cuda_status(cudaOccupancyMaxActiveClusters(&n, projection_kernel, &cfg),
+    st = cuda_status(cudaOccupancyMaxActiveClusters(&n, projection_kernel<false>, &cfg),
                      "projection max active clusters");
     if (st != LSTM_OK)
         return st;
@@ -442,9 +479,11 @@ int projection_prepare(int device)
 }
 
 int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                      const CUtensorMap &wlo_map, float *g, int rows, int kp, unsigned *fault,
-                      cudaStream_t stream)
+                      const CUtensorMap &wlo_map, float *g, int rows, int kp, int math,
+                      unsigned *fault, cudaStream_t stream)
 {
+    if (math != LSTM_MATH_3XTF32 && math != LSTM_MATH_TF32)
+        return fail(LSTM_E_INVALID, "projection: unknown math mode %d", math);
     if (rows <= 0 || kp <= 0 || kp % 32 != 0)
         return fail(LSTM_E_INVALID, "projection: rows %d, kp %d", rows, kp);
     const long mtiles = (static_cast<long>(rows) + BM - 1) / BM;
@@ -476,8 +515,11 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
         return st;
     const int kblocks = kp / BK;
     const int npairs = static_cast<int>(pairs);
-    return cuda_status(cudaLaunchKernelEx(&cfg, projection_kernel, x_map, whi_map, wlo_map, g_map,
-                                          rows, kblocks, npairs, fault),
+    return cuda_status(math == LSTM_MATH_TF32
+                           ? cudaLaunchKernelEx(&cfg, projection_kernel<true>, x_map, whi_map,
+                                                wlo_map, g_map, rows, kblocks, npairs, fault)
+                           : cudaLaunchKernelEx(&cfg, projection_kernel<false>, x_map, whi_map,
+                                                wlo_map, g_map, rows, kblocks, npairs, fault),
                        "projection launch");
 }
 

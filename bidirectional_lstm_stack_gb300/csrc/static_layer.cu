@@ -111,7 +111,8 @@ extern "C" int lstm_layer_forward_static(const float *x, int batch, int steps, i
         (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionWBoxRows)))
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((st = launch_projection(xm, hm, lm, gates, static_cast<int>(rows), kp, fault, s)))
+    if ((st = launch_projection(xm, hm, lm, gates, static_cast<int>(rows), kp, LSTM_MATH_3XTF32,
+                                fault, s)))
         return st;
     if ((st = launch_recurrence(gates, rp, bias, y, batch, steps, 0, fault, s)))
         return st;

@@ -33,9 +33,10 @@
  *  - The return value is LSTM_OK (0) or one of the LSTM_E_* codes;
  *    lstm_stack_last_error() then returns a message for the calling thread.
  *    No C++ exception crosses this boundary.
- *  - Finite inputs give finite, bounded outputs.  How NaN or infinite inputs
- *    surface is unspecified (the activations clamp their argument), as on the
- *    pages (`SPECIAL_VALUES`).
+ *  - Finite inputs give finite, bounded outputs (the activations' exponential
+ *    saturates to 0 or infinity, so every gate stays in [0, 1]).  How NaN or
+ *    infinite inputs surface is unspecified, as on the pages
+ *    (`SPECIAL_VALUES`).
  */
 #ifndef LSTM_STACK_H
 #define LSTM_STACK_H
@@ -62,6 +63,19 @@ enum {
     LSTM_E_CUDA = 5,     /* a CUDA runtime/driver call failed (message: its error string) */
     LSTM_E_ALLOC = 6,    /* host or device allocation failed */
     LSTM_E_FAULT = 7     /* a kernel's bounded wait ran out and it set its fault word */
+};
+
+/* How the input projection multiplies (lstmproj.rs `CudaMath` and
+ * `projection_rule`).  LSTM_MATH_3XTF32 (default): three TF32 tensor-core
+ * products per fp32 product (x_hi*w_hi + x_hi*w_lo + x_lo*w_hi), fp32-level
+ * accuracy.  LSTM_MATH_TF32: one product of the operands rounded to TF32
+ * (10 stored mantissa bits, to nearest, ties away), fp32 accumulation; a
+ * third of the tensor work, with the TF32 rounding error the pages found too
+ * large on some parts (`tf32_projection_accurate`).  The recurrence is fp32
+ * in both. */
+enum {
+    LSTM_MATH_3XTF32 = 0,
+    LSTM_MATH_TF32 = 1
 };
 
 /* ---------------------------------------------------------------------------
@@ -135,6 +149,11 @@ int lstm_stack_phase_times(lstm_stack *s, float *ms);
  * (direct launches every call); results are identical either way. */
 int lstm_stack_set_graphs(lstm_stack *s, int enable);
 
+/* Selects the projection's products for the following forward passes:
+ * LSTM_MATH_3XTF32 (default) or LSTM_MATH_TF32.  Errors: LSTM_E_INVALID
+ * (null stack, unknown mode). */
+int lstm_stack_set_math(lstm_stack *s, int math);
+
 /* Releases everything the stack owns (waits for its pending work first).
  * NULL is ignored. */
 void lstm_stack_destroy(lstm_stack *s);
@@ -178,6 +197,15 @@ int lstm_pack_layer(const float *w, const float *r, const float *b,
 int lstm_projection(const float *x, int rows, int in_width,
                     const float *wp_hi, const float *wp_lo, int kp, float *g,
                     void *stream);
+
+/* lstm_projection with a chosen product (see LSTM_MATH_*): with
+ * LSTM_MATH_TF32 it computes g[m][n] = sum_j tf32(x[m][j]) * wp_hi[n][j]
+ * (wp_hi is already W rounded to TF32) with fp32 accumulation, and wp_lo is
+ * not read (it may be NULL).  Errors: those of lstm_projection, and
+ * LSTM_E_INVALID for an unknown mode. */
+int lstm_projection_math(const float *x, int rows, int in_width,
+                         const float *wp_hi, const float *wp_lo, int kp, float *g,
+                         int math, void *stream);
 
 /* Step 3, device: one direction's recurrence over one layer.
  *   g    : device [batch*steps][1024] projection from lstm_projection
