@@ -427,7 +427,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synthetic.WORKLOADS))
-    ap.add_argument("--reference-windows", type=int, default=2,
+    ap.add_argument("--reference-windows", type=int, default=16,
                     help="windows per step of the --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
