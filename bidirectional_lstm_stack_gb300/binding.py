@@ -31,6 +31,8 @@ LSTM_E_ALLOC = 6
 LSTM_E_FAULT = 7
 LSTM_MATH_3XTF32 = 0
 LSTM_MATH_TF32 = 1
+LSTM_GATES_IFGO = 0
+LSTM_GATES_IOFC = 1
 
 _c_float_p = ctypes.POINTER(ctypes.c_float)
 _vp = ctypes.c_void_p
@@ -66,6 +68,8 @@ def load():
         i, sz = ctypes.c_int, ctypes.c_size_t
         sig = {
             "lstm_stack_create": (i, [ctypes.POINTER(_Weights), i, i, i, ctypes.POINTER(_vp)]),
+            "lstm_stack_create_ordered": (i, [ctypes.POINTER(_Weights), i, i, i, i,
+                                              ctypes.POINTER(_vp)]),
             "lstm_stack_forward": (i, [_vp, _vp, sz, _vp, sz, i, i, _vp]),
             "lstm_stack_forward_host": (i, [_vp, _vp, sz, _vp, sz, i, i, _vp]),
             "lstm_stack_enable_phase_timing": (i, [_vp, i]),
@@ -75,6 +79,7 @@ def load():
             "lstm_stack_destroy": (None, [_vp]),
             "lstm_stack_last_error": (ctypes.c_char_p, []),
             "lstm_pack_layer": (i, [_vp, _vp, _vp, i, i, _vp, _vp, _vp, _vp]),
+            "lstm_pack_layer_ordered": (i, [_vp, _vp, _vp, i, i, i, _vp, _vp, _vp, _vp]),
             "lstm_projection": (i, [_vp, i, i, _vp, _vp, i, _vp, _vp]),
             "lstm_projection_math": (i, [_vp, i, i, _vp, _vp, i, _vp, i, _vp]),
             "lstm_recurrence": (i, [_vp, _vp, _vp, _vp, i, i, i, _vp]),
@@ -118,16 +123,16 @@ def _host(a, dtype=np.float32) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=dtype))
 
 
-def lstm_pack_layer(w, r, b, in_width: int, kp: int):
+def lstm_pack_layer(w, r, b, in_width: int, kp: int, gate_order: int = LSTM_GATES_IFGO):
     """Host packer; returns (wp_hi, wp_lo, rp, bias) numpy arrays."""
     w, r, b = _host(w), _host(r), _host(b)
     wp_hi = np.empty((GATE_COLUMNS, kp), np.float32)
     wp_lo = np.empty((GATE_COLUMNS, kp), np.float32)
     rp = np.empty((2, 4 * HIDDEN, HIDDEN), np.float32)
     bias = np.empty((2, 4 * HIDDEN), np.float32)
-    _check(load().lstm_pack_layer(w.ctypes.data, r.ctypes.data, b.ctypes.data, in_width, kp,
-                                  wp_hi.ctypes.data, wp_lo.ctypes.data, rp.ctypes.data,
-                                  bias.ctypes.data))
+    _check(load().lstm_pack_layer_ordered(w.ctypes.data, r.ctypes.data, b.ctypes.data, in_width,
+                                          kp, gate_order, wp_hi.ctypes.data, wp_lo.ctypes.data,
+                                          rp.ctypes.data, bias.ctypes.data))
     return wp_hi, wp_lo, rp, bias
 
 
@@ -182,8 +187,10 @@ def lstm_fault_status() -> int:
     return int(v.value)
 
 
-def lstm_stack_create(layers, max_batch: int, max_steps: int, device: int = 0):
-    """Creates a stack from source weights (list of dicts w, r, b; numpy).
+def lstm_stack_create(layers, max_batch: int, max_steps: int, device: int = 0,
+                      gate_order: int = LSTM_GATES_IFGO):
+    """Creates a stack from source weights (list of dicts w, r, b; numpy) whose
+    gate row blocks are in ``gate_order`` (LSTM_GATES_IFGO or _IOFC).
 
     Returns the opaque handle (an int).  The host arrays are only read during
     the call.
@@ -195,8 +202,8 @@ def lstm_stack_create(layers, max_batch: int, max_steps: int, device: int = 0):
         ws.r[l] = a["r"].ctypes.data
         ws.b[l] = a["b"].ctypes.data
     h = _vp()
-    _check(load().lstm_stack_create(ctypes.byref(ws), max_batch, max_steps, device,
-                                    ctypes.byref(h)))
+    _check(load().lstm_stack_create_ordered(ctypes.byref(ws), gate_order, max_batch, max_steps,
+                                            device, ctypes.byref(h)))
     return h.value
 
 
@@ -240,11 +247,12 @@ def lstm_stack_destroy(handle) -> None:
 class LSTMStack:
     """Owns a stack handle; ``forward`` takes and returns torch CUDA tensors."""
 
-    def __init__(self, layers, max_batch: int, max_steps: int, device: int = 0):
+    def __init__(self, layers, max_batch: int, max_steps: int, device: int = 0,
+                 gate_order: int = LSTM_GATES_IFGO):
         self.device = device
         self.max_batch = max_batch
         self.max_steps = max_steps
-        self.handle = lstm_stack_create(layers, max_batch, max_steps, device)
+        self.handle = lstm_stack_create(layers, max_batch, max_steps, device, gate_order)
 
     def forward(self, x, y=None, stream=None):
         """x: [B, T, 60] float32 CUDA tensor -> y [B, T, 256] (new unless given)."""

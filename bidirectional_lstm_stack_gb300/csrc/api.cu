@@ -218,11 +218,30 @@ extern "C" const char *lstm_stack_last_error(void)
     return g_last_error.c_str();
 }
 
+namespace {
+// Source row block of gate k (k = 0..3 for i, f, g, o) in each gate order.
+const int kGateBlocks[2][4] = {
+    {0, 1, 2, 3},  // LSTM_GATES_IFGO: blocks i, f, g, o
+    {0, 2, 3, 1},  // LSTM_GATES_IOFC: blocks i, o, f, c (ONNX)
+};
+}  // namespace
+
 extern "C" int lstm_pack_layer(const float *w, const float *r, const float *b, int in_width,
                                int kp, float *wp_hi, float *wp_lo, float *rp, float *bias)
 {
+    return lstm_pack_layer_ordered(w, r, b, in_width, kp, LSTM_GATES_IFGO, wp_hi, wp_lo, rp,
+                                   bias);
+}
+
+extern "C" int lstm_pack_layer_ordered(const float *w, const float *r, const float *b,
+                                       int in_width, int kp, int gate_order, float *wp_hi,
+                                       float *wp_lo, float *rp, float *bias)
+{
     if (!w || !r || !b || !wp_hi || !wp_lo || !rp || !bias)
         return fail(LSTM_E_INVALID, "lstm_pack_layer: null pointer");
+    if (gate_order != LSTM_GATES_IFGO && gate_order != LSTM_GATES_IOFC)
+        return fail(LSTM_E_INVALID, "lstm_pack_layer: unknown gate order %d", gate_order);
+    const int *block = kGateBlocks[gate_order];
     if (in_width <= 0 || kp < in_width || kp % 32 != 0)
         return fail(LSTM_E_INVALID, "lstm_pack_layer: in_width %d, kp %d (need 0 < in_width <= kp, kp %% 32 == 0)",
                     in_width, kp);
@@ -230,7 +249,7 @@ extern "C" int lstm_pack_layer(const float *w, const float *r, const float *b, i
     for (int d = 0; d < 2; ++d) {
         for (int u = 0; u < H; ++u) {
             for (int k = 0; k < 4; ++k) {
-                const long src_row = static_cast<long>(d) * 4 * H + k * H + u;  // gate block k
+                const long src_row = static_cast<long>(d) * 4 * H + block[k] * H + u;
                 const long dst_row = static_cast<long>(d) * 4 * H + 4 * u + k;  // interleaved
                 for (int j = 0; j < kp; ++j) {
                     const float v = j < in_width ? w[src_row * in_width + j] : 0.0f;
@@ -241,7 +260,8 @@ extern "C" int lstm_pack_layer(const float *w, const float *r, const float *b, i
                 for (int j = 0; j < H; ++j)
                     rp[dst_row * H + j] = r[src_row * H + j];
                 const float *bd = b + static_cast<long>(d) * 8 * H;
-                bias[static_cast<long>(d) * 4 * H + 4 * u + k] = bd[k * H + u] + bd[4 * H + k * H + u];
+                bias[static_cast<long>(d) * 4 * H + 4 * u + k] =
+                    bd[block[k] * H + u] + bd[4 * H + block[k] * H + u];
             }
         }
     }
@@ -282,9 +302,18 @@ extern "C" void lstm_stack_destroy(lstm_stack *s)
 extern "C" int lstm_stack_create(const lstm_stack_weights *weights, int max_batch, int max_steps,
                                  int device, lstm_stack **out)
 {
+    return lstm_stack_create_ordered(weights, LSTM_GATES_IFGO, max_batch, max_steps, device, out);
+}
+
+extern "C" int lstm_stack_create_ordered(const lstm_stack_weights *weights, int gate_order,
+                                         int max_batch, int max_steps, int device,
+                                         lstm_stack **out)
+{
     if (!out)
         return fail(LSTM_E_INVALID, "lstm_stack_create: null output pointer");
     *out = nullptr;
+    if (gate_order != LSTM_GATES_IFGO && gate_order != LSTM_GATES_IOFC)
+        return fail(LSTM_E_INVALID, "lstm_stack_create: unknown gate order %d", gate_order);
     if (!weights)
         return fail(LSTM_E_INVALID, "lstm_stack_create: null weights");
     for (int l = 0; l < kLayers; ++l)
@@ -336,9 +365,9 @@ extern "C" int lstm_stack_create(const lstm_stack_weights *weights, int max_batc
         return fail(LSTM_E_ALLOC, "lstm_stack_create: host staging allocation failed");
     }
     for (int l = 0; l < kLayers; ++l) {
-        st = lstm_pack_layer(weights->w[l], weights->r[l], weights->b[l], s->in_width[l], s->kp[l],
-                             host + offs[l][0], host + offs[l][1], host + offs[l][2],
-                             host + offs[l][3]);
+        st = lstm_pack_layer_ordered(weights->w[l], weights->r[l], weights->b[l], s->in_width[l],
+                                     s->kp[l], gate_order, host + offs[l][0], host + offs[l][1],
+                                     host + offs[l][2], host + offs[l][3]);
         if (st != LSTM_OK) {
             free(host);
             lstm_stack_destroy(s);

@@ -108,6 +108,23 @@ typedef struct {
 int lstm_stack_create(const lstm_stack_weights *weights, int max_batch,
                       int max_steps, int device, lstm_stack **out);
 
+/* Gate order of the source row blocks of W, R, Wb and Rb.  The pages' source
+ * layout (`Oxide::with_recurrence`: W [2][512][in], R [2][512][128],
+ * B = per direction Wb ++ Rb) is ONNX-shaped; ONNX orders the blocks
+ * i, o, f, c (c = the cell candidate g), PyTorch and this library's default
+ * i, f, g, o. */
+enum {
+    LSTM_GATES_IFGO = 0,
+    LSTM_GATES_IOFC = 1
+};
+
+/* lstm_stack_create for weights whose row blocks are in `gate_order`
+ * (LSTM_GATES_IFGO or LSTM_GATES_IOFC); everything else as there.  Errors:
+ * those of lstm_stack_create, and LSTM_E_INVALID for an unknown order. */
+int lstm_stack_create_ordered(const lstm_stack_weights *weights, int gate_order,
+                              int max_batch, int max_steps, int device,
+                              lstm_stack **out);
+
 /* y = stack(x) for `batch` independent windows of `steps` steps.
  *   x : device [batch][steps][60],  x_len = batch*steps*60 floats
  *   y : device [batch][steps][256], y_len = batch*steps*256 floats;
@@ -180,6 +197,15 @@ const char *lstm_stack_last_error(void);
 int lstm_pack_layer(const float *w, const float *r, const float *b,
                     int in_width, int kp, float *wp_hi, float *wp_lo,
                     float *rp, float *bias);
+
+/* lstm_pack_layer for source blocks in `gate_order` (LSTM_GATES_*): packed
+ * row d*512 + 4u + k (k = 0..3 for i, f, g, o) takes the source row of gate k
+ * of unit u in that order (for LSTM_GATES_IOFC: i from block 0, f from 2,
+ * g from 3, o from 1), and likewise for R and the bias.  Errors:
+ * LSTM_E_INVALID (as lstm_pack_layer, or an unknown order). */
+int lstm_pack_layer_ordered(const float *w, const float *r, const float *b,
+                            int in_width, int kp, int gate_order, float *wp_hi,
+                            float *wp_lo, float *rp, float *bias);
 
 /* Step 2, device: the input projection of one layer for both directions,
  *   g[m][n] = sum_j x[m][j] * wp[n][j],  m < rows, n < 1024,

@@ -121,3 +121,25 @@ def test_packer_rejects_bad_kp(lib):
     with pytest.raises(binding.LSTMError) as e:
         binding.lstm_pack_layer(w, np.zeros((2, 4 * H, H)), np.zeros((2, 8 * H)), 60, 60)
     assert e.value.code == binding.LSTM_E_INVALID
+
+
+def _to_iofc(a, H, axis):
+    """Reorders i, f, g, o row blocks (length H each) into ONNX's i, o, f, c."""
+    i, f, g, o = np.split(a, 4, axis=axis)
+    return np.concatenate([i, o, f, g], axis=axis)
+
+
+def test_packer_onnx_gate_order_matches_default(lib):
+    rng = np.random.default_rng(5)
+    w = rng.uniform(-1, 1, (2, 4 * H, 60)).astype(np.float32)
+    r = rng.uniform(-1, 1, (2, 4 * H, H)).astype(np.float32)
+    b = rng.uniform(-1, 1, (2, 8 * H)).astype(np.float32)
+    b_onnx = np.concatenate([_to_iofc(b[:, :4 * H], H, 1), _to_iofc(b[:, 4 * H:], H, 1)], axis=1)
+    ref = binding.lstm_pack_layer(w, r, b, 60, 64)
+    got = binding.lstm_pack_layer(_to_iofc(w, H, 1), _to_iofc(r, H, 1), b_onnx, 60, 64,
+                                  binding.LSTM_GATES_IOFC)
+    for a, c in zip(ref, got):
+        np.testing.assert_array_equal(a, c)
+    with pytest.raises(binding.LSTMError) as e:
+        binding.lstm_pack_layer(w, r, b, 60, 64, 2)
+    assert e.value.code == binding.LSTM_E_INVALID

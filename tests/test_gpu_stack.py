@@ -142,3 +142,28 @@ def test_forward_inside_a_caller_graph_capture(stack, layers):
     g.replay()
     torch.cuda.synchronize()
     assert_within(y.cpu().numpy(), oracle.lstm_stack(x_np, layers), what="captured forward")
+
+
+def _to_iofc(a, axis):
+    """Reorders i, f, g, o row blocks into ONNX's i, o, f, c."""
+    i, f, g, o = np.split(a, 4, axis=axis)
+    return np.concatenate([i, o, f, g], axis=axis)
+
+
+def test_onnx_gate_order_stack(stack, layers):
+    # the same stack from ONNX-ordered weights gives the same bits
+    onnx = [{"w": _to_iofc(l["w"], 1), "r": _to_iofc(l["r"], 1),
+             "b": np.concatenate([_to_iofc(l["b"][:, :512], 1), _to_iofc(l["b"][:, 512:], 1)],
+                                 axis=1)} for l in layers]
+    x = synthetic.stack_input(synthetic.WORKLOADS["b8_t589_x3"])
+    s2 = binding.LSTMStack(onnx, 8, 589, gate_order=binding.LSTM_GATES_IOFC)
+    try:
+        import torch
+        y2 = s2(cuda(x))
+        torch.cuda.synchronize()
+        y2 = y2.cpu().numpy()
+    finally:
+        s2.close()
+    y1 = _forward(stack, x)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    assert_within(y2, oracle.lstm_stack(x, layers), what="onnx gate order")
