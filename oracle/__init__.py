@@ -72,6 +72,9 @@ def _load():
                 f.argtypes = [
                     ctypes.c_long, ctypes.c_int, ctypes.c_int, _dptr, _dptr, _dptr]
             lib.oracle_tf32_array.argtypes = [ctypes.c_long, _dptr, _dptr]
+            lib.oracle_heads.argtypes = [
+                ctypes.c_long, _dptr, _dptr, _dptr, _dptr, _dptr, _dptr, _dptr,
+                ctypes.c_double, _dptr]
             lib.oracle_recurrence.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, _dptr, _dptr, _dptr,
                 _dptr]
@@ -180,3 +183,22 @@ def recurrence(G, R, bias, batch: int, steps: int) -> np.ndarray:
     y = np.zeros((batch, steps, 2 * H), dtype=np.float64)
     _load().oracle_recurrence(batch, steps, H, _p(G), _p(R), _p(bias), _p(y))
     return y
+
+
+def heads(y, W0, b0, W1, b1, W2, b2, slope: float = 0.01) -> np.ndarray:
+    """The segmentation model's dense heads on stack output rows.
+
+    y ``[M, 256]``; W0 ``[256, 128]``, W1 ``[128, 128]``, W2 ``[128, 7]``
+    (row-major ``[k, n]``, as the pages store them), biases ``[n]``.  Returns
+    the log-probabilities ``[M, 7]`` of
+    ``log_softmax(leaky(leaky(y W0 + b0) W1 + b1) W2 + b2)``.
+    """
+    y, W0, b0, W1, b1, W2, b2 = map(_f64, (y, W0, b0, W1, b1, W2, b2))
+    M = y.shape[0]
+    assert y.shape == (M, 256) and W0.shape == (256, 128) and b0.shape == (128,)
+    assert W1.shape == (128, 128) and b1.shape == (128,)
+    assert W2.shape == (128, 7) and b2.shape == (7,)
+    out = np.zeros((M, 7), dtype=np.float64)
+    _load().oracle_heads(M, _p(y), _p(W0), _p(b0), _p(W1), _p(b1), _p(W2), _p(b2),
+                         float(slope), _p(out))
+    return out

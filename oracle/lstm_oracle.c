@@ -282,3 +282,57 @@ void oracle_recurrence(int B, int T, int H, const double *G,
         }
     }
 }
+
+/*
+ * The segmentation model's dense heads on the stack output (segdense.rs,
+ * `Site`: `Linear0` a row-major 256-to-128 projection `[k, n]` with bias and
+ * LeakyReLU, `Linear1` 128-to-128 with bias and LeakyReLU, `Linear2` 128-to-7
+ * with bias and log-softmax; `DenseOxide`: the epilogues fused), for every
+ * row m < M of y [M][256]:
+ *   h1 = leaky(y[m] . W0 + b0),  h2 = leaky(h1 . W1 + b1),
+ *   z  = h2 . W2 + b2,           out[m] = z - log(sum_j exp(z_j)),
+ * with leaky(v) = v for v >= 0 and slope * v below (the pages name LeakyReLU
+ * without a slope; the reading taken is a caller-given slope, PyTorch's 0.01
+ * by default).  The log-sum-exp is taken as max_j z_j + log(sum_j exp(z_j -
+ * max)), the same value written so it cannot overflow.
+ *   W0 : [256][128] (row k holds input k's weights to the 128 outputs),
+ *   W1 : [128][128], W2 : [128][7],  out : [M][7]
+ */
+static double leaky(double v, double slope) { return v >= 0.0 ? v : slope * v; }
+
+void oracle_heads(long M, const double *y, const double *W0, const double *b0,
+                  const double *W1, const double *b1, const double *W2,
+                  const double *b2, double slope, double *out)
+{
+    #pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m) {
+        double h1[128], h2[128], z[7];
+        for (int n = 0; n < 128; ++n) {
+            double acc = b0[n];
+            for (int k = 0; k < 256; ++k)
+                acc += y[m * 256 + k] * W0[k * 128 + n];
+            h1[n] = leaky(acc, slope);
+        }
+        for (int n = 0; n < 128; ++n) {
+            double acc = b1[n];
+            for (int k = 0; k < 128; ++k)
+                acc += h1[k] * W1[k * 128 + n];
+            h2[n] = leaky(acc, slope);
+        }
+        double zmax = -INFINITY;
+        for (int n = 0; n < 7; ++n) {
+            double acc = b2[n];
+            for (int k = 0; k < 128; ++k)
+                acc += h2[k] * W2[k * 7 + n];
+            z[n] = acc;
+            if (acc > zmax)
+                zmax = acc;
+        }
+        double s = 0.0;
+        for (int n = 0; n < 7; ++n)
+            s += exp(z[n] - zmax);
+        const double lse = zmax + log(s);
+        for (int n = 0; n < 7; ++n)
+            out[m * 7 + n] = z[n] - lse;
+    }
+}

@@ -338,3 +338,60 @@ def test_tf32_stack_is_float64_stack_on_rounded_operands():
     y = oracle.lstm_stack(x, lays, projection="tf32")
     np.testing.assert_array_equal(y, cur)
     assert np.abs(y - oracle.lstm_stack(x, lays)).max() > 1e-6
+
+
+# ---- dense heads (linear0, linear1, classifier) ----------------------------
+
+def test_heads_zero_weights_closed_form():
+    # all weights zero: z = b2, so out = b2 - log(sum(exp(b2))); with b2 = 0
+    # every class gets exactly -log 7
+    M = 3
+    y = np.random.default_rng(40).standard_normal((M, 256))
+    z = np.zeros
+    out = oracle.heads(y, z((256, 128)), z(128), z((128, 128)), z(128), z((128, 7)), z(7))
+    np.testing.assert_array_equal(out, np.full((M, 7), -np.log(7.0)))
+    b2 = np.array([0.5, -1.0, 2.0, 0.0, 3.0, -2.5, 1.0])
+    out = oracle.heads(y, z((256, 128)), z(128), z((128, 128)), z(128), z((128, 7)), b2)
+    np.testing.assert_allclose(out, np.tile(b2 - np.log(np.exp(b2).sum()), (M, 1)),
+                               rtol=0, atol=1e-15)
+
+
+def test_heads_leaky_slope_and_orientation():
+    # W0 routes input k to output perm[k] ([k, n] storage), W1 is the identity,
+    # W2 picks outputs 0..6: with negative inputs both LeakyReLUs scale by the
+    # slope, so z = slope^2 * y[perm^-1[0..6]]
+    rng = np.random.default_rng(41)
+    slope = 0.2
+    perm = rng.permutation(128)
+    W0 = np.zeros((256, 128))
+    W0[np.arange(128), perm] = 1.0
+    W1 = np.eye(128)
+    W2 = np.zeros((128, 7))
+    W2[np.arange(7), np.arange(7)] = 1.0
+    y = -rng.uniform(0.5, 2.0, (4, 256))
+    out = oracle.heads(y, W0, np.zeros(128), W1, np.zeros(128), W2, np.zeros(7), slope)
+    inv = np.argsort(perm)
+    zz = slope * slope * y[:, inv[:7]]
+    ref = zz - np.log(np.exp(zz).sum(axis=1, keepdims=True))
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-14)
+
+
+def test_heads_match_torch_and_normalise():
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    rng = np.random.default_rng(42)
+    M = 9
+    y = rng.standard_normal((M, 256))
+    W0, b0 = rng.uniform(-0.06, 0.06, (256, 128)), rng.uniform(-0.06, 0.06, 128)
+    W1, b1 = rng.uniform(-0.09, 0.09, (128, 128)), rng.uniform(-0.09, 0.09, 128)
+    W2, b2 = rng.uniform(-0.09, 0.09, (128, 7)), rng.uniform(-0.09, 0.09, 7)
+    out = oracle.heads(y, W0, b0, W1, b1, W2, b2)
+    t = lambda a: torch.from_numpy(a)
+    h = F.leaky_relu(t(y) @ t(W0) + t(b0), 0.01)
+    h = F.leaky_relu(h @ t(W1) + t(b1), 0.01)
+    ref = F.log_softmax(h @ t(W2) + t(b2), dim=1).numpy()
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(np.exp(out).sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    # log-softmax is unchanged by a constant added to every logit
+    np.testing.assert_allclose(oracle.heads(y, W0, b0, W1, b1, W2, b2 + 3.0), out,
+                               rtol=0, atol=1e-13)
