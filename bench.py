@@ -90,6 +90,31 @@ def flops_projection(rows: int) -> float:
     return sum(2.0 * rows * 1024 * (60 if l == 0 else 256) for l in range(LAYERS))
 
 
+def flops_heads(rows: int) -> float:
+    """Algorithmic flops of the dense heads: 2 * rows * (256*128 + 128*128 + 128*7)."""
+    return 2.0 * rows * (256 * 128 + 128 * 128 + 128 * 7)
+
+
+def time_heads(heads, y, steps, warmup, flush, stream):
+    """Per-call device time (ms) of the dense heads on the stack output y,
+    L2 flushed between calls."""
+    import torch
+    out = torch.empty((*y.shape[:-1], 7), device=y.device)
+    for _ in range(warmup):
+        heads.forward(y, out, stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(i)
+            starts[i].record(stream)
+            heads.forward(y, out, stream)
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
 def flops_recurrence_launch(batch: int, steps: int) -> float:
     """Algorithmic flops of one recurrence launch (one direction, one layer):
     the 512 x 128 matrix-vector product per window and step."""
@@ -319,6 +344,12 @@ def run_ours(args):
     binding.lstm_stack_set_math(stack.handle, binding.LSTM_MATH_3XTF32)
     tf32_s = max_over_ranks(sum(ms_t) / 1e3, device=torch.device("cuda", dev))
 
+    # the segmentation model's dense heads on this forward's output (3 launches)
+    heads = binding.LSTMHeads(synthetic.heads_weights(), wl.batch * wl.steps, device=dev)
+    ms_h = time_heads(heads, y, args.steps, args.warmup, flush, stream)
+    heads.close()
+    heads_ms = float(np.mean(ms_h))
+
     # end to end through the host-buffer entry point (pinned host memory)
     xp = torch.from_numpy(x_host).pin_memory()
     yp = torch.empty((wl.batch, wl.steps, 2 * H), dtype=torch.float32).pin_memory()
@@ -405,6 +436,11 @@ def run_ours(args):
         "tf32_mode": {"windows_per_s": wl.batch * world * args.steps / tf32_s,
                       "ms_per_step": tf32_s * 1e3 / args.steps,
                       "projection_ms": [round(float(v), 4) for v in ph_t[:, 0]]},
+        "heads": {"kernels": "linear0+LeakyReLU, linear1+LeakyReLU, classifier+log-softmax",
+                  "rows": wl.batch * wl.steps, "ms": heads_ms,
+                  "achieved_tflops": flops_heads(wl.batch * wl.steps) / (heads_ms * 1e-3) / 1e12,
+                  "frac_of_3xtf32_peak": flops_heads(wl.batch * wl.steps) / (heads_ms * 1e-3)
+                  / 1e12 / proj_peak},
         "e2e": {"value": e2e_value, "unit": "windows/s",
                 "h2d_bytes_per_step": int(xn.nbytes), "d2h_bytes_per_step": int(yn.nbytes)},
         "gpu_launches": 12 * args.steps,

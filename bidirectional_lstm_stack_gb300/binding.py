@@ -87,6 +87,10 @@ def load():
             "lstm_recurrence_max_clusters": (i, [i, i, i, i, i, ctypes.POINTER(i)]),
             "lstm_fault_status": (i, [ctypes.POINTER(ctypes.c_uint)]),
             "lstm_layer_forward_static": (i, [_vp, i, i, i, _vp, _vp, i, _vp, _vp, _vp, _vp]),
+            "lstm_heads_create": (i, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, i, i,
+                                      ctypes.POINTER(_vp)]),
+            "lstm_heads_forward": (i, [_vp, _vp, sz, _vp, sz, i, _vp]),
+            "lstm_heads_destroy": (None, [_vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -270,6 +274,50 @@ class LSTMStack:
     def close(self):
         if self.handle:
             lstm_stack_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+HEADS_CLASSES = 7
+
+
+class LSTMHeads:
+    """The segmentation model's dense heads (linear0, linear1, classifier) on
+    stack output rows; ``forward`` takes and returns torch CUDA tensors."""
+
+    def __init__(self, weights, max_rows: int, negative_slope: float = 0.01, device: int = 0):
+        arrs = {k: _host(weights[k]) for k in ("w0", "b0", "w1", "b1", "w2", "b2")}
+        h = _vp()
+        _check(load().lstm_heads_create(*(arrs[k].ctypes.data for k in
+                                          ("w0", "b0", "w1", "b1", "w2", "b2")),
+                                        float(negative_slope), max_rows, device, ctypes.byref(h)))
+        self.handle = h.value
+        self.max_rows = max_rows
+        self.device = device
+
+    def forward(self, y, out=None, stream=None):
+        """y: [..., 256] float32 CUDA tensor -> log-probabilities [..., 7]."""
+        import torch
+        if y.shape[-1] != OUTPUT:
+            raise ValueError(f"input width {y.shape[-1]}, expected {OUTPUT}")
+        rows = y.numel() // OUTPUT
+        if out is None:
+            out = torch.empty((*y.shape[:-1], HEADS_CLASSES), dtype=torch.float32,
+                              device=y.device)
+        _check(load().lstm_heads_forward(self.handle, _ptr(y), y.numel(), _ptr(out), out.numel(),
+                                         rows, _stream(stream, y.device)))
+        return out
+
+    __call__ = forward
+
+    def close(self):
+        if self.handle:
+            load().lstm_heads_destroy(self.handle)
             self.handle = None
 
     def __del__(self):  # pragma: no cover

@@ -63,8 +63,6 @@ unsigned *fault_word()
     return addr[dev];
 }
 
-namespace {
-
 // Round-to-nearest (ties away from zero) to TF32: keep 10 mantissa bits.
 float tf32_round(float x)
 {
@@ -78,23 +76,7 @@ float tf32_round(float x)
     return r;
 }
 
-// Makes `device` current for the scope and restores the previous one.
-struct DeviceGuard {
-    int prev = -1;
-    bool ok = false;
-    explicit DeviceGuard(int device)
-    {
-        if (cudaGetDevice(&prev) != cudaSuccess)
-            prev = -1;
-        ok = (prev == device) || cudaSetDevice(device) == cudaSuccess;
-    }
-    ~DeviceGuard()
-    {
-        if (prev >= 0)
-            cudaSetDevice(prev);
-    }
-};
-
+namespace {
 int check_device(int device)
 {
     cudaDeviceProp prop;
@@ -113,6 +95,7 @@ int check_device(int device)
         return fail(LSTM_E_DEVICE, "device %d does not support cluster launch", device);
     return LSTM_OK;
 }
+}  // namespace
 
 int prepare_device(int device)
 {
@@ -160,7 +143,6 @@ int pointer_device(const void *p, int *device)
 constexpr int kLayers = LSTM_STACK_LAYERS;
 constexpr int kPhaseEvents = 3 * 2 * kLayers;  // (projection, fwd, rev) x (start, end) x layers
 
-}  // namespace
 }  // namespace lstm
 
 using namespace lstm;

@@ -38,6 +38,34 @@ enum : unsigned {
 // resolved per device on first use).
 unsigned *fault_word();
 
+// ---- host helpers (api.cu) -------------------------------------------------
+// Round-to-nearest (ties away from zero) to TF32: keep 10 mantissa bits.
+float tf32_round(float x);
+// Checks the device (cc 10.3, cluster launch) and sets the kernels'
+// per-device attributes, once per device.
+int prepare_device(int device);
+// LSTM_E_INVALID unless p is 16-byte aligned.
+int check_aligned(const void *p, const char *what);
+// The device that owns device pointer p; LSTM_E_INVALID for host memory.
+int pointer_device(const void *p, int *device);
+
+// Makes `device` current for the scope and restores the previous one.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int device)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess)
+            prev = -1;
+        ok = (prev == device) || cudaSetDevice(device) == cudaSuccess;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0)
+            cudaSetDevice(prev);
+    }
+};
+
 // ---- projection (projection.cu) ------------------------------------------
 // Rows per TMA box of the projection's operands: X rows, and the W gate rows
 // one CTA of a 2-CTA cluster loads (half of a 256-row W tile).
@@ -54,6 +82,26 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
                       const CUtensorMap &wlo_map, float *g, int rows, int kp, int math,
                       unsigned *fault, cudaStream_t stream);
 int projection_prepare(int device);
+
+// ---- dense heads of the segmentation model (projection.cu kernels) --------
+// W rows one CTA of a 2-CTA cluster loads: half of a 128-column LeakyReLU
+// tile, half of the 16-column classifier tile.
+constexpr int kHeadWBoxRows = 64;
+constexpr int kClassifierWBoxRows = 8;
+// Store map of a row-major fp32 matrix [rows][cols] written in 32 x 32
+// slices with the 128-byte swizzle.
+int encode_store_map(CUtensorMap *map, float *base, long rows, int cols);
+// out[rows][128] = leaky(X . W^T + bias) with W^T given as TF32 hi/lo planes
+// [128][kp] (maps from encode_matrix_map with kHeadWBoxRows), 3xTF32.
+int launch_head_leaky(const CUtensorMap &x_map, const CUtensorMap &whi_map,
+                      const CUtensorMap &wlo_map, const CUtensorMap &out_map,
+                      const float *bias, float slope, int rows, int kp, unsigned *fault,
+                      cudaStream_t stream);
+// out[rows][7] = log_softmax(X . W^T + bias) with W^T planes [16][kp] (rows
+// 7..15 zero; maps with kClassifierWBoxRows), 3xTF32.
+int launch_head_classifier(const CUtensorMap &x_map, const CUtensorMap &whi_map,
+                           const CUtensorMap &wlo_map, const float *bias, float *out, int rows,
+                           int kp, unsigned *fault, cudaStream_t stream);
 
 // ---- recurrence (recurrence.cu) ------------------------------------------
 int launch_recurrence(const float *g, const float *rp, const float *bias,
@@ -265,6 +313,16 @@ __device__ __forceinline__ uint32_t cluster_nid_x()
     return r;
 }
 // 32 lanes x 32 consecutive 32-bit columns: thread (lane) gets its lane's row.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr)
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "

@@ -43,43 +43,67 @@
 namespace lstm {
 namespace {
 
-constexpr int BM = 128;  // rows of G per tile (MMA M)
-constexpr int BN = 256;  // gate columns per tile (MMA N)
+constexpr int BM = 128;  // rows per tile (MMA M)
 constexpr int BK = 16;   // fp32 per K block = 64 bytes
 constexpr int A_BYTES = BM * BK * 4;                     // 8 KiB
-constexpr int B_BYTES = BN * BK * 4;                     // 16 KiB
-constexpr int RING_BYTES = 4 * (2 * A_BYTES + 2 * B_BYTES);  // 192 KiB of stages
-
-// The stage ring of each mode: 3xTF32 keeps A hi, A lo, B hi, B lo per stage
-// (48 KiB, 4 stages); the single-product mode only A hi and B hi (24 KiB), so
-// the same ring holds 8 stages and twice the K blocks in flight.
-template <bool SINGLE>
-struct Ring {
-    static constexpr int STAGE_BYTES = SINGLE ? A_BYTES + B_BYTES : 2 * A_BYTES + 2 * B_BYTES;
-    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;
-    static constexpr int A_LO = A_BYTES;                         // 3xTF32 only
-    static constexpr int B_HI = SINGLE ? A_BYTES : 2 * A_BYTES;
-    static constexpr int B_LO = B_HI + B_BYTES;                  // 3xTF32 only
-    static constexpr uint32_t TX_BYTES = SINGLE ? A_BYTES + B_BYTES : A_BYTES + 2 * B_BYTES;
-};
-constexpr int MAX_STAGES = Ring<true>::STAGES;
-constexpr uint32_t ACC_COLS = BN;                        // fp32 columns per accumulator
-constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;             // two accumulators
+constexpr int RING_BYTES = 192 * 1024;                   // the K-block stage ring
+constexpr int MAX_STAGES = 8;
 constexpr int CONVERTERS = 128;                          // warps 0-3
 constexpr int EPILOGUE = 128;                            // warps 4-7
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
-constexpr int OUT_COLS = 32;                             // G columns per store slice
+constexpr int OUT_COLS = 32;                             // columns per store slice
 constexpr int OUT_BYTES = 32 * OUT_COLS * 4;             // one warp's 32 rows: 4 KiB
 constexpr int OUT_OFFSET = RING_BYTES;                   // staging: 4 warps x 2 slices
 constexpr size_t SMEM_BYTES = OUT_OFFSET + 4 * 2 * OUT_BYTES + 1024 + 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
-constexpr int TILES_N = kGateColumns / BN;          // 4
 constexpr int CLUSTER = 2;                          // CTAs sharing a W tile
 constexpr uint16_t PAIR_MASK = (1u << CLUSTER) - 1;
-constexpr int B_HALF_BYTES = B_BYTES / CLUSTER;     // W rows one CTA loads
-static_assert(BN / CLUSTER == kProjectionWBoxRows && BM == kProjectionBoxRows, "TMA boxes");
+
+// What an instantiation writes: the LSTM gate pre-activations G (1024
+// columns in tiles of 256, no bias), or one dense head layer of the
+// segmentation model: bias + LeakyReLU (a 128-column tile), or bias +
+// log-softmax over the 7 classes (a 16-column tile; W rows 7..15 are zero).
+enum Epilogue { kEpiGates = 0, kEpiLeaky = 1, kEpiLogSoftmax = 2 };
+constexpr int kClasses = 7;
+
+template <int BN_, bool SINGLE_, int EPI_>
+struct Shape {
+    static constexpr int BN = BN_;  // MMA N: output columns per tile
+    static constexpr bool SINGLE = SINGLE_;
+    static constexpr int EPI = EPI_;
+    static constexpr int B_BYTES = BN * BK * 4;
+    // 3xTF32 keeps A hi, A lo, B hi, B lo per stage; the single-product
+    // mode only A hi and B hi, so the same ring holds twice the K blocks
+    static constexpr int STAGE_BYTES = SINGLE ? A_BYTES + B_BYTES : 2 * (A_BYTES + B_BYTES);
+    static constexpr int STAGES =
+        RING_BYTES / STAGE_BYTES < MAX_STAGES ? RING_BYTES / STAGE_BYTES : MAX_STAGES;
+    static constexpr int A_LO = A_BYTES;                         // 3xTF32 only
+    static constexpr int B_HI = SINGLE ? A_BYTES : 2 * A_BYTES;
+    static constexpr int B_LO = B_HI + B_BYTES;                  // 3xTF32 only
+    static constexpr uint32_t TX_BYTES = SINGLE ? A_BYTES + B_BYTES : A_BYTES + 2 * B_BYTES;
+    static constexpr int B_HALF_BYTES = B_BYTES / CLUSTER;      // W rows one CTA loads
+    static constexpr uint32_t ACC_COLS = BN;                     // per accumulator
+    static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+    static constexpr int TILES_N = EPI == kEpiGates ? kGateColumns / BN : 1;
+    // instruction descriptor, kind::tf32: D fp32, A and B TF32, both K-major
+    static constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
+                                      (static_cast<uint32_t>(BN >> 3) << 17) |
+                                      (static_cast<uint32_t>(BM >> 4) << 24);
+    static_assert(STAGE_BYTES % 1024 == 0 && BN % 16 == 0 && BN <= 256 && STAGES >= 4,
+                  "tile shape");
+    static_assert(EPI != kEpiLogSoftmax || BN == 16, "the classifier tile is 16 columns");
+};
+using GatesShape = Shape<256, false, kEpiGates>;
+using GatesTf32Shape = Shape<256, true, kEpiGates>;
+using LeakyShape = Shape<128, false, kEpiLeaky>;
+using ClassifierShape = Shape<16, false, kEpiLogSoftmax>;
+static_assert(GatesShape::BN / CLUSTER == kProjectionWBoxRows && BM == kProjectionBoxRows,
+              "TMA boxes");
+static_assert(LeakyShape::BN / CLUSTER == kHeadWBoxRows &&
+                  ClassifierShape::BN / CLUSTER == kClassifierWBoxRows,
+              "head TMA boxes");
 
 // tcgen05 shared-memory matrix descriptor: K-major operand, 64-byte
 // swizzle, 8-row groups 512 bytes apart.
@@ -91,12 +115,6 @@ __device__ __forceinline__ uint64_t sw64_desc(uint32_t addr)
            (static_cast<uint64_t>(1) << 46) |           // descriptor version (tcgen05)
            (static_cast<uint64_t>(4) << 61);            // 64-byte swizzle
 }
-
-// Instruction descriptor, kind::tf32: D fp32, A and B TF32, both K-major,
-// N = 256, M = 128.
-constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
-                           (static_cast<uint32_t>(BN >> 3) << 17) |
-                           (static_cast<uint32_t>(BM >> 4) << 24);
 
 __device__ __forceinline__ void split4(float4 v, float4 &hi, float4 &lo)
 {
@@ -120,17 +138,23 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, unsig
     }
 }
 
-template <bool SINGLE>
+template <class S>
 __global__ void __launch_bounds__(THREADS, 1)
 projection_kernel(const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap whi_map,
                   const __grid_constant__ CUtensorMap wlo_map,
-                  const __grid_constant__ CUtensorMap g_map, int rows,
-                  int kblocks, int pairs, unsigned *fault)
+                  const __grid_constant__ CUtensorMap out_map, float *__restrict__ out,
+                  const float *__restrict__ bias, float slope, int rows, int kblocks, int pairs,
+                  unsigned *fault)
 {
-    using RG = Ring<SINGLE>;
-    constexpr int STAGES = RG::STAGES;
-    constexpr int STAGE_BYTES = RG::STAGE_BYTES;
+    using RG = S;
+    constexpr bool SINGLE = S::SINGLE;
+    constexpr int STAGES = S::STAGES;
+    constexpr int STAGE_BYTES = S::STAGE_BYTES;
+    constexpr int BN = S::BN;
+    constexpr int TILES_N = S::TILES_N;
+    constexpr uint32_t ACC_COLS = S::ACC_COLS;
+    constexpr uint32_t IDESC = S::IDESC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -164,10 +188,10 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         ptx::prefetch_tensormap(&x_map);
         ptx::prefetch_tensormap(&whi_map);
         ptx::prefetch_tensormap(&wlo_map);
-        ptx::prefetch_tensormap(&g_map);
+        ptx::prefetch_tensormap(&out_map);
     }
     if (warp == MMA_WARP) {
-        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+        ptx::tmem_alloc(tmem_slot, S::TMEM_COLS);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -199,10 +223,10 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     uint8_t *st = smem + s * STAGE_BYTES;
                     ptx::mbar_arrive_expect_tx(&full[s], RG::TX_BYTES);
                     ptx::tma_load_2d(st, &x_map, &full[s], kb * BK, m0);
-                    ptx::tma_load_2d_multicast(st + RG::B_HI + rank * B_HALF_BYTES, &whi_map,
+                    ptx::tma_load_2d_multicast(st + RG::B_HI + rank * S::B_HALF_BYTES, &whi_map,
                                                &full[s], kb * BK, nh, PAIR_MASK);
                     if constexpr (!SINGLE)
-                        ptx::tma_load_2d_multicast(st + RG::B_LO + rank * B_HALF_BYTES, &wlo_map,
+                        ptx::tma_load_2d_multicast(st + RG::B_LO + rank * S::B_HALF_BYTES, &wlo_map,
                                                    &full[s], kb * BK, nh, PAIR_MASK);
                     issued = kbi + 1;
                 }
@@ -300,7 +324,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         // epilogue: warp 4+q reads TMEM lanes 32q .. 32q+31 (warp id mod 4 = q)
         const int q = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint8_t *out = smem + OUT_OFFSET + q * 2 * OUT_BYTES;
+        uint8_t *stage_out = smem + OUT_OFFSET + q * 2 * OUT_BYTES;
         int slices = 0;  // store slices this warp issued
         int ti = 0;
         for (int t = first; t < pairs; t += stride, ++ti) {
@@ -315,44 +339,79 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             const int m0 = ((t / TILES_N) * CLUSTER + rank) * BM + q * 32;  // this warp's rows
             const int n0 = (t % TILES_N) * BN;
             const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(a) * ACC_COLS;
-            // Pace the stores: slice c of this tile goes out once the next
-            // tile's mainloop has issued c/8 of its K blocks, so G streams to
-            // memory under the next tile's compute instead of every CTA
-            // writing its whole tile at once and stalling the loads.
-            const bool paced = t + stride < pairs;
-            const long next_kb = static_cast<long>(ti + 1) * kblocks;
-#pragma unroll 1
-            for (int c = 0; c < BN / OUT_COLS; ++c, ++slices) {
-                if (paced) {
-                    const long want = next_kb + (static_cast<long>(c) * kblocks) / (BN / OUT_COLS);
-                    if (*progress < want && !*abort_flag) {
-                        const uint64_t start = ptx::globaltimer();
-                        while (*progress < want && !*abort_flag &&
-                               ptx::globaltimer() - start < WAIT_LIMIT_NS)
-                            __nanosleep(64);
-                    }
-                }
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(acc + c * OUT_COLS, r);
+            if constexpr (S::EPI == kEpiLogSoftmax) {
+                // lane = row: the 7 class logits, log-softmax, 7 floats out
+                uint32_t r[16];
+                ptx::tmem_ld_32x32b_x16(acc, r);
                 ptx::tmem_ld_wait();
-                // the store that last used this buffer (two slices ago) has read it
-                uint8_t *buf = out + (slices & 1) * OUT_BYTES;
-                if (lane == 0)
-                    ptx::bulk_wait_group_read<1>();
-                __syncwarp();
-                // lane = row; 16-byte chunk v of the row goes to chunk v ^ (row % 8)
-                float4 *row = reinterpret_cast<float4 *>(buf + lane * (OUT_COLS * 4));
+                const long m = static_cast<long>(m0) + lane;
+                if (m < rows) {
+                    float z[kClasses];
+                    float zmax = -INFINITY;
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    row[v ^ (lane & 7)] =
-                        make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (m0 < rows)
-                        ptx::tma_store_2d(&g_map, buf, n0 + c * OUT_COLS, m0);
-                    ptx::bulk_commit_group();
+                    for (int j = 0; j < kClasses; ++j) {
+                        z[j] = __uint_as_float(r[j]) + __ldg(bias + j);
+                        zmax = fmaxf(zmax, z[j]);
+                    }
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < kClasses; ++j)
+                        sum += expf(z[j] - zmax);
+                    const float lse = zmax + logf(sum);
+#pragma unroll
+                    for (int j = 0; j < kClasses; ++j)
+                        out[m * kClasses + j] = z[j] - lse;
+                }
+            } else {
+                // Pace the stores: slice c of this tile goes out once the
+                // next tile's mainloop has issued c/slices of its K blocks,
+                // so the output streams to memory under the next tile's
+                // compute instead of every CTA writing its whole tile at once
+                // and stalling the loads.
+                constexpr int NSLICE = BN / OUT_COLS;
+                const bool paced = t + stride < pairs;
+                const long next_kb = static_cast<long>(ti + 1) * kblocks;
+#pragma unroll 1
+                for (int c = 0; c < NSLICE; ++c, ++slices) {
+                    if (paced) {
+                        const long want = next_kb + (static_cast<long>(c) * kblocks) / NSLICE;
+                        if (*progress < want && !*abort_flag) {
+                            const uint64_t start = ptx::globaltimer();
+                            while (*progress < want && !*abort_flag &&
+                                   ptx::globaltimer() - start < WAIT_LIMIT_NS)
+                                __nanosleep(64);
+                        }
+                    }
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(acc + c * OUT_COLS, r);
+                    ptx::tmem_ld_wait();
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        v[j] = __uint_as_float(r[j]);
+                        if constexpr (S::EPI == kEpiLeaky) {
+                            v[j] += __ldg(bias + n0 + c * OUT_COLS + j);
+                            v[j] = v[j] >= 0.0f ? v[j] : slope * v[j];
+                        }
+                    }
+                    // the store that last used this buffer (two slices ago) has read it
+                    uint8_t *buf = stage_out + (slices & 1) * OUT_BYTES;
+                    if (lane == 0)
+                        ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
+                    // lane = row; 16-byte chunk j of the row goes to chunk j ^ (row % 8)
+                    float4 *row = reinterpret_cast<float4 *>(buf + lane * (OUT_COLS * 4));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        row[j ^ (lane & 7)] =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (m0 < rows)
+                            ptx::tma_store_2d(&out_map, buf, n0 + c * OUT_COLS, m0);
+                        ptx::bulk_commit_group();
+                    }
                 }
             }
             ptx::tc_fence_before();
@@ -379,7 +438,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         }
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, TMEM_COLS);
+        ptx::tmem_dealloc(tmem, S::TMEM_COLS);
     }
     // neither CTA leaves while the other may still multicast into it or
     // release its stages
@@ -438,58 +497,35 @@ int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols, 
     return encode_map(map, base, rows, cols, BK, box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-int projection_prepare(int device)
+int encode_store_map(CUtensorMap *map, float *base, long rows, int cols)
 {
-    if (device < 0 || device >= 64)
-        return fail(LSTM_E_INVALID, "device %d out of range", device);
-    int sms = 0;
-    int st = cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
-                         "SM count");
-    if (st != LSTM_OK)
-        return st;
-    g_sm_count[device] = sms;
-    for (const void *fn : {reinterpret_cast<const void *>(&projection_kernel<false>),
-                           reinterpret_cast<const void *>(&projection_kernel<true>)}) {
-        st = cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              static_cast<int>(SMEM_BYTES)),
-                         "projection shared-memory attribute");
-        if (st != LSTM_OK)
-            return st;
-    }
-    // the persistent grid is no larger than what runs at once (both modes
-    // have the same block and shared-memory size)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CLUSTER);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    st = cuda_status(cudaOccupancyMaxActiveClusters(&n, projection_kernel<false>, &cfg),
-                     "projection max active clusters");
-    if (st != LSTM_OK)
-        return st;
-    g_max_clusters[device] = n > 0 ? n : sms / CLUSTER;
-    return LSTM_OK;
+    return encode_map(map, base, rows, cols, OUT_COLS, 32, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                      const CUtensorMap &wlo_map, float *g, int rows, int kp, int math,
-                      unsigned *fault, cudaStream_t stream)
+namespace {
+// Every instantiation, for the per-device attributes.
+const void *const kKernels[] = {
+    reinterpret_cast<const void *>(&projection_kernel<GatesShape>),
+    reinterpret_cast<const void *>(&projection_kernel<GatesTf32Shape>),
+    reinterpret_cast<const void *>(&projection_kernel<LeakyShape>),
+    reinterpret_cast<const void *>(&projection_kernel<ClassifierShape>),
+};
+
+// Persistent grid over the row tiles (pairs of 128-row tiles, one per CTA of
+// a 2-CTA cluster) times S::TILES_N column tiles, no larger than what runs at
+// once.  out_map is only read by the TMA-store epilogues.
+template <class S>
+int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
+                 const CUtensorMap &wlo_map, const CUtensorMap &out_map, float *out,
+                 const float *bias, float slope, int rows, int kp, unsigned *fault,
+                 cudaStream_t stream)
 {
-    if (math != LSTM_MATH_3XTF32 && math != LSTM_MATH_TF32)
-        return fail(LSTM_E_INVALID, "projection: unknown math mode %d", math);
     if (rows <= 0 || kp <= 0 || kp % 32 != 0)
-        return fail(LSTM_E_INVALID, "projection: rows %d, kp %d", rows, kp);
+        return fail(LSTM_E_INVALID, "tensor-core GEMM: rows %d, kp %d", rows, kp);
     const long mtiles = (static_cast<long>(rows) + BM - 1) / BM;
-    const long pairs = (mtiles + CLUSTER - 1) / CLUSTER * TILES_N;
+    const long pairs = (mtiles + CLUSTER - 1) / CLUSTER * S::TILES_N;
     if (pairs > 0x7fffffffL)
-        return fail(LSTM_E_OVERFLOW, "projection: %d rows", rows);
+        return fail(LSTM_E_OVERFLOW, "tensor-core GEMM: %d rows", rows);
     int dev = 0;
     int st = cuda_status(cudaGetDevice(&dev), "current device");
     if (st != LSTM_OK)
@@ -509,18 +545,90 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // G is written in 32 x 32 slices (one epilogue warp's rows), 128-byte swizzle
-    CUtensorMap g_map;
-    if ((st = encode_map(&g_map, g, rows, kGateColumns, OUT_COLS, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
-        return st;
     const int kblocks = kp / BK;
     const int npairs = static_cast<int>(pairs);
-    return cuda_status(math == LSTM_MATH_TF32
-                           ? cudaLaunchKernelEx(&cfg, projection_kernel<true>, x_map, whi_map,
-                                                wlo_map, g_map, rows, kblocks, npairs, fault)
-                           : cudaLaunchKernelEx(&cfg, projection_kernel<false>, x_map, whi_map,
-                                                wlo_map, g_map, rows, kblocks, npairs, fault),
-                       "projection launch");
+    return cuda_status(cudaLaunchKernelEx(&cfg, projection_kernel<S>, x_map, whi_map, wlo_map,
+                                          out_map, out, bias, slope, rows, kblocks, npairs,
+                                          fault),
+                       "tensor-core GEMM launch");
+}
+}  // namespace
+
+int projection_prepare(int device)
+{
+    if (device < 0 || device >= 64)
+        return fail(LSTM_E_INVALID, "device %d out of range", device);
+    int sms = 0;
+    int st = cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
+                         "SM count");
+    if (st != LSTM_OK)
+        return st;
+    g_sm_count[device] = sms;
+    for (const void *fn : kKernels) {
+        st = cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(SMEM_BYTES)),
+                         "projection shared-memory attribute");
+        if (st != LSTM_OK)
+            return st;
+    }
+    // the persistent grid is no larger than what runs at once (every
+    // instantiation has the same block and shared-memory size)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CLUSTER);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    st = cuda_status(cudaOccupancyMaxActiveClusters(&n, projection_kernel<GatesShape>, &cfg),
+                     "projection max active clusters");
+    if (st != LSTM_OK)
+        return st;
+    g_max_clusters[device] = n > 0 ? n : sms / CLUSTER;
+    return LSTM_OK;
+}
+
+int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
+                      const CUtensorMap &wlo_map, float *g, int rows, int kp, int math,
+                      unsigned *fault, cudaStream_t stream)
+{
+    if (math != LSTM_MATH_3XTF32 && math != LSTM_MATH_TF32)
+        return fail(LSTM_E_INVALID, "projection: unknown math mode %d", math);
+    if (rows <= 0)
+        return fail(LSTM_E_INVALID, "projection: rows %d", rows);
+    // G is written in 32 x 32 slices (one epilogue warp's rows), 128-byte swizzle
+    CUtensorMap g_map;
+    int st = encode_store_map(&g_map, g, rows, kGateColumns);
+    if (st != LSTM_OK)
+        return st;
+    return math == LSTM_MATH_TF32
+               ? launch_tiles<GatesTf32Shape>(x_map, whi_map, wlo_map, g_map, nullptr, nullptr,
+                                              0.0f, rows, kp, fault, stream)
+               : launch_tiles<GatesShape>(x_map, whi_map, wlo_map, g_map, nullptr, nullptr, 0.0f,
+                                          rows, kp, fault, stream);
+}
+
+int launch_head_leaky(const CUtensorMap &x_map, const CUtensorMap &whi_map,
+                      const CUtensorMap &wlo_map, const CUtensorMap &out_map,
+                      const float *bias, float slope, int rows, int kp, unsigned *fault,
+                      cudaStream_t stream)
+{
+    return launch_tiles<LeakyShape>(x_map, whi_map, wlo_map, out_map, nullptr, bias, slope, rows,
+                                    kp, fault, stream);
+}
+
+int launch_head_classifier(const CUtensorMap &x_map, const CUtensorMap &whi_map,
+                           const CUtensorMap &wlo_map, const float *bias, float *out, int rows,
+                           int kp, unsigned *fault, cudaStream_t stream)
+{
+    // no store map: the log-softmax rows (7 floats) are written directly
+    return launch_tiles<ClassifierShape>(x_map, whi_map, wlo_map, x_map, out, bias, 0.0f, rows,
+                                         kp, fault, stream);
 }
 
 } // namespace lstm

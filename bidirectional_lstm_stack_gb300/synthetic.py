@@ -83,6 +83,24 @@ def stack_weights(seed: int = WEIGHT_SEED, hidden: int = HIDDEN,
     return out
 
 
+HEADS_SEED = 7
+
+
+def heads_weights(seed: int = HEADS_SEED, dtype=np.float32):
+    """Random weights of the segmentation model's dense heads, row-major
+    ``[k, n]``: w0 ``[256, 128]``, w1 ``[128, 128]``, w2 ``[128, 7]`` and the
+    biases ``[n]``, every entry U(-1/sqrt(k), 1/sqrt(k)) for its layer's
+    input width k (the default range of a freshly initialised linear
+    layer)."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    for name, (k, n) in (("0", (2 * HIDDEN, 128)), ("1", (128, 128)), ("2", (128, 7))):
+        bound = 1.0 / np.sqrt(k)
+        out["w" + name] = rng.uniform(-bound, bound, size=(k, n)).astype(dtype)
+        out["b" + name] = rng.uniform(-bound, bound, size=(n,)).astype(dtype)
+    return out
+
+
 def stack_input(workload: Workload, features: int = FEATURES,
                 dtype=np.float32) -> np.ndarray:
     """The input ``[B, T, features]`` of a workload, from its seed."""

@@ -304,6 +304,46 @@ int lstm_layer_forward_static(const float *x, int batch, int steps,
  * device. */
 int lstm_fault_status(unsigned int *fault);
 
+/* ---------------------------------------------------------------------------
+ * Dense heads of the segmentation model on the stack output (segdense.rs,
+ * `Site::Linear0` / `Linear1` / `Linear2` and `DenseOxide`, which fuses the
+ * bias, LeakyReLU and log-softmax epilogues into the GEMMs).  For each row
+ * m of y [rows][256] (a stack output row):
+ *   h1 = leaky(y[m] W0 + b0),  h2 = leaky(h1 W1 + b1),
+ *   logp[m] = log_softmax(h2 W2 + b2)  (7 classes),
+ * leaky(v) = v for v >= 0, negative_slope * v below (the pages name the
+ * activation without a slope; PyTorch's default is 0.01).  Every layer runs
+ * on the tensor cores in 3xTF32 with fp32 accumulation.
+ * ------------------------------------------------------------------------- */
+
+#define LSTM_HEADS_HIDDEN 128
+#define LSTM_HEADS_CLASSES 7
+
+typedef struct lstm_heads lstm_heads; /* opaque; owned by the library */
+
+/* Packs the weights (host fp32, read during the call only; row-major [k, n]
+ * as the pages store them):
+ *   w0 : [256][128], b0 : [128],  w1 : [128][128], b1 : [128],
+ *   w2 : [128][7],   b2 : [7]
+ * and allocates the two [max_rows][128] intermediate buffers on `device`.
+ * Errors: LSTM_E_INVALID (null, max_rows <= 0), LSTM_E_DEVICE, LSTM_E_CUDA,
+ * LSTM_E_ALLOC.  Nothing is leaked on failure. */
+int lstm_heads_create(const float *w0, const float *b0, const float *w1,
+                      const float *b1, const float *w2, const float *b2,
+                      float negative_slope, int max_rows, int device,
+                      lstm_heads **out);
+
+/* logp (device [rows][7]) = the heads on y (device [rows][256], 16-byte
+ * aligned; e.g. lstm_stack_forward's output with rows = batch*steps),
+ * asynchronously on `stream`; allocates nothing.  Calls on one object must
+ * not overlap (they share its intermediate buffers).  Errors: LSTM_E_INVALID
+ * (null, rows outside 1..max_rows, misaligned, wrong device), LSTM_E_LENGTH
+ * (y_len != rows*256 or logp_len != rows*7), LSTM_E_CUDA. */
+int lstm_heads_forward(lstm_heads *h, const float *y, size_t y_len, float *logp,
+                       size_t logp_len, int rows, void *stream);
+
+void lstm_heads_destroy(lstm_heads *h);
+
 #ifdef __cplusplus
 }
 #endif

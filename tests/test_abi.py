@@ -143,3 +143,15 @@ def test_packer_onnx_gate_order_matches_default(lib):
     with pytest.raises(binding.LSTMError) as e:
         binding.lstm_pack_layer(w, r, b, 60, 64, 2)
     assert e.value.code == binding.LSTM_E_INVALID
+
+
+def test_heads_create_rejects_null_weights(lib):
+    import ctypes
+    out = ctypes.c_void_p()
+    w = np.zeros(256 * 128, np.float32)
+    ptrs = [w.ctypes.data] * 5 + [None]
+    assert lib.lstm_heads_create(*ptrs, 0.01, 10, 0, ctypes.byref(out)) == binding.LSTM_E_INVALID
+    assert not out.value
+    assert lib.lstm_heads_create(*([w.ctypes.data] * 6), 0.01, 0, 0,
+                                 ctypes.byref(out)) == binding.LSTM_E_INVALID
+    lib.lstm_heads_destroy(None)
