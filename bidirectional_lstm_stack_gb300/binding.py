@@ -91,6 +91,9 @@ def load():
                                       ctypes.POINTER(_vp)]),
             "lstm_heads_forward": (i, [_vp, _vp, sz, _vp, sz, i, _vp]),
             "lstm_heads_destroy": (None, [_vp]),
+            "lstm_test_fail_allocations": (i, [i, i]),
+            "lstm_test_fail_launches": (i, [i, i]),
+            "lstm_test_recurrence_timeout": (i, [i, ctypes.c_uint, i]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -45,6 +45,52 @@ int cuda_status(cudaError_t err, const char *what)
     return fail(LSTM_E_CUDA, "%s: %s (%s)", what, cudaGetErrorString(err), cudaGetErrorName(err));
 }
 
+namespace {
+// Failure injection (lstm_test_* hooks): let `skip` calls through, then fail
+// `count` of them.
+struct Injection {
+    std::mutex mu;
+    int skip = 0;
+    int count = 0;
+    bool take()
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (count <= 0)
+            return false;
+        if (skip > 0) {
+            --skip;
+            return false;
+        }
+        --count;
+        return true;
+    }
+    void set(int s, int c)
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        skip = s > 0 ? s : 0;
+        count = c > 0 ? c : 0;
+    }
+};
+Injection g_fail_allocs;
+Injection g_fail_launches;
+}  // namespace
+
+cudaError_t device_alloc(void **p, size_t bytes)
+{
+    if (g_fail_allocs.take()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+
+int check_launch_injection(const char *what)
+{
+    if (g_fail_launches.take())
+        return fail(LSTM_E_CUDA, "%s: injected launch failure (test hook)", what);
+    return LSTM_OK;
+}
+
 unsigned *fault_word()
 {
     // one address per device; resolved with that device current
@@ -176,6 +222,7 @@ struct lstm_stack {
     bool timed_once = false;
     cudaEvent_t phase[kPhaseEvents] = {};
     unsigned *fault = nullptr;
+    unsigned *fault_host = nullptr;  // pinned copy of the fault word (forward_host)
     // CUDA-graph replay of the forward pass, one instantiated graph per
     // argument set (least recently used evicted)
     struct Graph {
@@ -262,6 +309,8 @@ extern "C" void lstm_stack_destroy(lstm_stack *s)
     cudaFree(s->ping[1]);
     cudaFree(s->x_stage);
     cudaFree(s->y_stage);
+    if (s->fault_host)
+        cudaFreeHost(s->fault_host);
     for (int l = 0; l < kLayers; ++l) {
         if (s->fork[l])
             cudaEventDestroy(s->fork[l]);
@@ -357,7 +406,7 @@ extern "C" int lstm_stack_create_ordered(const lstm_stack_weights *weights, int 
         }
     }
     auto alloc = [&](float **p, long floats, const char *what) -> int {
-        cudaError_t e = cudaMalloc(reinterpret_cast<void **>(p), floats * sizeof(float));
+        cudaError_t e = device_alloc(reinterpret_cast<void **>(p), floats * sizeof(float));
         if (e != cudaSuccess) {
             cudaGetLastError();
             return fail(LSTM_E_ALLOC, "cudaMalloc of %s (%ld bytes): %s", what,
@@ -375,6 +424,9 @@ extern "C" int lstm_stack_create_ordered(const lstm_stack_weights *weights, int 
     if (st == LSTM_OK) st = alloc(&s->ping[1], max_rows * kOutput, "layer buffer 1");
     if (st == LSTM_OK) st = alloc(&s->x_stage, max_rows * kFeatures, "input staging");
     if (st == LSTM_OK) st = alloc(&s->y_stage, max_rows * kOutput, "output staging");
+    if (st == LSTM_OK)
+        st = cuda_status(cudaMallocHost(reinterpret_cast<void **>(&s->fault_host), sizeof(unsigned)),
+                         "pinned fault word");
     if (st != LSTM_OK) {
         lstm_stack_destroy(s);
         return st;
@@ -463,25 +515,35 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
         if ((st = cuda_status(cudaEventRecord(s->fork[l], stream), "fork record")) ||
             (st = cuda_status(cudaStreamWaitEvent(s->side, s->fork[l], 0), "fork wait")))
             return st;
-        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 1, 0), stream, cudaEventRecordExternal), "event")))
-            return st;
-        st = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps, 0, s->fault,
-                               stream);
+        // The side stream is forked from here: whatever fails below, it is
+        // joined back before returning (a capture must end joined, and the
+        // caller's stream must not run ahead of work on the side stream).
+        auto directions = [&]() -> int {
+            int r;
+            if (s->timing && (r = cuda_status(cudaEventRecordWithFlags(ev(l, 1, 0), stream, cudaEventRecordExternal), "event")))
+                return r;
+            if ((r = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps, 0,
+                                       s->fault, stream)))
+                return r;
+            if (s->timing && (r = cuda_status(cudaEventRecordWithFlags(ev(l, 1, 1), stream, cudaEventRecordExternal), "event")))
+                return r;
+            if (s->timing && (r = cuda_status(cudaEventRecordWithFlags(ev(l, 2, 0), s->side, cudaEventRecordExternal), "event")))
+                return r;
+            if ((r = launch_recurrence(s->gates, s->rp[l] + kGates * kHidden, s->bias[l] + kGates,
+                                       dst, batch, steps, 1, s->fault, s->side)))
+                return r;
+            if (s->timing && (r = cuda_status(cudaEventRecordWithFlags(ev(l, 2, 1), s->side, cudaEventRecordExternal), "event")))
+                return r;
+            return LSTM_OK;
+        };
+        st = directions();
+        int jst = cuda_status(cudaEventRecord(s->join[l], s->side), "join record");
+        if (jst == LSTM_OK)
+            jst = cuda_status(cudaStreamWaitEvent(stream, s->join[l], 0), "join wait");
         if (st != LSTM_OK)
             return st;
-        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 1, 1), stream, cudaEventRecordExternal), "event")))
-            return st;
-        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 2, 0), s->side, cudaEventRecordExternal), "event")))
-            return st;
-        st = launch_recurrence(s->gates, s->rp[l] + kGates * kHidden, s->bias[l] + kGates, dst,
-                               batch, steps, 1, s->fault, s->side);
-        if (st != LSTM_OK)
-            return st;
-        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 2, 1), s->side, cudaEventRecordExternal), "event")))
-            return st;
-        if ((st = cuda_status(cudaEventRecord(s->join[l], s->side), "join record")) ||
-            (st = cuda_status(cudaStreamWaitEvent(stream, s->join[l], 0), "join wait")))
-            return st;
+        if (jst != LSTM_OK)
+            return jst;
     }
     if (s->timing)
         s->timed_once = true;
@@ -505,7 +567,7 @@ int forward_replay(lstm_stack *s, const float *x, float *y, int batch, int steps
     int st = cuda_status(cudaStreamIsCapturing(stream, &cs), "stream capture status");
     if (st != LSTM_OK)
         return st;
-    if (!s->use_graphs || cs != cudaStreamCaptureStatusNone)
+    if (!s->use_graphs || cs != cudaStreamCaptureStatusNone || recurrence_test_active(s->device))
         return forward_device(s, x, y, batch, steps, stream);
     lstm_stack::Graph *hit = nullptr, *victim = &s->graphs[0];
     for (auto &gr : s->graphs) {
@@ -609,7 +671,21 @@ extern "C" int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_
                                           cudaMemcpyDeviceToHost, st_),
                           "output copy")))
         return st;
-    return cuda_status(cudaStreamSynchronize(st_), "forward_host synchronize");
+    // the kernels' fault word comes back with the result
+    if ((st = cuda_status(cudaMemcpyAsync(s->fault_host, s->fault, sizeof(unsigned),
+                                          cudaMemcpyDeviceToHost, st_),
+                          "fault word copy")))
+        return st;
+    if ((st = cuda_status(cudaStreamSynchronize(st_), "forward_host synchronize")))
+        return st;
+    if (const unsigned bits = *s->fault_host) {
+        cudaMemset(s->fault, 0, sizeof(unsigned));
+        return fail(LSTM_E_FAULT,
+                    "forward_host: a kernel's bounded wait ran out (fault bits 0x%x); the "
+                    "result is not valid",
+                    bits);
+    }
+    return LSTM_OK;
 }
 
 extern "C" int lstm_stack_enable_phase_timing(lstm_stack *s, int enable)
@@ -759,4 +835,33 @@ extern "C" int lstm_fault_status(unsigned int *fault)
                           "fault word read")))
         return st;
     return cuda_status(cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(unsigned)), "fault word clear");
+}
+
+// ---- failure-injection hooks (tests only) ----------------------------------
+
+extern "C" int lstm_test_fail_allocations(int skip, int count)
+{
+    g_fail_allocs.set(skip, count);
+    return LSTM_OK;
+}
+
+extern "C" int lstm_test_fail_launches(int skip, int count)
+{
+    g_fail_launches.set(skip, count);
+    return LSTM_OK;
+}
+
+extern "C" int lstm_test_recurrence_timeout(int withhold, unsigned int wait_limit_us, int device)
+{
+    if (wait_limit_us > 2000000u)
+        return fail(LSTM_E_INVALID, "recurrence test: wait limit %u us above 2 s", wait_limit_us);
+    int st = prepare_device(device);
+    if (st != LSTM_OK)
+        return st;
+    DeviceGuard guard(device);
+    if (!guard.ok)
+        return fail(LSTM_E_CUDA, "cannot make device %d current", device);
+    const unsigned long long limit =
+        wait_limit_us ? wait_limit_us * 1000ull : 2000000000ull;  // 0: the default 2 s
+    return recurrence_set_test(withhold != 0, limit);
 }

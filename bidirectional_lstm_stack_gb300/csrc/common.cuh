@@ -44,6 +44,18 @@ float tf32_round(float x);
 // Checks the device (cc 10.3, cluster launch) and sets the kernels'
 // per-device attributes, once per device.
 int prepare_device(int device);
+// cudaMalloc, or an injected cudaErrorMemoryAllocation while the
+// lstm_test_fail_allocations counter is positive.
+cudaError_t device_alloc(void **p, size_t bytes);
+// LSTM_E_CUDA (an injected launch failure) while the lstm_test_fail_launches
+// counter is positive, else LSTM_OK; every kernel launch asks first.
+int check_launch_injection(const char *what);
+// Recurrence failure test: CTA 0 of every cluster withholds its h pushes and
+// every wait gives up after wait_limit_ns (default: 2 s, no withholding).
+int recurrence_set_test(int withhold, unsigned long long wait_limit_ns);
+// Whether a failure-test setting is in force on `device` (the stack then
+// launches directly instead of replaying a graph captured without it).
+bool recurrence_test_active(int device);
 // LSTM_E_INVALID unless p is 16-byte aligned.
 int check_aligned(const void *p, const char *what);
 // The device that owns device pointer p; LSTM_E_INVALID for host memory.

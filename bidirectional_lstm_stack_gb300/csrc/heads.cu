@@ -115,14 +115,14 @@ extern "C" int lstm_heads_create(const float *w0, const float *b0, const float *
             host[off_b[l] + n] = src_b[l][n];
         }
     }
-    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&h->weights), total * sizeof(float));
+    cudaError_t e = device_alloc(reinterpret_cast<void **>(&h->weights), total * sizeof(float));
     if (e == cudaSuccess)
         e = cudaMemcpy(h->weights, host, total * sizeof(float), cudaMemcpyHostToDevice);
     free(host);
     if (e == cudaSuccess)
-        e = cudaMalloc(reinterpret_cast<void **>(&h->h1), max_rows * kMid * sizeof(float));
+        e = device_alloc(reinterpret_cast<void **>(&h->h1), max_rows * kMid * sizeof(float));
     if (e == cudaSuccess)
-        e = cudaMalloc(reinterpret_cast<void **>(&h->h2), max_rows * kMid * sizeof(float));
+        e = device_alloc(reinterpret_cast<void **>(&h->h2), max_rows * kMid * sizeof(float));
     if (e != cudaSuccess) {
         cudaGetLastError();
         lstm_heads_destroy(h);

@@ -547,6 +547,8 @@ int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     cfg.numAttrs = 1;
     const int kblocks = kp / BK;
     const int npairs = static_cast<int>(pairs);
+    if ((st = check_launch_injection("tensor-core GEMM launch")))
+        return st;
     return cuda_status(cudaLaunchKernelEx(&cfg, projection_kernel<S>, x_map, whi_map, wlo_map,
                                           out_map, out, bias, slope, rows, kblocks, npairs,
                                           fault),

@@ -61,6 +61,16 @@ constexpr int HROW = KC * CHUNK_STRIDE;  // floats per window in the h buffer
 constexpr int PF = 4;                 // projection prefetch depth (steps)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
+// Failure-test settings per device, passed to every launch as kernel
+// parameters: the per-wait limit, and whether CTA 0 of every cluster
+// withholds its h pushes (so its peers' waits run out).  Defaults: 2 s, no
+// withholding.
+struct RecurrenceTest {
+    unsigned long long wait_limit_ns = WAIT_LIMIT_NS;
+    int withhold = 0;
+};
+RecurrenceTest g_rec_test[64];
+
 // s(z) = 1 / (1 + e^-z), in [0, 1] for every finite z without a clamp:
 // e^-z overflows to +inf for z < about -88 and __fdividef(1, inf) is 0.
 __device__ __forceinline__ float sigmoid_bounded(float z)
@@ -90,7 +100,7 @@ template <int C, int NW, int NCH = 1, int THREADS = threads_for<C>()>
 __global__ void __launch_bounds__(THREADS, 1)
 recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                   const float *__restrict__ bias, float *__restrict__ y, int batch, int steps,
-                  int direction, unsigned *fault)
+                  int direction, unsigned *fault, unsigned long long wait_limit_ns, int withhold)
 {
     constexpr int U = kHidden / C;       // units per CTA
     constexpr int SLOTS = THREADS / 8;   // 8-lane groups per CTA
@@ -228,6 +238,10 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch)
         c[ch] = 0.0f;
+    // Failure test: CTA 0 of the cluster pushes nothing, so its peers'
+    // waits run out.
+    if (withhold && rank == 0)
+        goto done;
     for (int s0 = 0; s0 < steps; s0 += PFD) {
 #pragma unroll
         for (int p = 0; p < PFD; ++p) {
@@ -241,15 +255,20 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             if (s > 0) {
                 const uint32_t phase = ((s - 1) >> 1) & 1;
                 volatile int *abort_v = &abort_flag;
-                if (!ptx::mbar_try_wait_cluster(&hbar[par], phase) && !*abort_v) {
+                // A wait that runs out (or sees that another warp's did) ends
+                // this thread's steps: it neither re-arms nor pushes again,
+                // so no stuck barrier is armed or credited after the fault.
+                if (!ptx::mbar_try_wait_cluster(&hbar[par], phase)) {
+                    if (*abort_v)
+                        goto done;
                     const uint64_t start = ptx::globaltimer();
                     while (!ptx::mbar_try_wait_cluster(&hbar[par], phase)) {
                         if (*abort_v)
-                            break;
-                        if (ptx::globaltimer() - start > WAIT_LIMIT_NS) {
+                            goto done;
+                        if (ptx::globaltimer() - start > wait_limit_ns) {
                             atomicOr(fault, kFaultRecurrence);
                             *abort_v = 1;
-                            break;
+                            goto done;
                         }
                     }
                 }
@@ -348,6 +367,7 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             gload(s + PFD, gq[p]);
         }
     }
+done:
     // no CTA leaves while a peer may still write into its shared memory
     __syncwarp();
     ptx::cluster_arrive_release();
@@ -456,12 +476,39 @@ int launch_variant(const Variant &v, const float *g, const float *rp, const floa
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    int dev = 0;
+    int st = cuda_status(cudaGetDevice(&dev), "current device");
+    if (st != LSTM_OK)
+        return st;
+    RecurrenceTest test = (dev >= 0 && dev < 64) ? g_rec_test[dev] : RecurrenceTest{};
+    if ((st = check_launch_injection("recurrence launch")))
+        return st;
     void *args[] = {const_cast<float **>(&g), const_cast<float **>(&rp),
-                    const_cast<float **>(&bias), &y, &batch, &steps, &direction, &fault};
+                    const_cast<float **>(&bias), &y, &batch, &steps, &direction, &fault,
+                    &test.wait_limit_ns, &test.withhold};
     return cuda_status(cudaLaunchKernelExC(&cfg, v.fn, args), "recurrence launch");
 }
 
 } // namespace
+
+int recurrence_set_test(int withhold, unsigned long long wait_limit_ns)
+{
+    int dev = 0;
+    int st = cuda_status(cudaGetDevice(&dev), "current device");
+    if (st != LSTM_OK)
+        return st;
+    if (dev < 0 || dev >= 64)
+        return fail(LSTM_E_INVALID, "device %d out of range", dev);
+    g_rec_test[dev].wait_limit_ns = wait_limit_ns;
+    g_rec_test[dev].withhold = withhold;
+    return LSTM_OK;
+}
+
+bool recurrence_test_active(int device)
+{
+    return device >= 0 && device < 64 &&
+           (g_rec_test[device].withhold || g_rec_test[device].wait_limit_ns != WAIT_LIMIT_NS);
+}
 
 int recurrence_prepare(int)
 {

@@ -344,6 +344,32 @@ int lstm_heads_forward(lstm_heads *h, const float *y, size_t y_len, float *logp,
 
 void lstm_heads_destroy(lstm_heads *h);
 
+/* ---------------------------------------------------------------------------
+ * Failure-injection hooks, for tests of the error paths without a GPU fault.
+ * The pages have no counterpart.  Process-wide; not for production use.
+ * ------------------------------------------------------------------------- */
+
+/* After `skip` more device allocations by the library, the next `count` fail
+ * as if cudaMalloc had run out of memory (the calls then return
+ * LSTM_E_ALLOC and free what they had allocated).  count 0 turns it off. */
+int lstm_test_fail_allocations(int skip, int count);
+
+/* After `skip` more kernel launches by the library, the next `count` fail
+ * with LSTM_E_CUDA ("injected launch failure") instead of launching; the
+ * call that hits one still joins its side stream, so the stack stays usable.
+ * count 0 turns it off. */
+int lstm_test_fail_launches(int skip, int count);
+
+/* On `device`: with withhold != 0, CTA 0 of every recurrence cluster stops
+ * pushing its hidden state, so its peers' per-step waits run out; every
+ * recurrence wait gives up after wait_limit_us microseconds (at most 2 s;
+ * 0 = the default 2 s).  A wait that runs out sets the fault word
+ * (lstm_fault_status; lstm_stack_forward_host returns LSTM_E_FAULT), stops
+ * waiting and lets the kernel finish: the context stays usable.  (0, 0)
+ * restores normal operation.  Errors: LSTM_E_INVALID, LSTM_E_DEVICE,
+ * LSTM_E_CUDA. */
+int lstm_test_recurrence_timeout(int withhold, unsigned int wait_limit_us, int device);
+
 #ifdef __cplusplus
 }
 #endif
