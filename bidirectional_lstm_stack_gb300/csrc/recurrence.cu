@@ -33,8 +33,10 @@
 // dependence makes the double buffer safe: a CTA can only push step s+1's h
 // once it holds every unit's h_s, i.e. once every warp of every CTA has
 // finished reading the buffer it is about to overwrite.  Each wait is bounded
-// in time; when one runs out the kernel records a fault bit, stops waiting
-// and finishes (with wrong results) instead of hanging.
+// in time; when one runs out the kernel records a fault bit and every thread
+// that sees it leaves its step loop for the final cluster barrier (no stuck
+// barrier is re-armed or credited again), so the kernel ends, with invalid
+// results, instead of hanging.
 // The arithmetic per (window, unit, gate) is the same for every cluster size
 // and tile width (same K chunks, same pairing, same reduction tree), so all
 // variants give bitwise-identical results.
