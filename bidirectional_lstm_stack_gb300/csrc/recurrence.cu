@@ -73,15 +73,28 @@ struct RecurrenceTest {
 };
 RecurrenceTest g_rec_test[64];
 
-// s(z) = 1 / (1 + e^-z), in [0, 1] for every finite z without a clamp:
-// e^-z overflows to +inf for z < about -88 and __fdividef(1, inf) is 0.
-__device__ __forceinline__ float sigmoid_bounded(float z)
+// Activations through base-2 exponentials of pre-scaled arguments: the
+// recurrent weights, the bias and the projection value of gate q are
+// multiplied by k_q = -log2(e) (-2 log2(e) for the cell candidate) as they
+// are loaded, so a step produces w = k_q z directly and
+//   s(z) = 1 / (1 + 2^w),   tanh(z) = 2 s(2z) - 1 = 2 / (1 + 2^w) - 1.
+// 2^w overflows to +inf for large w and 1/inf is 0, so every gate is in
+// [0, 1] (the candidate in [-1, 1]) for every finite z, without a clamp.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2_approx(float x)
 {
-    return __fdividef(1.0f, 1.0f + __expf(-z));
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-__device__ __forceinline__ float tanh_bounded(float z)
+__device__ __forceinline__ float inv_one_plus_ex2(float w)
 {
-    return 2.0f * sigmoid_bounded(2.0f * z) - 1.0f;
+    return __fdividef(1.0f, 1.0f + ex2_approx(w));
+}
+// tanh(c) = 2 / (1 + 2^(-2 log2(e) c)) - 1
+__device__ __forceinline__ float tanh_bounded(float c)
+{
+    return fmaf(2.0f, inv_one_plus_ex2(c * (-2.0f * kLog2e)), -1.0f);
 }
 
 // One butterfly level: lanes that differ in `mask` exchange half of their
@@ -136,23 +149,26 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     const int valid_tw = min(TW, batch - tile * TW);
     const uint32_t step_bytes = static_cast<uint32_t>(kHidden * valid_tw * 4);
 
-    // weights: 4 gate rows of unit u, columns kc*16 .. kc*16+15, as pairs
+    // weights: 4 gate rows of unit u, columns kc*16 .. kc*16+15, as pairs,
+    // each row scaled by its gate's k_q (see the activations above)
     float2 r2[4][KLEN / 2];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
+        const float kq = q == 2 ? -2.0f * kLog2e : -kLog2e;
         const float2 *src =
             reinterpret_cast<const float2 *>(rp + (4 * u + q) * kHidden + kc * KLEN);
 #pragma unroll
         for (int i = 0; i < KLEN / 2; ++i)
-            r2[q][i] = src[i];
+            r2[q][i] = make_float2(src[i].x * kq, src[i].y * kq);
     }
 
     // The values this lane holds after each chunk's reduction: index
     // idx = w*4 + gate within the chunk (the same for every chunk).
     // Activations are branch-free across the lanes (which hold different
-    // gates): act = m * s(m * z) + a with (m, a) = (2, -1) for the cell
-    // candidate, i.e. tanh(z) = 2 s(2z) - 1, and (1, 0) for the gates.
-    float act_m[HV], act_a[HV], bias_v[HV];
+    // gates): act = m / (1 + 2^w) + a with (m, a) = (2, -1) for the cell
+    // candidate and (1, 0) for the gates; w = k_q z = k_q (G + bias) +
+    // (k_q R) h.
+    float act_m[HV], act_a[HV], bias_v[HV], gk[HV];
     int wv[HV];
     const float *gcol[HV];
 #pragma unroll
@@ -160,7 +176,8 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
         const int idx = V >= 8 ? kc * HV + v : (kc >> 1);
         const int q = idx & 3;
         wv[v] = idx >> 2;
-        bias_v[v] = bias[4 * u + q];
+        gk[v] = q == 2 ? -2.0f * kLog2e : -kLog2e;
+        bias_v[v] = bias[4 * u + q] * gk[v];
         act_m[v] = q == 2 ? 2.0f : 1.0f;
         act_a[v] = q == 2 ? -1.0f : 0.0f;
         gcol[v] = g + direction * kGates + 4 * u + q;
@@ -328,8 +345,8 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                 float act[HV];
 #pragma unroll
                 for (int v = 0; v < HV; ++v) {
-                    const float z = held[ch][v] + (gq[p][ch][v] + bias_v[v]);
-                    act[v] = fmaf(act_m[v], sigmoid_bounded(act_m[v] * z), act_a[v]);
+                    const float w = held[ch][v] + fmaf(gq[p][ch][v], gk[v], bias_v[v]);
+                    act[v] = fmaf(act_m[v], inv_one_plus_ex2(w), act_a[v]);
                 }
                 float gate[4];
 #pragma unroll
