@@ -91,11 +91,6 @@ __device__ __forceinline__ float inv_one_plus_ex2(float w)
 {
     return __fdividef(1.0f, 1.0f + ex2_approx(w));
 }
-// tanh(c) = 2 / (1 + 2^(-2 log2(e) c)) - 1
-__device__ __forceinline__ float tanh_bounded(float c)
-{
-    return fmaf(2.0f, inv_one_plus_ex2(c * (-2.0f * kLog2e)), -1.0f);
-}
 
 // One butterfly level: lanes that differ in `mask` exchange half of their
 // N values; each keeps the sum for the half its mask bit selects.
@@ -355,7 +350,10 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                     gate[q] = __shfl_sync(0xffffffffu, act[q % HV], src, 8);
                 }
                 c[ch] = gate[1] * c[ch] + gate[0] * gate[2];
-                h[ch] = gate[3] * tanh_bounded(c[ch]);
+                // h = o tanh(c) = o (2 r - 1) with r = 1 / (1 + 2^(-2 log2(e) c)):
+                // one fused multiply-add after r
+                const float r = inv_one_plus_ex2(c[ch] * (-2.0f * kLog2e));
+                h[ch] = fmaf(2.0f * gate[3], r, -gate[3]);
             }
 
             // 4. gather the warp's four units of window wl, push them (16
