@@ -435,15 +435,16 @@ int max_active_clusters(const Variant &v, int *out);
 // The default variant for a batch.  Candidates in order of preference, from
 // per-step timings of every variant with both directions running (GB300,
 // T = 589, us per step): up to 32 windows, narrow clusters of 8 (128 threads,
-// one window per cluster; 0.44 at one window, 0.48 at 8, 0.63 at 32); then
-// clusters of 4 with one window per group (0.63 at 32, 1.26 at 64; two CTAs
-// per SM), then 2, 4 and 8 chunks of two windows per lane (0.98 us at 64
-// windows, 1.70 at 128, 2.98 at 256).  The first whose clusters for both
-// directions fit the device at once wins; past that, the widest tile.
+// one window per cluster; 0.44 at one window, 0.48 at 8, 0.60 at 32); then
+// narrow clusters with two windows per group (0.73 at 48 windows); clusters
+// of 4 with one window per group (0.62 at 32); then 2, 4 and 8 chunks of two
+// windows per lane (0.98 us at 64 windows, 1.70 at 128, 2.98 at 256).  The
+// first whose clusters for both directions fit the device at once wins; past
+// that, the widest tile.
 const Variant *choose_variant(int batch)
 {
-    static const int order[][4] = {{8, 1, 1, 128}, {4, 1, 1, 0}, {4, 2, 2, 0}, {4, 2, 4, 0},
-                                   {4, 2, 8, 0}};
+    static const int order[][4] = {{8, 1, 1, 128}, {8, 2, 1, 128}, {4, 1, 1, 0},
+                                   {4, 2, 2, 0},   {4, 2, 4, 0},   {4, 2, 8, 0}};
     constexpr int N = sizeof(order) / sizeof(order[0]);
     constexpr int NARROW_MAX_BATCH = 32;
     static std::mutex mu;
