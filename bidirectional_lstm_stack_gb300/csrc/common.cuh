@@ -94,26 +94,13 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
                       const CUtensorMap &wlo_map, float *g, int rows, int kp, int math,
                       unsigned *fault, cudaStream_t stream);
 int projection_prepare(int device);
-
-// ---- dense heads of the segmentation model (projection.cu kernels) --------
-// W rows one CTA of a 2-CTA cluster loads: half of a 128-column LeakyReLU
-// tile, half of the 16-column classifier tile.
-constexpr int kHeadWBoxRows = 64;
-constexpr int kClassifierWBoxRows = 8;
 // Store map of a row-major fp32 matrix [rows][cols] written in 32 x 32
-// slices with the 128-byte swizzle.
+// slices with the 128-byte swizzle (the projection's G).
 int encode_store_map(CUtensorMap *map, float *base, long rows, int cols);
-// out[rows][128] = leaky(X . W^T + bias) with W^T given as TF32 hi/lo planes
-// [128][kp] (maps from encode_matrix_map with kHeadWBoxRows), 3xTF32.
-int launch_head_leaky(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                      const CUtensorMap &wlo_map, const CUtensorMap &out_map,
-                      const float *bias, float slope, int rows, int kp, unsigned *fault,
-                      cudaStream_t stream);
-// out[rows][7] = log_softmax(X . W^T + bias) with W^T planes [16][kp] (rows
-// 7..15 zero; maps with kClassifierWBoxRows), 3xTF32.
-int launch_head_classifier(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                           const CUtensorMap &wlo_map, const float *bias, float *out, int rows,
-                           int kp, unsigned *fault, cudaStream_t stream);
+
+// ---- dense heads of the segmentation model (heads.cu) ----------------------
+// W rows one CTA of a 2-CTA cluster loads: half of a 128-row W k-block.
+constexpr int kHeadWBoxRows = 64;
 
 // ---- recurrence (recurrence.cu) ------------------------------------------
 int launch_recurrence(const float *g, const float *rp, const float *bias,
@@ -301,6 +288,17 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
                  "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
+// The same with A in tensor memory: A's rows are tensor-memory lanes, its K
+// elements consecutive 32-bit columns starting at a_tmem.
+__device__ __forceinline__ void mma_tf32_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
 // Arrives once on `bar` when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
@@ -431,6 +429,69 @@ __device__ __forceinline__ void cluster_arrive_release()
 __device__ __forceinline__ void cluster_wait_acquire()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers (thread = lane).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+                 "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+                 "%32};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+                 "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
+                 "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+                 "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major operand, 64-byte
+// swizzle, 8-row groups 512 bytes apart.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t addr)
+{
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>(1) << 16) |           // leading offset (unused, swizzled K-major)
+           (static_cast<uint64_t>(512 >> 4) << 32) |    // stride offset: 8 rows x 64 B
+           (static_cast<uint64_t>(1) << 46) |           // descriptor version (tcgen05)
+           (static_cast<uint64_t>(4) << 61);            // 64-byte swizzle
+}
+
+// Instruction descriptor of kind::tf32, M = m, N = n: D fp32, A and B TF32,
+// both K-major.
+__host__ __device__ constexpr uint32_t tf32_idesc(int m, int n)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Splits four fp32 values into TF32 hi parts and TF32 remainders.
+__device__ __forceinline__ void split4(float4 v, float4 &hi, float4 &lo)
+{
+    hi.x = tf32_rna(v.x); lo.x = tf32_rna(v.x - hi.x);
+    hi.y = tf32_rna(v.y); lo.y = tf32_rna(v.y - hi.y);
+    hi.z = tf32_rna(v.z); lo.z = tf32_rna(v.z - hi.z);
+    hi.w = tf32_rna(v.w); lo.w = tf32_rna(v.w - hi.w);
+}
+
+// Waits without regard to any abort flag, up to limit_ns (used to drain
+// in-flight work before shared or tensor memory goes away).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity, unsigned *fault,
+                                                uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return;
+    const uint64_t start = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - start > limit_ns) {
+            atomicOr(fault, kFaultDrain);
+            return;
+        }
+    }
 }
 
 } // namespace ptx

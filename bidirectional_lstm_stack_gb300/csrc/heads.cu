@@ -6,17 +6,35 @@
 //     h1 = leaky(y W0 + b0),  h2 = leaky(h1 W1 + b1),
 //     out = log_softmax(h2 W2 + b2)  (7 classes).
 //
-// Each layer is one launch of the tensor-core GEMM of projection.cu (3xTF32,
-// persistent, 2-CTA clusters sharing each W tile by multicast) with its
-// epilogue fused: bias and LeakyReLU on the accumulator before the TMA store
-// of h1 / h2, or bias and log-softmax over the 7 class logits of a row,
-// written directly.  h1 and h2 are [rows][128] scratch the object owns.  The
-// weights are packed once at create: transposed to [n][k] (the K-major B
-// operand) and split into TF32 hi/lo planes; the classifier's 7 output rows
-// are padded to the 16-row MMA tile with zeros.
+// Design (sm_103a): one persistent kernel runs all three layers on 128-row
+// tiles, CTAs paired in clusters of two along the rows (each W k-block is
+// loaded half by each CTA and multicast into both):
+//  * warp 8 (TMA producer) streams, per tile, 16 k-blocks of y with W0 and
+//    then 8 k-blocks of W1 through a 6-stage ring;
+//  * warps 0-3 split the y blocks into TF32 hi (in place) and lo;
+//  * one thread of warp 9 issues tcgen05.mma kind::tf32 (M = 128, N = 128):
+//    linear0 as y_hi W0_hi + y_hi W0_lo + y_lo W0_hi into accumulator 1, then
+//    linear1 with its A operand, h1 split into TF32 hi/lo, read straight from
+//    tensor memory, into accumulator 2;
+//  * warps 4-7 (epilogue; warp 4+q owns rows 32q..32q+31, one row per lane)
+//    read accumulator 1, add b0, apply LeakyReLU, split h1 and write both
+//    halves back into tensor memory for linear1; then read accumulator 2, add
+//    b1, apply LeakyReLU and, still in registers, multiply h2 by the
+//    classifier's 128 x 7 weights (fp32 FMAs, weights broadcast from shared
+//    memory: a 16-column MMA would sit at its per-instruction floor), add b2
+//    and write the log-softmax of the 7 logits.
+// Tensor memory (512 columns): accumulator 1 [0, 128), h1 hi [128, 256),
+// h1 lo [256, 384), accumulator 2 [384, 512).  The MMA thread starts linear1
+// of a tile once the epilogue has written its h1 (which also means it has
+// read accumulator 1 and, before that, accumulator 2 of the previous tile);
+// the epilogue rewrites h1 only after linear1 of the previous tile completed.
+// Every wait is bounded in time; a wait that runs out sets a fault bit, every
+// role stops, and the CTA drains its loads and MMAs before freeing tensor
+// memory.
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include "common.cuh"
@@ -27,18 +45,399 @@ namespace {
 constexpr int kIn = LSTM_STACK_OUTPUT;      // 256
 constexpr int kMid = LSTM_HEADS_HIDDEN;     // 128
 constexpr int kCls = LSTM_HEADS_CLASSES;    // 7
-constexpr int kClsRows = 16;                // classifier MMA tile (N)
+constexpr int kClsPad = 8;                  // classifier weight row, padded
+
+constexpr int BM = 128;                     // rows per tile
+constexpr int BK = 16;                      // fp32 per K block (64 bytes)
+constexpr int K0_BLOCKS = kIn / BK;         // 16: linear0
+constexpr int K1_BLOCKS = kMid / BK;        // 8: linear1
+constexpr int BLOCKS_PER_TILE = K0_BLOCKS + K1_BLOCKS;
+constexpr int A_BYTES = BM * BK * 4;        // 8 KiB
+constexpr int W_BYTES = kMid * BK * 4;      // 8 KiB: one W k-block, 128 rows
+constexpr int CLUSTER = 2;
+constexpr uint16_t PAIR_MASK = (1u << CLUSTER) - 1;
+constexpr int W_HALF_BYTES = W_BYTES / CLUSTER;
+constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * W_BYTES;  // A hi, A lo, W hi, W lo
+constexpr int A_LO = A_BYTES;
+constexpr int W_HI = 2 * A_BYTES;
+constexpr int W_LO = W_HI + W_BYTES;
+constexpr int STAGES = 6;
+constexpr int RING_BYTES = STAGES * STAGE_BYTES;  // 192 KiB
+// parameters in shared memory: b0, b1, W2 (rows padded to 8), b2 (padded)
+constexpr int P_B0 = 0;
+constexpr int P_B1 = P_B0 + kMid;
+constexpr int P_W2 = P_B1 + kMid;
+constexpr int P_B2 = P_W2 + kMid * kClsPad;
+constexpr int P_FLOATS = P_B2 + kClsPad;
+constexpr size_t SMEM_BYTES = RING_BYTES + P_FLOATS * 4 + 256 + 1024;
+constexpr uint32_t ACC1 = 0, H1HI = 128, H1LO = 256, ACC2 = 384, TMEM_COLS = 512;
+constexpr uint32_t IDESC = ptx::tf32_idesc(BM, kMid);
+constexpr int CONVERTERS = 128;
+constexpr int EPILOGUE = 128;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int THREADS = 320;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+static_assert(kMid / CLUSTER == kHeadWBoxRows, "W box rows");
+static_assert(RING_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "stage alignment");
+
+__global__ void __launch_bounds__(THREADS, 1)
+heads_kernel(const __grid_constant__ CUtensorMap y_map,
+             const __grid_constant__ CUtensorMap w0hi_map,
+             const __grid_constant__ CUtensorMap w0lo_map,
+             const __grid_constant__ CUtensorMap w1hi_map,
+             const __grid_constant__ CUtensorMap w1lo_map, const float *__restrict__ params,
+             float slope, float *__restrict__ logp, int rows, int pairs, unsigned *fault)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *par = reinterpret_cast<float *>(smem + RING_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(par + P_FLOATS);
+    uint64_t *conv = full + STAGES;
+    uint64_t *empty = conv + STAGES;
+    uint64_t *acc1_full = empty + STAGES;
+    uint64_t *acc2_full = acc1_full + 1;
+    uint64_t *ep1_done = acc2_full + 1;   // h1 in tensor memory (and accumulator 1 read)
+    uint64_t *mma_done = ep1_done + 1;    // every MMA issued complete (teardown)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    for (int i = threadIdx.x; i < P_FLOATS; i += THREADS)
+        par[i] = params[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&conv[s], CONVERTERS);
+            ptx::mbar_init(&empty[s], CLUSTER);  // both CTAs' MMAs release a stage
+        }
+        ptx::mbar_init(acc1_full, 1);
+        ptx::mbar_init(acc2_full, 1);
+        ptx::mbar_init(ep1_done, EPILOGUE);
+        ptx::mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == PRODUCER_WARP && lane == 0) {
+        ptx::prefetch_tensormap(&y_map);
+        ptx::prefetch_tensormap(&w0hi_map);
+        ptx::prefetch_tensormap(&w0lo_map);
+        ptx::prefetch_tensormap(&w1hi_map);
+        ptx::prefetch_tensormap(&w1lo_map);
+    }
+    if (warp == MMA_WARP) {
+        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    // the peer's barriers are initialised before any multicast reaches them
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int rank = static_cast<int>(ptx::cluster_ctarank());
+    const int first = static_cast<int>(ptx::cluster_id_x());
+    const int stride = static_cast<int>(ptx::cluster_nid_x());
+    long issued = 0;  // producer: stages whose loads were issued
+
+    if (warp == PRODUCER_WARP) {
+        if (lane == 0) {
+            long kbi = 0;
+            for (int t = first; t < pairs && !*abort_flag; t += stride) {
+                const int m0 = (t * CLUSTER + rank) * BM;
+                bool ok = true;
+                for (int kb = 0; kb < BLOCKS_PER_TILE; ++kb, ++kbi) {
+                    const int s = static_cast<int>(kbi % STAGES);
+                    const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
+                    if (n > 0 && !ptx::mbar_wait_bounded(&empty[s], (n - 1) & 1, abort_flag, fault,
+                                                         kFaultProducer, WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = smem + s * STAGE_BYTES;
+                    const int wrow = rank * (kMid / CLUSTER);  // this CTA's half of W
+                    if (kb < K0_BLOCKS) {
+                        ptx::mbar_arrive_expect_tx(&full[s], A_BYTES + 2 * W_BYTES);
+                        ptx::tma_load_2d(st, &y_map, &full[s], kb * BK, m0);
+                        ptx::tma_load_2d_multicast(st + W_HI + rank * W_HALF_BYTES, &w0hi_map,
+                                                   &full[s], kb * BK, wrow, PAIR_MASK);
+                        ptx::tma_load_2d_multicast(st + W_LO + rank * W_HALF_BYTES, &w0lo_map,
+                                                   &full[s], kb * BK, wrow, PAIR_MASK);
+                    } else {
+                        const int k = (kb - K0_BLOCKS) * BK;
+                        ptx::mbar_arrive_expect_tx(&full[s], 2 * W_BYTES);
+                        ptx::tma_load_2d_multicast(st + W_HI + rank * W_HALF_BYTES, &w1hi_map,
+                                                   &full[s], k, wrow, PAIR_MASK);
+                        ptx::tma_load_2d_multicast(st + W_LO + rank * W_HALF_BYTES, &w1lo_map,
+                                                   &full[s], k, wrow, PAIR_MASK);
+                    }
+                    issued = kbi + 1;
+                }
+                if (!ok)
+                    break;
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            long kbi = 0;
+            int ti = 0;
+            for (int t = first; t < pairs && !*abort_flag; t += stride, ++ti) {
+                bool ok = true;
+                // linear0 into accumulator 1 (the epilogue read it before it
+                // wrote the previous tile's h1, which linear1 waited for)
+                for (int kb = 0; kb < K0_BLOCKS && ok; ++kb, ++kbi) {
+                    const int s = static_cast<int>(kbi % STAGES);
+                    const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
+                    if (!ptx::mbar_wait_bounded(&conv[s], n & 1, abort_flag, fault, kFaultMma,
+                                                WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_hi = ptx::smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t a_lo = a_hi + A_LO;
+                    const uint32_t b_hi = a_hi + W_HI;
+                    const uint32_t b_lo = a_hi + W_LO;
+#pragma unroll
+                    for (int j = 0; j < BK / 8; ++j) {
+                        const uint32_t off = j * 32;  // 8 TF32 along K
+                        ptx::mma_tf32(tmem + ACC1, ptx::sw64_desc(a_hi + off),
+                                      ptx::sw64_desc(b_hi + off), IDESC, (kb | j) != 0);
+                        ptx::mma_tf32(tmem + ACC1, ptx::sw64_desc(a_hi + off),
+                                      ptx::sw64_desc(b_lo + off), IDESC, 1);
+                        ptx::mma_tf32(tmem + ACC1, ptx::sw64_desc(a_lo + off),
+                                      ptx::sw64_desc(b_hi + off), IDESC, 1);
+                    }
+                    ptx::mma_commit_multicast(&empty[s], PAIR_MASK);
+                }
+                ptx::mma_commit(acc1_full);  // also when stopping: frees the epilogue
+                if (!ok)
+                    break;
+                // linear1 into accumulator 2 once h1 of this tile is in place
+                if (!ptx::mbar_wait_bounded(ep1_done, ti & 1, abort_flag, fault, kFaultMma,
+                                            WAIT_LIMIT_NS))
+                    break;
+                ptx::tc_fence_after();
+                for (int kb = 0; kb < K1_BLOCKS && ok; ++kb, ++kbi) {
+                    const int s = static_cast<int>(kbi % STAGES);
+                    const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
+                    if (!ptx::mbar_wait_bounded(&conv[s], n & 1, abort_flag, fault, kFaultMma,
+                                                WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t b_hi = ptx::smem_u32(smem + s * STAGE_BYTES) + W_HI;
+                    const uint32_t b_lo = b_hi + W_BYTES;
+#pragma unroll
+                    for (int j = 0; j < BK / 8; ++j) {
+                        const uint32_t off = j * 32;
+                        const uint32_t kcol = static_cast<uint32_t>(kb * BK + j * 8);
+                        ptx::mma_tf32_tmem_a(tmem + ACC2, tmem + H1HI + kcol,
+                                             ptx::sw64_desc(b_hi + off), IDESC, (kb | j) != 0);
+                        ptx::mma_tf32_tmem_a(tmem + ACC2, tmem + H1HI + kcol,
+                                             ptx::sw64_desc(b_lo + off), IDESC, 1);
+                        ptx::mma_tf32_tmem_a(tmem + ACC2, tmem + H1LO + kcol,
+                                             ptx::sw64_desc(b_hi + off), IDESC, 1);
+                    }
+                    ptx::mma_commit_multicast(&empty[s], PAIR_MASK);
+                }
+                ptx::mma_commit(acc2_full);
+                if (!ok)
+                    break;
+            }
+            // every MMA issued has completed before tensor memory is freed
+            ptx::mma_commit(mma_done);
+            ptx::mbar_wait_drain(mma_done, 0, fault, WAIT_LIMIT_NS);
+        }
+    } else if (warp < 4) {
+        // converters: split the y blocks into TF32 hi (in place) and lo; the
+        // W1 stages only pass through
+        const int tid = threadIdx.x;
+        long kbi = 0;
+        for (int t = first; t < pairs && !*abort_flag; t += stride) {
+            bool ok = true;
+            for (int kb = 0; kb < BLOCKS_PER_TILE; ++kb, ++kbi) {
+                const int s = static_cast<int>(kbi % STAGES);
+                const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
+                if (!ptx::mbar_wait_bounded(&full[s], n & 1, abort_flag, fault, kFaultConverter,
+                                            WAIT_LIMIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                if (kb < K0_BLOCKS) {
+                    float4 *a = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES);
+                    float4 *alo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + A_LO);
+#pragma unroll
+                    for (int i = 0; i < A_BYTES / 16 / CONVERTERS; ++i) {
+                        const int idx = tid + i * CONVERTERS;
+                        float4 hi, lo;
+                        ptx::split4(a[idx], hi, lo);
+                        a[idx] = hi;
+                        alo[idx] = lo;
+                    }
+                    ptx::fence_proxy_async_smem();
+                }
+                ptx::mbar_arrive(&conv[s]);
+            }
+            if (!ok)
+                break;
+        }
+    } else if (warp >= 4) {
+        // epilogue: warp 4+q owns tensor-memory lanes (tile rows) 32q..32q+31
+        const int q = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        int ti = 0;
+        for (int t = first; t < pairs; t += stride, ++ti) {
+            const long row = static_cast<long>(t * CLUSTER + rank) * BM + q * 32 + lane;
+            bool got = ptx::mbar_wait_bounded(acc1_full, ti & 1, abort_flag, fault, kFaultEpilogue,
+                                              WAIT_LIMIT_NS);
+            // tcgen05.ld / st are warp-collective: continue only if every lane may
+            if (!__all_sync(0xffffffffu, got) || *abort_flag)
+                break;
+            ptx::tc_fence_after();
+            // h1 = leaky(acc1 + b0), written back as TF32 hi/lo columns
+#pragma unroll 1
+            for (int c = 0; c < kMid / 32; ++c) {
+                uint32_t r[32], hi[32], lo[32];
+                ptx::tmem_ld_32x32b_x32(tmem + lane_base + ACC1 + c * 32, r);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float v = __uint_as_float(r[j]) + par[P_B0 + c * 32 + j];
+                    v = v >= 0.0f ? v : slope * v;
+                    const float h = ptx::tf32_rna(v);
+                    hi[j] = __float_as_uint(h);
+                    lo[j] = __float_as_uint(ptx::tf32_rna(v - h));
+                }
+                ptx::tmem_st_32x32b_x32(tmem + lane_base + H1HI + c * 32, hi);
+                ptx::tmem_st_32x32b_x32(tmem + lane_base + H1LO + c * 32, lo);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ep1_done);
+            got = ptx::mbar_wait_bounded(acc2_full, ti & 1, abort_flag, fault, kFaultEpilogue,
+                                         WAIT_LIMIT_NS);
+            if (!__all_sync(0xffffffffu, got) || *abort_flag)
+                break;
+            ptx::tc_fence_after();
+            // h2 = leaky(acc2 + b1) in registers, z = h2 W2 + b2 (fp32 FMAs)
+            float z[kClsPad];
+#pragma unroll
+            for (int j = 0; j < kClsPad; ++j)
+                z[j] = 0.0f;
+#pragma unroll 1
+            for (int c = 0; c < kMid / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(tmem + lane_base + ACC2 + c * 32, r);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    float v = __uint_as_float(r[k]) + par[P_B1 + c * 32 + k];
+                    v = v >= 0.0f ? v : slope * v;
+                    const float4 *w = reinterpret_cast<const float4 *>(
+                        par + P_W2 + (c * 32 + k) * kClsPad);
+                    const float4 w0 = w[0], w1 = w[1];
+                    z[0] = fmaf(v, w0.x, z[0]);
+                    z[1] = fmaf(v, w0.y, z[1]);
+                    z[2] = fmaf(v, w0.z, z[2]);
+                    z[3] = fmaf(v, w0.w, z[3]);
+                    z[4] = fmaf(v, w1.x, z[4]);
+                    z[5] = fmaf(v, w1.y, z[5]);
+                    z[6] = fmaf(v, w1.z, z[6]);
+                }
+            }
+            ptx::tc_fence_before();
+            if (row < rows) {
+                float zmax = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kCls; ++j) {
+                    z[j] += par[P_B2 + j];
+                    zmax = fmaxf(zmax, z[j]);
+                }
+                float sum = 0.0f;
+#pragma unroll
+                for (int j = 0; j < kCls; ++j)
+                    sum += expf(z[j] - zmax);
+                const float lse = zmax + logf(sum);
+#pragma unroll
+                for (int j = 0; j < kCls; ++j)
+                    logp[row * kCls + j] = z[j] - lse;
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == PRODUCER_WARP && lane == 0) {
+        // every issued TMA load has landed before the shared memory goes away
+        for (long kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
+            ptx::mbar_wait_drain(&full[kb % STAGES], static_cast<uint32_t>(kb / STAGES) & 1, fault,
+                                 WAIT_LIMIT_NS);
+    }
+    if (warp == MMA_WARP) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+    // neither CTA leaves while the other may still multicast into it or
+    // release its stages
+    __syncwarp();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+}
+
+int g_max_clusters[64] = {};
+
+// Per-device set-up, with that device current: the kernel's shared-memory
+// attribute and the number of its clusters that run at once.
+int heads_prepare(int device)
+{
+    static std::mutex mu;
+    static bool done[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[device])
+        return LSTM_OK;
+    int st = cuda_status(cudaFuncSetAttribute(heads_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(SMEM_BYTES)),
+                         "heads shared-memory attribute");
+    if (st != LSTM_OK)
+        return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CLUSTER);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    st = cuda_status(cudaOccupancyMaxActiveClusters(&n, heads_kernel, &cfg),
+                     "heads max active clusters");
+    if (st != LSTM_OK)
+        return st;
+    g_max_clusters[device] = n > 0 ? n : 74;
+    done[device] = true;
+    return LSTM_OK;
+}
 }  // namespace
 
 struct lstm_heads {
     int device = 0;
     long max_rows = 0;
     float slope = 0.01f;
-    float *weights = nullptr;  // one allocation: packed planes and biases
-    float *w_hi[3] = {}, *w_lo[3] = {}, *bias[3] = {};
-    float *h1 = nullptr, *h2 = nullptr;  // [max_rows][128]
-    CUtensorMap map_whi[3], map_wlo[3];
-    CUtensorMap load_h1, load_h2, store_h1, store_h2;
+    float *weights = nullptr;  // one allocation: packed planes and the parameters
+    float *w0_hi = nullptr, *w0_lo = nullptr, *w1_hi = nullptr, *w1_lo = nullptr;
+    float *params = nullptr;   // b0, b1, W2 (rows padded to 8), b2 (padded)
+    CUtensorMap map_w0hi, map_w0lo, map_w1hi, map_w1lo;
     CUtensorMap map_y;
     const float *map_y_base = nullptr;
     long map_y_rows = -1;
@@ -51,8 +450,6 @@ extern "C" void lstm_heads_destroy(lstm_heads *h)
         return;
     DeviceGuard guard(h->device);
     cudaFree(h->weights);
-    cudaFree(h->h1);
-    cudaFree(h->h2);
     delete h;
 }
 
@@ -74,6 +471,8 @@ extern "C" int lstm_heads_create(const float *w0, const float *b0, const float *
     DeviceGuard guard(device);
     if (!guard.ok)
         return fail(LSTM_E_CUDA, "cannot make device %d current", device);
+    if ((st = heads_prepare(device)) != LSTM_OK)
+        return st;
     lstm_heads *h = new (std::nothrow) lstm_heads();
     if (!h)
         return fail(LSTM_E_ALLOC, "lstm_heads_create: host allocation failed");
@@ -86,69 +485,55 @@ extern "C" int lstm_heads_create(const float *w0, const float *b0, const float *
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
     }
 
-    // layer l: source W [K][N] row-major ([k, n]), packed [Npad][K]
-    const float *src_w[3] = {w0, w1, w2};
-    const float *src_b[3] = {b0, b1, b2};
-    const int K[3] = {kIn, kMid, kMid};
-    const int N[3] = {kMid, kMid, kCls};
-    const int Npad[3] = {kMid, kMid, kClsRows};
-    long off_hi[3], off_lo[3], off_b[3], total = 0;
-    for (int l = 0; l < 3; ++l) {
-        off_hi[l] = total;  total += static_cast<long>(Npad[l]) * K[l];
-        off_lo[l] = total;  total += static_cast<long>(Npad[l]) * K[l];
-        off_b[l] = total;   total += Npad[l];
-        total = (total + 63) / 64 * 64;  // every plane 256-byte aligned
-    }
+    // W0 [256][128] and W1 [128][128] (row-major [k, n]) become K-major
+    // [n][k] TF32 hi/lo planes; W2 [128][7] stays fp32, rows padded to 8
+    const long n0 = static_cast<long>(kMid) * kIn, n1 = static_cast<long>(kMid) * kMid;
+    const long o_w0hi = 0, o_w0lo = o_w0hi + n0, o_w1hi = o_w0lo + n0, o_w1lo = o_w1hi + n1;
+    const long o_par = o_w1lo + n1;
+    const long total = (o_par + P_FLOATS + 63) / 64 * 64;
     float *host = static_cast<float *>(calloc(total, sizeof(float)));
     if (!host) {
         lstm_heads_destroy(h);
         return fail(LSTM_E_ALLOC, "lstm_heads_create: host staging allocation failed");
     }
-    for (int l = 0; l < 3; ++l) {
-        for (int n = 0; n < N[l]; ++n) {
-            for (int k = 0; k < K[l]; ++k) {
-                const float v = src_w[l][static_cast<long>(k) * N[l] + n];
-                const float hi = tf32_round(v);
-                host[off_hi[l] + static_cast<long>(n) * K[l] + k] = hi;
-                host[off_lo[l] + static_cast<long>(n) * K[l] + k] = tf32_round(v - hi);
-            }
-            host[off_b[l] + n] = src_b[l][n];
-        }
+    auto split = [](float v, float *hi, float *lo) {
+        *hi = tf32_round(v);
+        *lo = tf32_round(v - *hi);
+    };
+    for (int n = 0; n < kMid; ++n) {
+        for (int k = 0; k < kIn; ++k)
+            split(w0[static_cast<long>(k) * kMid + n], &host[o_w0hi + n * kIn + k],
+                  &host[o_w0lo + n * kIn + k]);
+        for (int k = 0; k < kMid; ++k)
+            split(w1[static_cast<long>(k) * kMid + n], &host[o_w1hi + n * kMid + k],
+                  &host[o_w1lo + n * kMid + k]);
+        host[o_par + P_B0 + n] = b0[n];
+        host[o_par + P_B1 + n] = b1[n];
     }
+    for (int k = 0; k < kMid; ++k)
+        for (int j = 0; j < kCls; ++j)
+            host[o_par + P_W2 + k * kClsPad + j] = w2[k * kCls + j];
+    for (int j = 0; j < kCls; ++j)
+        host[o_par + P_B2 + j] = b2[j];
     cudaError_t e = device_alloc(reinterpret_cast<void **>(&h->weights), total * sizeof(float));
     if (e == cudaSuccess)
         e = cudaMemcpy(h->weights, host, total * sizeof(float), cudaMemcpyHostToDevice);
     free(host);
-    if (e == cudaSuccess)
-        e = device_alloc(reinterpret_cast<void **>(&h->h1), max_rows * kMid * sizeof(float));
-    if (e == cudaSuccess)
-        e = device_alloc(reinterpret_cast<void **>(&h->h2), max_rows * kMid * sizeof(float));
     if (e != cudaSuccess) {
         cudaGetLastError();
         lstm_heads_destroy(h);
         return fail(LSTM_E_ALLOC, "lstm_heads_create: device allocation: %s",
                     cudaGetErrorString(e));
     }
-    const int box_rows[3] = {kHeadWBoxRows, kHeadWBoxRows, kClassifierWBoxRows};
-    for (int l = 0; l < 3 && st == LSTM_OK; ++l) {
-        h->w_hi[l] = h->weights + off_hi[l];
-        h->w_lo[l] = h->weights + off_lo[l];
-        h->bias[l] = h->weights + off_b[l];
-        st = encode_matrix_map(&h->map_whi[l], h->w_hi[l], Npad[l], K[l], box_rows[l]);
-        if (st == LSTM_OK)
-            st = encode_matrix_map(&h->map_wlo[l], h->w_lo[l], Npad[l], K[l], box_rows[l]);
-    }
-    // the scratch maps cover max_rows: rows past a call's count are scratch
-    // too, and the classifier writes only the call's rows
-    if (st == LSTM_OK)
-        st = encode_matrix_map(&h->load_h1, h->h1, max_rows, kMid, kProjectionBoxRows);
-    if (st == LSTM_OK)
-        st = encode_matrix_map(&h->load_h2, h->h2, max_rows, kMid, kProjectionBoxRows);
-    if (st == LSTM_OK)
-        st = encode_store_map(&h->store_h1, h->h1, max_rows, kMid);
-    if (st == LSTM_OK)
-        st = encode_store_map(&h->store_h2, h->h2, max_rows, kMid);
-    if (st != LSTM_OK) {
+    h->w0_hi = h->weights + o_w0hi;
+    h->w0_lo = h->weights + o_w0lo;
+    h->w1_hi = h->weights + o_w1hi;
+    h->w1_lo = h->weights + o_w1lo;
+    h->params = h->weights + o_par;
+    if ((st = encode_matrix_map(&h->map_w0hi, h->w0_hi, kMid, kIn, kHeadWBoxRows)) ||
+        (st = encode_matrix_map(&h->map_w0lo, h->w0_lo, kMid, kIn, kHeadWBoxRows)) ||
+        (st = encode_matrix_map(&h->map_w1hi, h->w1_hi, kMid, kMid, kHeadWBoxRows)) ||
+        (st = encode_matrix_map(&h->map_w1lo, h->w1_lo, kMid, kMid, kHeadWBoxRows))) {
         lstm_heads_destroy(h);
         return st;
     }
@@ -190,13 +575,28 @@ extern "C" int lstm_heads_forward(lstm_heads *h, const float *y, size_t y_len, f
         h->map_y_base = y;
         h->map_y_rows = rows;
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((st = launch_head_leaky(h->map_y, h->map_whi[0], h->map_wlo[0], h->store_h1, h->bias[0],
-                                h->slope, rows, kIn, h->fault, s)))
+    const long mtiles = (static_cast<long>(rows) + BM - 1) / BM;
+    const long pairs = (mtiles + CLUSTER - 1) / CLUSTER;
+    const int fit = g_max_clusters[h->device] > 0 ? g_max_clusters[h->device] : 74;
+    const long clusters = pairs < fit ? pairs : fit;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((st = check_launch_injection("heads launch")))
         return st;
-    if ((st = launch_head_leaky(h->load_h1, h->map_whi[1], h->map_wlo[1], h->store_h2,
-                                h->bias[1], h->slope, rows, kMid, h->fault, s)))
-        return st;
-    return launch_head_classifier(h->load_h2, h->map_whi[2], h->map_wlo[2], h->bias[2], logp, rows,
-                                  kMid, h->fault, s);
+    const int npairs = static_cast<int>(pairs);
+    return cuda_status(cudaLaunchKernelEx(&cfg, heads_kernel, h->map_y, h->map_w0hi, h->map_w0lo,
+                                          h->map_w1hi, h->map_w1lo,
+                                          static_cast<const float *>(h->params), h->slope, logp,
+                                          rows, npairs, h->fault),
+                       "heads launch");
 }

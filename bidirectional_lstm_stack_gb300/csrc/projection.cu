@@ -61,18 +61,11 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 constexpr int CLUSTER = 2;                          // CTAs sharing a W tile
 constexpr uint16_t PAIR_MASK = (1u << CLUSTER) - 1;
 
-// What an instantiation writes: the LSTM gate pre-activations G (1024
-// columns in tiles of 256, no bias), or one dense head layer of the
-// segmentation model: bias + LeakyReLU (a 128-column tile), or bias +
-// log-softmax over the 7 classes (a 16-column tile; W rows 7..15 are zero).
-enum Epilogue { kEpiGates = 0, kEpiLeaky = 1, kEpiLogSoftmax = 2 };
-constexpr int kClasses = 7;
-
-template <int BN_, bool SINGLE_, int EPI_>
+// One instantiation: tiles of BN gate columns, 3xTF32 or single products.
+template <int BN_, bool SINGLE_>
 struct Shape {
     static constexpr int BN = BN_;  // MMA N: output columns per tile
     static constexpr bool SINGLE = SINGLE_;
-    static constexpr int EPI = EPI_;
     static constexpr int B_BYTES = BN * BK * 4;
     // 3xTF32 keeps A hi, A lo, B hi, B lo per stage; the single-product
     // mode only A hi and B hi, so the same ring holds twice the K blocks
@@ -86,56 +79,23 @@ struct Shape {
     static constexpr int B_HALF_BYTES = B_BYTES / CLUSTER;      // W rows one CTA loads
     static constexpr uint32_t ACC_COLS = BN;                     // per accumulator
     static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
-    static constexpr int TILES_N = EPI == kEpiGates ? kGateColumns / BN : 1;
-    // instruction descriptor, kind::tf32: D fp32, A and B TF32, both K-major
-    static constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
-                                      (static_cast<uint32_t>(BN >> 3) << 17) |
-                                      (static_cast<uint32_t>(BM >> 4) << 24);
+    static constexpr int TILES_N = kGateColumns / BN;
+    static constexpr uint32_t IDESC = ptx::tf32_idesc(BM, BN);
     static_assert(STAGE_BYTES % 1024 == 0 && BN % 16 == 0 && BN <= 256 && STAGES >= 4,
                   "tile shape");
-    static_assert(EPI != kEpiLogSoftmax || BN == 16, "the classifier tile is 16 columns");
 };
-using GatesShape = Shape<256, false, kEpiGates>;
-using GatesTf32Shape = Shape<256, true, kEpiGates>;
-using LeakyShape = Shape<128, false, kEpiLeaky>;
-using ClassifierShape = Shape<16, false, kEpiLogSoftmax>;
+using GatesShape = Shape<256, false>;
+using GatesTf32Shape = Shape<256, true>;
 static_assert(GatesShape::BN / CLUSTER == kProjectionWBoxRows && BM == kProjectionBoxRows,
               "TMA boxes");
-static_assert(LeakyShape::BN / CLUSTER == kHeadWBoxRows &&
-                  ClassifierShape::BN / CLUSTER == kClassifierWBoxRows,
-              "head TMA boxes");
 
-// tcgen05 shared-memory matrix descriptor: K-major operand, 64-byte
-// swizzle, 8-row groups 512 bytes apart.
-__device__ __forceinline__ uint64_t sw64_desc(uint32_t addr)
-{
-    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
-           (static_cast<uint64_t>(1) << 16) |           // leading offset (unused, swizzled K-major)
-           (static_cast<uint64_t>(512 >> 4) << 32) |    // stride offset: 8 rows x 64 B
-           (static_cast<uint64_t>(1) << 46) |           // descriptor version (tcgen05)
-           (static_cast<uint64_t>(4) << 61);            // 64-byte swizzle
-}
-
-__device__ __forceinline__ void split4(float4 v, float4 &hi, float4 &lo)
-{
-    hi.x = ptx::tf32_rna(v.x); lo.x = ptx::tf32_rna(v.x - hi.x);
-    hi.y = ptx::tf32_rna(v.y); lo.y = ptx::tf32_rna(v.y - hi.y);
-    hi.z = ptx::tf32_rna(v.z); lo.z = ptx::tf32_rna(v.z - hi.z);
-    hi.w = ptx::tf32_rna(v.w); lo.w = ptx::tf32_rna(v.w - hi.w);
-}
+using ptx::sw64_desc;
+using ptx::split4;
 
 // Waits without regard to the abort flag (used to drain in-flight work).
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, unsigned *fault)
 {
-    if (ptx::mbar_try_wait(bar, parity))
-        return;
-    const uint64_t start = ptx::globaltimer();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (ptx::globaltimer() - start > WAIT_LIMIT_NS) {
-            atomicOr(fault, kFaultDrain);
-            return;
-        }
-    }
+    ptx::mbar_wait_drain(bar, parity, fault, WAIT_LIMIT_NS);
 }
 
 template <class S>
@@ -143,8 +103,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 projection_kernel(const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap whi_map,
                   const __grid_constant__ CUtensorMap wlo_map,
-                  const __grid_constant__ CUtensorMap out_map, float *__restrict__ out,
-                  const float *__restrict__ bias, float slope, int rows, int kblocks, int pairs,
+                  const __grid_constant__ CUtensorMap out_map, int rows, int kblocks, int pairs,
                   unsigned *fault)
 {
     using RG = S;
@@ -339,79 +298,45 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             const int m0 = ((t / TILES_N) * CLUSTER + rank) * BM + q * 32;  // this warp's rows
             const int n0 = (t % TILES_N) * BN;
             const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(a) * ACC_COLS;
-            if constexpr (S::EPI == kEpiLogSoftmax) {
-                // lane = row: the 7 class logits, log-softmax, 7 floats out
-                uint32_t r[16];
-                ptx::tmem_ld_32x32b_x16(acc, r);
-                ptx::tmem_ld_wait();
-                const long m = static_cast<long>(m0) + lane;
-                if (m < rows) {
-                    float z[kClasses];
-                    float zmax = -INFINITY;
-#pragma unroll
-                    for (int j = 0; j < kClasses; ++j) {
-                        z[j] = __uint_as_float(r[j]) + __ldg(bias + j);
-                        zmax = fmaxf(zmax, z[j]);
-                    }
-                    float sum = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < kClasses; ++j)
-                        sum += expf(z[j] - zmax);
-                    const float lse = zmax + logf(sum);
-#pragma unroll
-                    for (int j = 0; j < kClasses; ++j)
-                        out[m * kClasses + j] = z[j] - lse;
-                }
-            } else {
-                // Pace the stores: slice c of this tile goes out once the
-                // next tile's mainloop has issued c/slices of its K blocks,
-                // so the output streams to memory under the next tile's
-                // compute instead of every CTA writing its whole tile at once
-                // and stalling the loads.
-                constexpr int NSLICE = BN / OUT_COLS;
-                const bool paced = t + stride < pairs;
-                const long next_kb = static_cast<long>(ti + 1) * kblocks;
+            // Pace the stores: slice c of this tile goes out once the next
+            // tile's mainloop has issued c/NSLICE of its K blocks, so G
+            // streams to memory under the next tile's compute instead of
+            // every CTA writing its whole tile at once and stalling the loads.
+            constexpr int NSLICE = BN / OUT_COLS;
+            const bool paced = t + stride < pairs;
+            const long next_kb = static_cast<long>(ti + 1) * kblocks;
 #pragma unroll 1
-                for (int c = 0; c < NSLICE; ++c, ++slices) {
-                    if (paced) {
-                        const long want = next_kb + (static_cast<long>(c) * kblocks) / NSLICE;
-                        if (*progress < want && !*abort_flag) {
-                            const uint64_t start = ptx::globaltimer();
-                            while (*progress < want && !*abort_flag &&
-                                   ptx::globaltimer() - start < WAIT_LIMIT_NS)
-                                __nanosleep(64);
-                        }
+            for (int c = 0; c < NSLICE; ++c, ++slices) {
+                if (paced) {
+                    const long want = next_kb + (static_cast<long>(c) * kblocks) / NSLICE;
+                    if (*progress < want && !*abort_flag) {
+                        const uint64_t start = ptx::globaltimer();
+                        while (*progress < want && !*abort_flag &&
+                               ptx::globaltimer() - start < WAIT_LIMIT_NS)
+                            __nanosleep(64);
                     }
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(acc + c * OUT_COLS, r);
-                    ptx::tmem_ld_wait();
-                    float v[32];
+                }
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(acc + c * OUT_COLS, r);
+                ptx::tmem_ld_wait();
+                // the store that last used this buffer (two slices ago) has read it
+                uint8_t *buf = stage_out + (slices & 1) * OUT_BYTES;
+                if (lane == 0)
+                    ptx::bulk_wait_group_read<1>();
+                __syncwarp();
+                // lane = row; 16-byte chunk j of the row goes to chunk j ^ (row % 8)
+                float4 *row = reinterpret_cast<float4 *>(buf + lane * (OUT_COLS * 4));
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        v[j] = __uint_as_float(r[j]);
-                        if constexpr (S::EPI == kEpiLeaky) {
-                            v[j] += __ldg(bias + n0 + c * OUT_COLS + j);
-                            v[j] = v[j] >= 0.0f ? v[j] : slope * v[j];
-                        }
-                    }
-                    // the store that last used this buffer (two slices ago) has read it
-                    uint8_t *buf = stage_out + (slices & 1) * OUT_BYTES;
-                    if (lane == 0)
-                        ptx::bulk_wait_group_read<1>();
-                    __syncwarp();
-                    // lane = row; 16-byte chunk j of the row goes to chunk j ^ (row % 8)
-                    float4 *row = reinterpret_cast<float4 *>(buf + lane * (OUT_COLS * 4));
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        row[j ^ (lane & 7)] =
-                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (m0 < rows)
-                            ptx::tma_store_2d(&out_map, buf, n0 + c * OUT_COLS, m0);
-                        ptx::bulk_commit_group();
-                    }
+                for (int j = 0; j < 8; ++j)
+                    row[j ^ (lane & 7)] =
+                        make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (m0 < rows)
+                        ptx::tma_store_2d(&out_map, buf, n0 + c * OUT_COLS, m0);
+                    ptx::bulk_commit_group();
                 }
             }
             ptx::tc_fence_before();
@@ -507,18 +432,15 @@ namespace {
 const void *const kKernels[] = {
     reinterpret_cast<const void *>(&projection_kernel<GatesShape>),
     reinterpret_cast<const void *>(&projection_kernel<GatesTf32Shape>),
-    reinterpret_cast<const void *>(&projection_kernel<LeakyShape>),
-    reinterpret_cast<const void *>(&projection_kernel<ClassifierShape>),
 };
 
 // Persistent grid over the row tiles (pairs of 128-row tiles, one per CTA of
 // a 2-CTA cluster) times S::TILES_N column tiles, no larger than what runs at
-// once.  out_map is only read by the TMA-store epilogues.
+// once.
 template <class S>
 int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                 const CUtensorMap &wlo_map, const CUtensorMap &out_map, float *out,
-                 const float *bias, float slope, int rows, int kp, unsigned *fault,
-                 cudaStream_t stream)
+                 const CUtensorMap &wlo_map, const CUtensorMap &out_map, int rows, int kp,
+                 unsigned *fault, cudaStream_t stream)
 {
     if (rows <= 0 || kp <= 0 || kp % 32 != 0)
         return fail(LSTM_E_INVALID, "tensor-core GEMM: rows %d, kp %d", rows, kp);
@@ -550,7 +472,7 @@ int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     if ((st = check_launch_injection("tensor-core GEMM launch")))
         return st;
     return cuda_status(cudaLaunchKernelEx(&cfg, projection_kernel<S>, x_map, whi_map, wlo_map,
-                                          out_map, out, bias, slope, rows, kblocks, npairs,
+                                          out_map, rows, kblocks, npairs,
                                           fault),
                        "tensor-core GEMM launch");
 }
@@ -609,28 +531,9 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     if (st != LSTM_OK)
         return st;
     return math == LSTM_MATH_TF32
-               ? launch_tiles<GatesTf32Shape>(x_map, whi_map, wlo_map, g_map, nullptr, nullptr,
-                                              0.0f, rows, kp, fault, stream)
-               : launch_tiles<GatesShape>(x_map, whi_map, wlo_map, g_map, nullptr, nullptr, 0.0f,
-                                          rows, kp, fault, stream);
-}
-
-int launch_head_leaky(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                      const CUtensorMap &wlo_map, const CUtensorMap &out_map,
-                      const float *bias, float slope, int rows, int kp, unsigned *fault,
-                      cudaStream_t stream)
-{
-    return launch_tiles<LeakyShape>(x_map, whi_map, wlo_map, out_map, nullptr, bias, slope, rows,
-                                    kp, fault, stream);
-}
-
-int launch_head_classifier(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                           const CUtensorMap &wlo_map, const float *bias, float *out, int rows,
-                           int kp, unsigned *fault, cudaStream_t stream)
-{
-    // no store map: the log-softmax rows (7 floats) are written directly
-    return launch_tiles<ClassifierShape>(x_map, whi_map, wlo_map, x_map, out, bias, 0.0f, rows,
-                                         kp, fault, stream);
+               ? launch_tiles<GatesTf32Shape>(x_map, whi_map, wlo_map, g_map, rows, kp, fault,
+                                              stream)
+               : launch_tiles<GatesShape>(x_map, whi_map, wlo_map, g_map, rows, kp, fault, stream);
 }
 
 } // namespace lstm

@@ -48,7 +48,7 @@ def test_allocation_failures_are_reported_and_leak_nothing(layers):
         assert e.value.code == binding.LSTM_E_ALLOC
     lib.lstm_test_fail_allocations(0, 0)
     assert abs(_free() - free0) < (4 << 20)
-    lib.lstm_test_fail_allocations(1, 1)
+    lib.lstm_test_fail_allocations(0, 1)  # the heads' one device allocation
     with pytest.raises(binding.LSTMError) as e:
         binding.LSTMHeads(synthetic.heads_weights(), 100)
     assert e.value.code == binding.LSTM_E_ALLOC
