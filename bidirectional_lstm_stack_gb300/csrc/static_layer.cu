@@ -25,26 +25,18 @@ namespace {
 constexpr long kStaticRows = 4096;
 __device__ __align__(256) float g_static_gates[kStaticRows * kGateColumns];
 
-// Per-device set-up, with that device current: resolve the array's device
-// address (a host-side name of a __device__ array is not a device address)
-// and set the kernels' launch attributes.
+// Per-device set-up, with that device current: the kernels' per-device
+// attributes (prepare_device) and the array's device address (a host-side
+// name of a __device__ array is not a device address).
 int static_setup(int device, float **gates)
 {
     static std::mutex mu;
     static float *addr[64] = {};
-    if (device < 0 || device >= 64)
-        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: device %d out of range", device);
+    int st = prepare_device(device);  // also rejects devices out of range
+    if (st != LSTM_OK)
+        return st;
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[device]) {
-        cudaDeviceProp prop;
-        int st = cuda_status(cudaGetDeviceProperties(&prop, device), "device properties");
-        if (st != LSTM_OK)
-            return st;
-        if (prop.major != 10 || prop.minor != 3)
-            return fail(LSTM_E_DEVICE, "device %d is compute capability %d.%d; the kernels are built for 10.3",
-                        device, prop.major, prop.minor);
-        if ((st = projection_prepare(device)) != LSTM_OK || (st = recurrence_prepare(device)) != LSTM_OK)
-            return st;
         void *p = nullptr;
         st = cuda_status(cudaGetSymbolAddress(&p, g_static_gates), "static gate buffer address");
         if (st != LSTM_OK)
@@ -53,11 +45,6 @@ int static_setup(int device, float **gates)
     }
     *gates = addr[device];
     return LSTM_OK;
-}
-
-bool aligned16(const void *p)
-{
-    return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
 }
 
 }  // namespace
@@ -83,22 +70,19 @@ extern "C" int lstm_layer_forward_static(const float *x, int batch, int steps, i
                     batch, steps, rows, kStaticRows);
     if (in_width <= 0 || in_width > kp || kp % 32 != 0)
         return fail(LSTM_E_INVALID, "lstm_layer_forward_static: in_width %d, kp %d", in_width, kp);
-    if (!aligned16(x) || !aligned16(wp_hi) || !aligned16(wp_lo) || !aligned16(rp) || !aligned16(y))
-        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: device pointers must be 16-byte aligned");
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, x) != cudaSuccess) {
-        cudaGetLastError();
-        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: x is not known to CUDA");
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
-        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: x is not device memory");
-    int current = -1;
-    int st = cuda_status(cudaGetDevice(&current), "current device");
-    if (st != LSTM_OK)
+    int st;
+    if ((st = check_aligned(x, "static layer input")) || (st = check_aligned(wp_hi, "wp_hi")) ||
+        (st = check_aligned(wp_lo, "wp_lo")) || (st = check_aligned(rp, "rp")) ||
+        (st = check_aligned(y, "static layer output")))
         return st;
-    if (attr.device != current)
+    int xdev = -1, current = -1;
+    if ((st = pointer_device(x, &xdev)))
+        return st;
+    if ((st = cuda_status(cudaGetDevice(&current), "current device")))
+        return st;
+    if (xdev != current)
         return fail(LSTM_E_INVALID, "lstm_layer_forward_static: x is on device %d, current device is %d",
-                    attr.device, current);
+                    xdev, current);
     float *gates = nullptr;
     if ((st = static_setup(current, &gates)) != LSTM_OK)
         return st;
