@@ -209,8 +209,7 @@ struct lstm_stack {
     float *ping[2] = {};        // [max_rows][256] each
     float *x_stage = nullptr;   // [max_rows][60]   (forward_host)
     float *y_stage = nullptr;   // [max_rows][256]  (forward_host)
-    CUtensorMap map_whi[kLayers];
-    CUtensorMap map_wlo[kLayers];
+    ProjectionW map_w[kLayers];
     CUtensorMap map_ping[2];
     CUtensorMap map_x;
     const float *map_x_base = nullptr;
@@ -436,9 +435,7 @@ extern "C" int lstm_stack_create_ordered(const lstm_stack_weights *weights, int 
         s->wp_lo[l] = s->weights + offs[l][1];
         s->rp[l] = s->weights + offs[l][2];
         s->bias[l] = s->weights + offs[l][3];
-        st = encode_matrix_map(&s->map_whi[l], s->wp_hi[l], kGateColumns, s->kp[l], kProjectionWBoxRows);
-        if (st == LSTM_OK)
-            st = encode_matrix_map(&s->map_wlo[l], s->wp_lo[l], kGateColumns, s->kp[l], kProjectionWBoxRows);
+        st = encode_projection_w(&s->map_w[l], s->wp_hi[l], s->wp_lo[l], s->kp[l]);
     }
     for (int i = 0; i < 2 && st == LSTM_OK; ++i)
         st = encode_matrix_map(&s->map_ping[i], s->ping[i], max_rows, kOutput, kProjectionBoxRows);
@@ -506,8 +503,8 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
         float *dst = l == kLayers - 1 ? y : s->ping[l & 1];
         if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 0, 0), stream, cudaEventRecordExternal), "event")))
             return st;
-        st = launch_projection(src, s->map_whi[l], s->map_wlo[l], s->gates, static_cast<int>(rows),
-                               s->kp[l], s->math, s->fault, stream);
+        st = launch_projection(src, s->map_w[l], s->gates, static_cast<int>(rows), s->kp[l],
+                               s->math, s->fault, stream);
         if (st != LSTM_OK)
             return st;
         if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 0, 1), stream, cudaEventRecordExternal), "event")))
@@ -747,13 +744,12 @@ extern "C" int lstm_projection_math(const float *x, int rows, int in_width, cons
     unsigned *fault = fault_word();
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
-    CUtensorMap xm, hm, lm;
+    CUtensorMap xm;
+    ProjectionW w;
     if ((st = encode_matrix_map(&xm, x, rows, in_width, kProjectionBoxRows)) ||
-        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionWBoxRows)) ||
-        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionWBoxRows)))
+        (st = encode_projection_w(&w, wp_hi, wp_lo, kp)))
         return st;
-    return launch_projection(xm, hm, lm, g, rows, kp, math, fault,
-                             static_cast<cudaStream_t>(stream));
+    return launch_projection(xm, w, g, rows, kp, math, fault, static_cast<cudaStream_t>(stream));
 }
 
 namespace {

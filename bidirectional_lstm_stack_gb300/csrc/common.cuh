@@ -83,16 +83,23 @@ struct DeviceGuard {
 // one CTA of a 2-CTA cluster loads (half of a 256-row W tile).
 constexpr int kProjectionBoxRows = 128;
 constexpr int kProjectionWBoxRows = 128;
+constexpr int kProjectionNarrowWBoxRows = 64;  // half of a 128-row W tile
 // Encodes the tensor map of a row-major fp32 matrix [rows][cols] read in
 // boxes of 16 columns x box_rows rows with the 64-byte swizzle.
 int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols,
                       int box_rows);
+// The tensor maps of one layer's packed W planes [1024][kp]: 128-row boxes
+// for the 256-column tiles, 64-row boxes for the 128-column tiles used when
+// few rows would leave most SMs idle.
+struct ProjectionW {
+    CUtensorMap hi, lo, hi_narrow, lo_narrow;
+};
+int encode_projection_w(ProjectionW *w, const float *wp_hi, const float *wp_lo, int kp);
 // G[rows][1024] = X . Wp^T in 3xTF32 (math LSTM_MATH_3XTF32) or with single
-// TF32 products (LSTM_MATH_TF32, wlo_map unused); the maps come from
+// TF32 products (LSTM_MATH_TF32, the lo plane unused); x_map from
 // encode_matrix_map (G's own store map is encoded per launch).
-int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                      const CUtensorMap &wlo_map, float *g, int rows, int kp, int math,
-                      unsigned *fault, cudaStream_t stream);
+int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, int rows, int kp,
+                      int math, unsigned *fault, cudaStream_t stream);
 int projection_prepare(int device);
 // Store map of a row-major fp32 matrix [rows][cols] written in 32 x 32
 // slices with the 128-byte swizzle (the projection's G).

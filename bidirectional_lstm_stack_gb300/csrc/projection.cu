@@ -86,7 +86,9 @@ struct Shape {
 };
 using GatesShape = Shape<256, false>;
 using GatesTf32Shape = Shape<256, true>;
-static_assert(GatesShape::BN / CLUSTER == kProjectionWBoxRows && BM == kProjectionBoxRows,
+using GatesNarrowShape = Shape<128, false>;  // few rows: twice the tiles
+static_assert(GatesShape::BN / CLUSTER == kProjectionWBoxRows && BM == kProjectionBoxRows &&
+                  GatesNarrowShape::BN / CLUSTER == kProjectionNarrowWBoxRows,
               "TMA boxes");
 
 using ptx::sw64_desc;
@@ -432,6 +434,7 @@ namespace {
 const void *const kKernels[] = {
     reinterpret_cast<const void *>(&projection_kernel<GatesShape>),
     reinterpret_cast<const void *>(&projection_kernel<GatesTf32Shape>),
+    reinterpret_cast<const void *>(&projection_kernel<GatesNarrowShape>),
 };
 
 // Persistent grid over the row tiles (pairs of 128-row tiles, one per CTA of
@@ -517,9 +520,21 @@ int projection_prepare(int device)
     return LSTM_OK;
 }
 
-int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
-                      const CUtensorMap &wlo_map, float *g, int rows, int kp, int math,
-                      unsigned *fault, cudaStream_t stream)
+int encode_projection_w(ProjectionW *w, const float *wp_hi, const float *wp_lo, int kp)
+{
+    int st;
+    if ((st = encode_matrix_map(&w->hi, wp_hi, kGateColumns, kp, kProjectionWBoxRows)) ||
+        (st = encode_matrix_map(&w->lo, wp_lo, kGateColumns, kp, kProjectionWBoxRows)) ||
+        (st = encode_matrix_map(&w->hi_narrow, wp_hi, kGateColumns, kp,
+                                kProjectionNarrowWBoxRows)) ||
+        (st = encode_matrix_map(&w->lo_narrow, wp_lo, kGateColumns, kp,
+                                kProjectionNarrowWBoxRows)))
+        return st;
+    return LSTM_OK;
+}
+
+int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, int rows, int kp,
+                      int math, unsigned *fault, cudaStream_t stream)
 {
     if (math != LSTM_MATH_3XTF32 && math != LSTM_MATH_TF32)
         return fail(LSTM_E_INVALID, "projection: unknown math mode %d", math);
@@ -530,10 +545,20 @@ int launch_projection(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     int st = encode_store_map(&g_map, g, rows, kGateColumns);
     if (st != LSTM_OK)
         return st;
-    return math == LSTM_MATH_TF32
-               ? launch_tiles<GatesTf32Shape>(x_map, whi_map, wlo_map, g_map, rows, kp, fault,
-                                              stream)
-               : launch_tiles<GatesShape>(x_map, whi_map, wlo_map, g_map, rows, kp, fault, stream);
+    if (math == LSTM_MATH_TF32)
+        return launch_tiles<GatesTf32Shape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream);
+    // With 256-column tiles a pair of row tiles is 4 cluster units; when those
+    // would fill at most half of the clusters that run at once, 128-column
+    // tiles give every CTA half the work on twice as many SMs.
+    int dev = 0;
+    if ((st = cuda_status(cudaGetDevice(&dev), "current device")))
+        return st;
+    const int fit = (dev >= 0 && dev < 64 && g_max_clusters[dev] > 0) ? g_max_clusters[dev] : 74;
+    const long units = (static_cast<long>(rows) + 2 * BM - 1) / (2 * BM) * GatesShape::TILES_N;
+    if (2 * units <= fit)
+        return launch_tiles<GatesNarrowShape>(x_map, w.hi_narrow, w.lo_narrow, g_map, rows, kp,
+                                              fault, stream);
+    return launch_tiles<GatesShape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream);
 }
 
 } // namespace lstm

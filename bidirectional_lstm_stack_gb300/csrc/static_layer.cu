@@ -89,14 +89,14 @@ extern "C" int lstm_layer_forward_static(const float *x, int batch, int steps, i
     unsigned *fault = fault_word();
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
-    CUtensorMap xm, hm, lm;
+    CUtensorMap xm;
+    ProjectionW w;
     if ((st = encode_matrix_map(&xm, x, rows, in_width, kProjectionBoxRows)) ||
-        (st = encode_matrix_map(&hm, wp_hi, kGateColumns, kp, kProjectionWBoxRows)) ||
-        (st = encode_matrix_map(&lm, wp_lo, kGateColumns, kp, kProjectionWBoxRows)))
+        (st = encode_projection_w(&w, wp_hi, wp_lo, kp)))
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((st = launch_projection(xm, hm, lm, gates, static_cast<int>(rows), kp, LSTM_MATH_3XTF32,
-                                fault, s)))
+    if ((st = launch_projection(xm, w, gates, static_cast<int>(rows), kp, LSTM_MATH_3XTF32, fault,
+                                s)))
         return st;
     if ((st = launch_recurrence(gates, rp, bias, y, batch, steps, 0, fault, s)))
         return st;
