@@ -167,3 +167,42 @@ def test_onnx_gate_order_stack(stack, layers):
     y1 = _forward(stack, x)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
     assert_within(y2, oracle.lstm_stack(x, layers), what="onnx gate order")
+
+
+def test_two_host_threads_with_their_own_stacks(layers):
+    # per-thread error state, per-stack scratch and thread-local graph capture:
+    # two threads forwarding concurrently on their own streams agree with the
+    # oracle (and with each other on the same input)
+    import threading
+
+    import torch
+    wl = synthetic.WORKLOADS["b8_t589_x3"]
+    x_np = synthetic.stack_input(wl)
+    results, errors = {}, []
+
+    def worker(k):
+        try:
+            torch.cuda.set_device(0)
+            s = binding.LSTMStack(layers, 8, 589)
+            stream = torch.cuda.Stream()
+            x = cuda(x_np)
+            with torch.cuda.stream(stream):
+                outs = [s(x, None, stream) for _ in range(3)]
+            stream.synchronize()
+            results[k] = [o.cpu().numpy() for o in outs]
+            s.close()
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    ref = oracle.lstm_stack(x_np, layers)
+    first = results[0][0]
+    for k in range(2):
+        for y in results[k]:
+            assert np.array_equal(y.view(np.uint32), first.view(np.uint32))
+    assert_within(first, ref, what="threads")
