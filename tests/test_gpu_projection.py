@@ -17,9 +17,11 @@ def weights():
 
 
 # rows: one row; a full tile; a tile plus one; several tiles with a ragged
-# tail; the small workload's 64 rows; the batch-8 workload's 4712 rows
-CASES = [(60, 1), (60, 64), (256, 128), (256, 129), (60, 300), (256, 300), (60, 4712),
-         (256, 4712)]
+# tail; the small workload's 64 rows; up to 2304 rows the kernel runs
+# 128-column tiles, above that (the batch-8 workload's 4712 rows) 256-column
+# tiles
+CASES = [(60, 1), (60, 64), (256, 128), (256, 129), (60, 300), (256, 300), (256, 1024),
+         (60, 1025), (256, 1500), (256, 2304), (60, 4712), (256, 4712)]
 
 
 @pytest.mark.parametrize("in_width,rows", CASES)
