@@ -419,6 +419,7 @@ const Variant kVariants[] = {
     variant<8, 1, 1, 128>(),    variant<8, 2, 1, 128>(), variant<16, 1, 1, 64>(),
     variant<16, 2, 1, 64>(),    variant<4, 4, 2>(),      variant<4, 4, 4>(),
     variant<4, 8, 1>(),         variant<4, 8, 2>(),      variant<4, 4, 1>(),
+    variant<8, 4, 1, 128>(),    variant<8, 8, 1, 128>(),
 };
 
 // threads == 0: the variant's default block size
@@ -438,16 +439,17 @@ int max_active_clusters(const Variant &v, int *out);
 // T = 589, us per step): up to 32 windows, narrow clusters of 8 (128 threads,
 // one window per cluster; 0.44 at one window, 0.48 at 8, 0.60 at 32); then
 // narrow clusters with two windows per group (0.73 at 48 windows); clusters
-// of 4 with one window per group (0.62 at 32); then 2 chunks of 2 windows per
-// lane (0.95 at 64 windows), of 4 windows (1.48 at 96 and 128) and of 8
-// windows (2.60 at 192 and 256: more windows per chunk means fewer gather
-// shuffles per window and more independent work per lane).  The first whose
+// of 4 with one window per group (0.62 at 32); 2 chunks of 2 windows per
+// lane (0.95 at 64 windows); narrow clusters with 4 windows per group (1.14
+// at 80); then 2 chunks of 4 windows (1.48 at 128) and of 8 windows (2.60 at
+// 192 and 256: more windows per chunk means fewer gather shuffles per window
+// and more independent work per lane).  The first whose
 // clusters for both directions fit the device at once wins; past that, the
 // widest tile.
 const Variant *choose_variant(int batch)
 {
-    static const int order[][4] = {{8, 1, 1, 128}, {8, 2, 1, 128}, {4, 1, 1, 0},
-                                   {4, 2, 2, 0},   {4, 4, 2, 0},   {4, 8, 2, 0}};
+    static const int order[][4] = {{8, 1, 1, 128}, {8, 2, 1, 128}, {4, 1, 1, 0},  {4, 2, 2, 0},
+                                   {8, 4, 1, 128}, {4, 4, 2, 0},   {4, 8, 2, 0}};
     constexpr int N = sizeof(order) / sizeof(order[0]);
     constexpr int NARROW_MAX_BATCH = 32;
     static std::mutex mu;

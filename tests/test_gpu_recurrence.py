@@ -14,7 +14,8 @@ VARIANTS = [(16, 1, 1, 0), (16, 2, 1, 0), (16, 4, 1, 0), (16, 8, 1, 0), (8, 1, 1
             (8, 2, 1, 0), (8, 4, 1, 0), (8, 8, 1, 0), (4, 1, 1, 0), (4, 2, 1, 0), (2, 1, 1, 0),
             (4, 1, 2, 0), (4, 1, 4, 0), (4, 1, 8, 0), (4, 2, 2, 0), (4, 2, 4, 0), (4, 2, 8, 0),
             (8, 2, 4, 0), (8, 1, 1, 128), (8, 2, 1, 128), (16, 1, 1, 64), (16, 2, 1, 64),
-            (4, 4, 1, 0), (4, 4, 2, 0), (4, 4, 4, 0), (4, 8, 1, 0), (4, 8, 2, 0)]
+            (4, 4, 1, 0), (4, 4, 2, 0), (4, 4, 4, 0), (4, 8, 1, 0), (4, 8, 2, 0),
+            (8, 4, 1, 128), (8, 8, 1, 128)]
 
 
 def _layer_inputs(batch, steps, layer_index=0, seed=21, scale=1.0):
