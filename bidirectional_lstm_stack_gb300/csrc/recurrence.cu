@@ -434,50 +434,67 @@ const Variant *find_variant(int cluster, int nw, int nch, int threads = 0)
 
 int max_active_clusters(const Variant &v, int *out);
 
-// The default variant for a batch.  Candidates in order of preference, from
-// per-step timings of every variant with both directions running (GB300,
-// T = 589, us per step): up to 32 windows, narrow clusters of 8 (128 threads,
-// one window per cluster; 0.44 at one window, 0.48 at 8, 0.60 at 32); then
-// narrow clusters with two windows per group (0.73 at 48 windows); clusters
-// of 4 with one window per group (0.62 at 32); 2 chunks of 2 windows per
-// lane (0.95 at 64 windows); narrow clusters with 4 windows per group (1.14
-// at 80); then 2 chunks of 4 windows (1.48 at 128) and of 8 windows (2.60 at
-// 192 and 256: more windows per chunk means fewer gather shuffles per window
-// and more independent work per lane).  The first whose
-// clusters for both directions fit the device at once wins; past that, the
-// widest tile.
+// The default variant for a batch: the candidate with the least estimated
+// step time, waves x full-load step time, where a wave is as many clusters
+// (for both directions) as the device runs at once
+// (cudaOccupancyMaxActiveClusters, queried per device) and the full-load
+// step times are measured with both directions running (GB300, T = 589, us):
+//   narrow clusters of 8, 128 threads, one window per cluster      0.62
+//   the same with 2 windows per group                             0.73
+//   clusters of 4, one window per group                           0.64
+//   clusters of 4, 2 chunks of 2 windows per lane                 0.95
+//   narrow clusters of 8, 4 windows per group                     1.14
+//   clusters of 4, 2 chunks of 4 windows                          1.48
+//   clusters of 4, 2 chunks of 8 windows                          2.60
+// (more windows per chunk: fewer gather shuffles per window and more
+// independent work per lane, so more windows per step on the same SMs).  A
+// partly loaded wave runs faster than its full-load time (0.45 us at one
+// window); ties go to the earlier candidate.
 const Variant *choose_variant(int batch)
 {
-    static const int order[][4] = {{8, 1, 1, 128}, {8, 2, 1, 128}, {4, 1, 1, 0},  {4, 2, 2, 0},
-                                   {8, 4, 1, 128}, {4, 4, 2, 0},   {4, 8, 2, 0}};
-    constexpr int N = sizeof(order) / sizeof(order[0]);
-    constexpr int NARROW_MAX_BATCH = 32;
+    struct Candidate {
+        int cluster, nw, nch, threads;
+        float us_per_step;  // full load
+    };
+    static const Candidate cand[] = {{8, 1, 1, 128, 0.62f}, {8, 2, 1, 128, 0.73f},
+                                     {4, 1, 1, 0, 0.64f},   {4, 2, 2, 0, 0.95f},
+                                     {8, 4, 1, 128, 1.14f}, {4, 4, 2, 0, 1.48f},
+                                     {4, 8, 2, 0, 2.60f}};
+    constexpr int N = sizeof(cand) / sizeof(cand[0]);
     static std::mutex mu;
     static int fits[64][N];
     static bool known[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        dev = -1;
-    if (dev >= 0) {
+        return find_variant(4, 8, 2);
+    {
         std::lock_guard<std::mutex> lock(mu);
         if (!known[dev]) {
             for (int i = 0; i < N; ++i) {
                 int n = 0;
-                const Variant *v = find_variant(order[i][0], order[i][1], order[i][2], order[i][3]);
+                const Variant *v =
+                    find_variant(cand[i].cluster, cand[i].nw, cand[i].nch, cand[i].threads);
                 fits[dev][i] = (v && max_active_clusters(*v, &n) == LSTM_OK) ? n : 0;
             }
             known[dev] = true;
         }
     }
+    const Variant *best = nullptr;
+    float best_cost = 0.0f;
     for (int i = 0; i < N; ++i) {
-        if (i == 0 && batch > NARROW_MAX_BATCH)
+        const Variant *v = find_variant(cand[i].cluster, cand[i].nw, cand[i].nch, cand[i].threads);
+        if (!v || fits[dev][i] < 2)
             continue;
-        const Variant *v = find_variant(order[i][0], order[i][1], order[i][2], order[i][3]);
         const long tiles = (static_cast<long>(batch) + v->tile - 1) / v->tile;
-        if (dev >= 0 && 2 * tiles <= fits[dev][i])
-            return v;
+        const long per_wave = fits[dev][i] / 2;  // clusters per direction at once
+        const long waves = (tiles + per_wave - 1) / per_wave;
+        const float cost = static_cast<float>(waves) * cand[i].us_per_step;
+        if (!best || cost < best_cost) {
+            best = v;
+            best_cost = cost;
+        }
     }
-    return find_variant(4, 8, 2);
+    return best ? best : find_variant(4, 8, 2);
 }
 
 int launch_variant(const Variant &v, const float *g, const float *rp, const float *bias, float *y,

@@ -58,7 +58,8 @@ def test_stack_matches_oracle(stack, layers, name):
 
 
 def test_stack_ragged_small_shapes(stack, layers):
-    for batch, steps in [(1, 1), (2, 3), (7, 129), (19, 40), (41, 30), (83, 12), (130, 9)]:
+    for batch, steps in [(1, 1), (2, 3), (7, 129), (19, 40), (41, 30), (83, 12), (130, 9),
+                         (192, 5)]:
         x = synthetic.random_matrix(batch * 1000 + steps, (batch, steps, 60))
         y = _forward(stack, x)
         assert_within(y, oracle.lstm_stack(x, layers), what=f"stack b{batch} t{steps}")
