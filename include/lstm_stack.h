@@ -241,8 +241,9 @@ int lstm_projection_math(const float *x, int rows, int in_width,
  *   y    : device [batch][steps][256]; writes columns d*128 .. d*128+127 only
  *   direction : 0 forward (t = 0..steps-1), 1 reverse (t = steps-1..0)
  * h and c start at zero for every window.  One thread-block cluster holds R
- * in shared memory split across its blocks and exchanges h through
- * distributed shared memory each step.  Errors: LSTM_E_INVALID,
+ * in its blocks' registers, split by hidden unit, and exchanges h through
+ * distributed shared memory each step; the variant (cluster shape and
+ * windows per cluster) is chosen from the batch size.  Errors: LSTM_E_INVALID,
  * LSTM_E_OVERFLOW, LSTM_E_DEVICE, LSTM_E_CUDA. */
 int lstm_recurrence(const float *g, const float *rp, const float *bias,
                     float *y, int batch, int steps, int direction,
@@ -255,8 +256,9 @@ int lstm_recurrence(const float *g, const float *rp, const float *bias,
  * (threads_per_block / 8) / (128 / cluster_size) * windows_per_chunk * chunks.
  * threads_per_block 0 selects the default (256; 512 for clusters of 2).
  * Variants (cluster, windows_per_chunk, chunks, threads): (16|8, 1|2|4|8, 1,
- * 0), (4, 1|2, 1, 0), (2, 1, 1, 0), (4, 1, 2|4|8, 0), (4, 2, 2|4|8, 0),
- * (8, 2, 4, 0), and the narrow (8, 1|2, 1, 128), (16, 1|2, 1, 64).  Every
+ * 0), (4, 1|2|4|8, 1, 0), (2, 1, 1, 0), (4, 1, 2|4|8, 0), (4, 2, 2|4|8, 0),
+ * (4, 4, 2|4, 0), (4, 8, 2, 0), (8, 2, 4, 0), and the narrow
+ * (8, 1|2|4|8, 1, 128), (16, 1|2, 1, 64).  Every
  * variant computes the same sums in the same order, so all give bitwise
  * identical y (the pages' three recurrence kernels are likewise bitwise
  * identical, lstmproj.rs module docs).  Errors as lstm_recurrence, plus
