@@ -12,7 +12,9 @@
 // lives in registers for the whole kernel: thread (slot, kc) holds the 4 x 16
 // weights of one unit for K chunk kc (16 columns).  Each step:
 //   1. every thread multiplies its weights with h_prev[kc*16 .. +16] of each
-//      of its NW windows from shared memory (paired FMAs, __ffma2_rn);
+//      of its windows from shared memory (paired FMAs, __ffma2_rn); a thread
+//      runs NCH independent chunks of NW windows, each phase below over all
+//      chunks, so their latencies overlap;
 //   2. the 8 lanes sharing a unit reduce their partial sums by a fixed
 //      butterfly (lane bits 2, 1, 0): a reduce-scatter that leaves each lane
 //      its share of the unit's gate pre-activations;
@@ -40,8 +42,6 @@
 // The arithmetic per (window, unit, gate) is the same for every cluster size
 // and tile width (same K chunks, same pairing, same reduction tree), so all
 // variants give bitwise-identical results.
-#include <stdio.h>
-
 #include <mutex>
 
 #include "common.cuh"
