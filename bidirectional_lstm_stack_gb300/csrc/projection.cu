@@ -13,7 +13,10 @@
 //    both CTAs' shared memory (half the W traffic from L2 per tile; clusters
 //    of four were measured slower);
 //  * K advances in blocks of 16 fp32 (64 bytes, 64-byte swizzle) through a
-//    4-stage shared-memory ring (48 KiB per stage);
+//    192 KiB shared-memory ring: 4 stages of 48 KiB (X, X lo, W hi, W lo) in
+//    3xTF32, 8 stages of 24 KiB in the single-product mode; with few rows
+//    (the 256-column grid would fill at most half the SMs) the tiles are 128
+//    columns wide, twice as many CTAs;
 //  * warp 8 (TMA producer) loads the X block and its half of the TF32 hi and
 //    lo planes of Wp (split on the host) into the ring; a stage is reused
 //    only once the MMAs of both CTAs have released it;
