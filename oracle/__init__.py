@@ -14,7 +14,8 @@ the pages are silent.
 
 Pins (the checks that tie the oracle to something other than itself) live in
 ``tests/test_oracle_pins.py``: zero weights, the R = 0 closed form, reverse
-equals forward on time-reversed input, a saturated-gate counter whose outputs
+equals forward on time-reversed input, brute force on H = 2, T = 3 (every gate
+written out as scalar arithmetic), a saturated-gate counter whose outputs
 are tanh of integers (``tests/golden/saturated_counter.json``), a one-hot
 projection, and agreement with ``torch.nn.LSTM`` in float64; for the TF32
 projection mode, the rounding against a bit-level definition and the TF32

@@ -15,6 +15,8 @@ packed column) fails at least one of them:
   integers (tests/golden/saturated_counter.json);
 * agreement with torch.nn.LSTM in float64 (a library routine with the same
   i,f,g,o gate blocks and separate input/recurrent biases);
+* brute force on H = 2, T = 3, input 2, both directions: every gate written
+  out as scalar arithmetic;
 * the packed projection against a one-hot W and against numpy's matmul;
 * TF32 projection mode: the oracle's rounding against a definition written
   on the bit layout (keep sign, exponent and the top 10 mantissa bits; the
@@ -395,3 +397,47 @@ def test_heads_match_torch_and_normalise():
     # log-softmax is unchanged by a constant added to every logit
     np.testing.assert_allclose(oracle.heads(y, W0, b0, W1, b1, W2, b2 + 3.0), out,
                                rtol=0, atol=1e-13)
+
+
+# ---- brute force: H = 2, T = 3, input 2, one layer, both directions -------
+
+def _brute_h2_t3(x, W, R, Wb, Rb, reverse):
+    """The LSTM written out scalar by scalar for two units: every gate's
+    pre-activation spelled out (rows i0 i1 f0 f1 g0 g1 o0 o1), no loop over
+    units or gates; the time loop (3 steps) is the only loop."""
+    import math
+
+    def sig(v):
+        return 1.0 / (1.0 + math.exp(-v))
+
+    h0 = h1 = c0 = c1 = 0.0
+    out = {}
+    for t in ((2, 1, 0) if reverse else (0, 1, 2)):
+        x0, x1 = float(x[t][0]), float(x[t][1])
+
+        def pre(r):
+            return (W[r][0] * x0 + W[r][1] * x1 + Wb[r]
+                    + R[r][0] * h0 + R[r][1] * h1 + Rb[r])
+
+        i0, i1 = sig(pre(0)), sig(pre(1))
+        f0, f1 = sig(pre(2)), sig(pre(3))
+        g0, g1 = math.tanh(pre(4)), math.tanh(pre(5))
+        o0, o1 = sig(pre(6)), sig(pre(7))
+        c0 = f0 * c0 + i0 * g0
+        c1 = f1 * c1 + i1 * g1
+        h0 = o0 * math.tanh(c0)
+        h1 = o1 * math.tanh(c1)
+        out[t] = (h0, h1)
+    return np.array([out[0], out[1], out[2]])
+
+
+def test_brute_force_h2_t3_both_directions():
+    rng = np.random.default_rng(50)
+    lay = {"w": rng.uniform(-0.8, 0.8, (2, 8, 2)), "r": rng.uniform(-0.8, 0.8, (2, 8, 2)),
+           "b": rng.uniform(-0.8, 0.8, (2, 16))}
+    x = rng.standard_normal((1, 3, 2))
+    y = oracle.lstm_stack(x, [lay])
+    for d in range(2):
+        ref = _brute_h2_t3(x[0], lay["w"][d], lay["r"][d], lay["b"][d][:8], lay["b"][d][8:],
+                           reverse=d == 1)
+        np.testing.assert_allclose(y[0, :, 2 * d:2 * d + 2], ref, rtol=0, atol=1e-15)
