@@ -207,3 +207,32 @@ def test_two_host_threads_with_their_own_stacks(layers):
         for y in results[k]:
             assert np.array_equal(y.view(np.uint32), first.view(np.uint32))
     assert_within(first, ref, what="threads")
+
+
+def test_per_layer_error_localises_drift(layers):
+    # the stack layer by layer through the step entry points: each layer's
+    # error on its own (GPU) input, and the error accumulated from x
+    import torch
+    wl = synthetic.WORKLOADS["b8_t589_x3"]
+    x = synthetic.stack_input(wl)
+    B, T = wl.batch, wl.steps
+    cur = cuda(x.reshape(B * T, 60))
+    ref_chain = x
+    for l, lay in enumerate(layers):
+        inw, kp = (60, 64) if l == 0 else (256, 256)
+        wp_hi, wp_lo, rp, bias = binding.lstm_pack_layer(lay["w"], lay["r"], lay["b"], inw, kp)
+        g = torch.empty((B * T, 1024), device="cuda")
+        y = torch.empty((B, T, 256), device="cuda")
+        binding.lstm_projection(cur, B * T, inw, cuda(wp_hi), cuda(wp_lo), kp, g)
+        rpt, bt = cuda(rp), cuda(bias)
+        for d in range(2):
+            binding.lstm_recurrence(g, rpt[d], bt[d], y, B, T, d)
+        torch.cuda.synchronize()
+        got = y.cpu().numpy()
+        local = oracle.lstm_stack(cur.cpu().numpy().reshape(B, T, inw), [lay])
+        ref_chain = oracle.lstm_stack(ref_chain, [lay])
+        e_local = assert_within(got, local, what=f"layer {l} on its own input")
+        e_chain = assert_within(got, ref_chain, what=f"layer {l} from x")
+        print(f"layer {l}: max abs err {e_local:.2e} on its input, {e_chain:.2e} from x")
+        cur = y.reshape(B * T, 256)
+    assert binding.lstm_fault_status() == 0

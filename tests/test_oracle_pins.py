@@ -233,10 +233,11 @@ def test_matches_torch_lstm_small():
                                _torch_lstm(x, layers), rtol=0, atol=1e-12)
 
 
-def test_matches_torch_lstm_full_width():
-    # the stack's real shape on the small workload (batch 1, T = 64)
+@pytest.mark.parametrize("name", ["b1_t64", "b1_t589"])
+def test_matches_torch_lstm_full_width(name):
+    # the stack's real shape on the one-window workloads (T = 64 and 589)
     layers = synthetic.stack_weights()
-    x = synthetic.stack_input(synthetic.WORKLOADS["b1_t64"])
+    x = synthetic.stack_input(synthetic.WORKLOADS[name])
     np.testing.assert_allclose(oracle.lstm_stack(x, layers),
                                _torch_lstm(x, layers), rtol=0, atol=1e-12)
 
