@@ -93,16 +93,25 @@ __device__ __forceinline__ float inv_one_plus_ex2(float w)
 }
 
 // One butterfly level: lanes that differ in `mask` exchange half of their
-// N values; each keeps the sum for the half its mask bit selects.
-template <int N>
+// N values; each keeps the sums for the half its mask bit selects.
+// PERM: the lane whose mask bit is set holds its values in an order with the
+// two halves swapped (the lane-dependent order of the partial sums set up
+// at kernel start), so every lane keeps its lower half and sends its upper
+// half, without selects.  Otherwise the values are in logical order and
+// each lane selects.  Both add the same two values.
+template <int N, bool PERM>
 __device__ __forceinline__ void reduce_level(const float (&in)[N], float (&out)[N / 2], int mask,
                                              bool upper)
 {
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
-        const float keep = upper ? in[i + N / 2] : in[i];
-        const float send = upper ? in[i] : in[i + N / 2];
-        out[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        if constexpr (PERM) {
+            out[i] = in[i] + __shfl_xor_sync(0xffffffffu, in[i + N / 2], mask);
+        } else {
+            const float keep = upper ? in[i + N / 2] : in[i];
+            const float send = upper ? in[i] : in[i + N / 2];
+            out[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
     }
 }
 
@@ -121,7 +130,14 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     constexpr int HV = V >= 8 ? V / 8 : 1;  // values a lane holds after the reduction
     constexpr int REPL = V >= 8 ? 4 / HV : 8;  // lanes holding one window's cell
     constexpr int PFD = NCH >= 4 ? 2 : PF;     // projection prefetch depth (steps)
+    // Select-free butterfly (lane-dependent order of the partial sums) for
+    // one window per chunk and for eight: measured faster there (GB300,
+    // T = 589: 0.45 -> 0.40 us per step at one window, 2.61 -> 2.54 at 256
+    // windows); with 2 or 4 windows per chunk it raised register use and
+    // step time, so those keep the selects.
+    constexpr bool PERM = NW == 1 || NW == 8;
     static_assert(U * SPU == SLOTS && C * U == kHidden && U % 4 == 0, "cluster shape");
+    static_assert(PFD % 2 == 0, "the step parity is taken from the unrolled step index");
 
     __shared__ __align__(16) float hbuf[2][TW][HROW];
     __shared__ __align__(8) uint64_t hbar[2];
@@ -144,14 +160,33 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     const int valid_tw = min(TW, batch - tile * TW);
     const uint32_t step_bytes = static_cast<uint32_t>(kHidden * valid_tw * 4);
 
-    // weights: 4 gate rows of unit u, columns kc*16 .. kc*16+15, as pairs,
-    // each row scaled by its gate's k_q (see the activations above)
+    // The partial sums of a chunk have logical index w*4 + q (window w of
+    // the chunk, gate q).  Lane kc keeps them in the order j -> j ^ xperm:
+    // each butterfly level below then keeps the lower half of a lane's
+    // array, which for a lane with that level's mask bit set is the upper
+    // half of the logical values.  The order only permutes which gate row
+    // and which window a slot computes; the sums and their order are the
+    // same, so results do not depend on it.
+    constexpr int X2 = V >= 8 ? V / 2 : 2, X1 = V >= 8 ? V / 4 : 1, X0 = V >= 8 ? V / 8 : 0;
+    auto xperm_of = [](int k) {
+        return PERM ? ((k & 4) ? X2 : 0) | ((k & 2) ? X1 : 0) | ((k & 1) ? X0 : 0) : 0;
+    };
+    // gate slot q holds gate q ^ xq; window slot w holds window w ^ (xperm >> 2)
+    // of the chunk, which the senders realise by storing window w's values
+    // of K chunk k at row w ^ (xperm_of(k) >> 2) of the chunk's rows, so
+    // that slot w is read from row w
+    const int xq = xperm_of(kc) & 3;
+
+    // weights: 4 gate rows of unit u (slot q: gate q ^ xq), columns
+    // kc*16 .. kc*16+15, as pairs, each row scaled by its gate's k_q (see the
+    // activations above)
     float2 r2[4][KLEN / 2];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float kq = q == 2 ? -2.0f * kLog2e : -kLog2e;
+        const int gq_row = q ^ xq;
+        const float kq = gq_row == 2 ? -2.0f * kLog2e : -kLog2e;
         const float2 *src =
-            reinterpret_cast<const float2 *>(rp + (4 * u + q) * kHidden + kc * KLEN);
+            reinterpret_cast<const float2 *>(rp + (4 * u + gq_row) * kHidden + kc * KLEN);
 #pragma unroll
         for (int i = 0; i < KLEN / 2; ++i)
             r2[q][i] = make_float2(src[i].x * kq, src[i].y * kq);
@@ -214,8 +249,12 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     float *ych0 = y + static_cast<long>(tile_w0 + wbase + wl) * steps * kOutput +
                   direction * kHidden + u0;
     const int bch0 = tile_w0 + wbase;  // window of chunk 0, w = 0
+    // the four units u0..u0+3 lie in K chunk u0 / 16; their row within the
+    // chunk's windows follows the readers' window order (see xperm_of)
     const uint32_t send_off0 = static_cast<uint32_t>(
-        ((wbase + wl) * HROW + (u0 / KLEN) * CHUNK_STRIDE + (u0 % KLEN)) * 4);
+        ((wbase + (wl ^ (xperm_of(u0 / KLEN) >> 2))) * HROW + (u0 / KLEN) * CHUNK_STRIDE +
+         (u0 % KLEN)) *
+        4);
     // the peers this lane sends to, and their h buffers and mbarriers for
     // both parities, as cluster addresses (a peer's shared memory is one
     // contiguous window, so offsets within it carry over)
@@ -262,7 +301,7 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             const int s = s0 + p;
             if (s >= steps)
                 break;
-            const int par = s & 1;
+            const int par = p & 1;  // = s & 1: s0 is a multiple of the even PFD
             const int t = direction ? steps - 1 - s : s;
 
             // 0. h_{s-1} complete in buffer `par`
@@ -322,13 +361,13 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             for (int ch = 0; ch < NCH; ++ch) {
                 if constexpr (V >= 8) {
                     float a[V / 2], b2[V / 4];
-                    reduce_level<V>(part[ch], a, 4, (kc & 4) != 0);
-                    reduce_level<V / 2>(a, b2, 2, (kc & 2) != 0);
-                    reduce_level<V / 4>(b2, held[ch], 1, (kc & 1) != 0);
+                    reduce_level<V, PERM>(part[ch], a, 4, (kc & 4) != 0);
+                    reduce_level<V / 2, PERM>(a, b2, 2, (kc & 2) != 0);
+                    reduce_level<V / 4, PERM>(b2, held[ch], 1, (kc & 1) != 0);
                 } else {
                     float a[2], b2[1];
-                    reduce_level<4>(part[ch], a, 4, (kc & 4) != 0);
-                    reduce_level<2>(a, b2, 2, (kc & 2) != 0);
+                    reduce_level<4, PERM>(part[ch], a, 4, (kc & 4) != 0);
+                    reduce_level<2, PERM>(a, b2, 2, (kc & 2) != 0);
                     held[ch][0] = b2[0] + __shfl_xor_sync(0xffffffffu, b2[0], 1);
                 }
             }
@@ -439,16 +478,16 @@ int max_active_clusters(const Variant &v, int *out);
 // (for both directions) as the device runs at once
 // (cudaOccupancyMaxActiveClusters, queried per device) and the full-load
 // step times are measured with both directions running (GB300, T = 589, us):
-//   narrow clusters of 8, 128 threads, one window per cluster      0.62
+//   narrow clusters of 8, 128 threads, one window per cluster      0.57
 //   the same with 2 windows per group                             0.73
-//   clusters of 4, one window per group                           0.64
+//   clusters of 4, one window per group                           0.58
 //   clusters of 4, 2 chunks of 2 windows per lane                 0.95
 //   narrow clusters of 8, 4 windows per group                     1.14
 //   clusters of 4, 2 chunks of 4 windows                          1.48
-//   clusters of 4, 2 chunks of 8 windows                          2.60
+//   clusters of 4, 2 chunks of 8 windows                          2.52
 // (more windows per chunk: fewer gather shuffles per window and more
 // independent work per lane, so more windows per step on the same SMs).  A
-// partly loaded wave runs faster than its full-load time (0.45 us at one
+// partly loaded wave runs faster than its full-load time (0.39 us at one
 // window); ties go to the earlier candidate.
 const Variant *choose_variant(int batch)
 {
@@ -456,10 +495,10 @@ const Variant *choose_variant(int batch)
         int cluster, nw, nch, threads;
         float us_per_step;  // full load
     };
-    static const Candidate cand[] = {{8, 1, 1, 128, 0.62f}, {8, 2, 1, 128, 0.73f},
-                                     {4, 1, 1, 0, 0.64f},   {4, 2, 2, 0, 0.95f},
+    static const Candidate cand[] = {{8, 1, 1, 128, 0.57f}, {8, 2, 1, 128, 0.73f},
+                                     {4, 1, 1, 0, 0.58f},   {4, 2, 2, 0, 0.95f},
                                      {8, 4, 1, 128, 1.14f}, {4, 4, 2, 0, 1.48f},
-                                     {4, 8, 2, 0, 2.60f}};
+                                     {4, 8, 2, 0, 2.52f}};
     constexpr int N = sizeof(cand) / sizeof(cand[0]);
     static std::mutex mu;
     static int fits[64][N];
