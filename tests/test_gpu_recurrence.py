@@ -70,6 +70,20 @@ def test_every_variant_matches_oracle(variant):
     assert_within(y, ref, what=f"variant {variant}")
 
 
+@pytest.mark.parametrize("steps", [3, 4, 5, 6, 7, 8, 9, 10, 11])
+@pytest.mark.parametrize("variant", [(8, 1, 1, 128), (4, 2, 4, 0), (4, 4, 4, 0), (4, 8, 2, 0)])
+def test_every_tail_length(variant, steps):
+    # the step loop runs groups of 4 steps (2 with four or more chunks per
+    # lane) and checks for the sequence end only in the last two groups:
+    # every remainder and every count of full groups before the tail
+    batch = 6
+    lay, G, rp, bias = _layer_inputs(batch, steps, seed=24)
+    y = _run(G, rp, bias, batch, steps, variant)
+    ref = oracle.recurrence(G.astype(np.float64), lay["r"], lay["b"], batch, steps)
+    assert_within(y, ref, what=f"variant {variant} T={steps}")
+    assert binding.lstm_fault_status() == 0
+
+
 def test_variants_are_bitwise_identical():
     batch, steps = 37, 41
     _, G, rp, bias = _layer_inputs(batch, steps, seed=23)
