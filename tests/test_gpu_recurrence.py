@@ -84,6 +84,19 @@ def test_every_tail_length(variant, steps):
     assert binding.lstm_fault_status() == 0
 
 
+@pytest.mark.parametrize("batch", [1, 4, 5, 9, 17, 23])
+@pytest.mark.parametrize("variant", [(4, 4, 2, 0), (4, 4, 4, 0), (4, 8, 2, 0), (8, 4, 1, 128)])
+def test_partly_and_wholly_empty_chunks(variant, batch):
+    # tiles whose last chunks hold no window of the batch (those chunks have
+    # no barrier traffic at all in the chunk-major variants)
+    steps = 13
+    lay, G, rp, bias = _layer_inputs(batch, steps, seed=25)
+    y = _run(G, rp, bias, batch, steps, variant)
+    ref = oracle.recurrence(G.astype(np.float64), lay["r"], lay["b"], batch, steps)
+    assert_within(y, ref, what=f"variant {variant} B={batch}")
+    assert binding.lstm_fault_status() == 0
+
+
 def test_variants_are_bitwise_identical():
     batch, steps = 37, 41
     _, G, rp, bias = _layer_inputs(batch, steps, seed=23)
