@@ -673,16 +673,16 @@ int max_active_clusters(const Variant &v, int *out);
 // (for both directions) as the device runs at once
 // (cudaOccupancyMaxActiveClusters, queried per device) and the full-load
 // step times are measured with both directions running (GB300, T = 589, us):
-//   narrow clusters of 8, 128 threads, one window per cluster      0.57
+//   narrow clusters of 8, 128 threads, one window per cluster      0.58
 //   the same with 2 windows per group                             0.73
 //   clusters of 4, one window per group                           0.58
-//   clusters of 4, 2 chunks of 2 windows per lane                 0.95
-//   narrow clusters of 8, 4 windows per group                     1.14
-//   clusters of 4, 2 chunks of 4 windows                          1.48
-//   clusters of 4, 2 chunks of 8 windows                          2.52
+//   clusters of 4, 2 chunks of 2 windows per lane                 0.94
+//   narrow clusters of 8, 4 windows per group                     1.12
+//   clusters of 4, 2 chunks of 4 windows (chunk-major)            1.33
+//   clusters of 4, 2 chunks of 8 windows (chunk-major)            2.22
 // (more windows per chunk: fewer gather shuffles per window and more
 // independent work per lane, so more windows per step on the same SMs).  A
-// partly loaded wave runs faster than its full-load time (0.39 us at one
+// partly loaded wave runs faster than its full-load time (0.40 us at one
 // window); ties go to the earlier candidate.
 const Variant *choose_variant(int batch)
 {
@@ -690,10 +690,10 @@ const Variant *choose_variant(int batch)
         int cluster, nw, nch, threads;
         float us_per_step;  // full load
     };
-    static const Candidate cand[] = {{8, 1, 1, 128, 0.57f}, {8, 2, 1, 128, 0.73f},
-                                     {4, 1, 1, 0, 0.58f},   {4, 2, 2, 0, 0.95f},
-                                     {8, 4, 1, 128, 1.14f}, {4, 4, 2, 0, 1.48f},
-                                     {4, 8, 2, 0, 2.52f}};
+    static const Candidate cand[] = {{8, 1, 1, 128, 0.58f}, {8, 2, 1, 128, 0.73f},
+                                     {4, 1, 1, 0, 0.58f},   {4, 2, 2, 0, 0.94f},
+                                     {8, 4, 1, 128, 1.12f}, {4, 4, 2, 0, 1.33f},
+                                     {4, 8, 2, 0, 2.22f}};
     constexpr int N = sizeof(cand) / sizeof(cand[0]);
     static std::mutex mu;
     static int fits[64][N];
