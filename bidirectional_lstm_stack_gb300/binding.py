@@ -72,6 +72,8 @@ def load():
                                               ctypes.POINTER(_vp)]),
             "lstm_stack_forward": (i, [_vp, _vp, sz, _vp, sz, i, i, _vp]),
             "lstm_stack_forward_host": (i, [_vp, _vp, sz, _vp, sz, i, i, _vp]),
+            "lstm_stack_forward_host_async": (i, [_vp, _vp, sz, _vp, sz, i, i, _vp]),
+            "lstm_stack_host_sync": (i, [_vp]),
             "lstm_stack_enable_phase_timing": (i, [_vp, i]),
             "lstm_stack_set_graphs": (i, [_vp, i]),
             "lstm_stack_set_math": (i, [_vp, i]),
@@ -226,6 +228,21 @@ def lstm_stack_forward_host(handle, x: np.ndarray, y: np.ndarray, batch: int, st
     assert x.flags.c_contiguous and y.flags.c_contiguous
     _check(load().lstm_stack_forward_host(handle, x.ctypes.data, x.size, y.ctypes.data, y.size,
                                           batch, steps, _stream(stream)))
+
+
+def lstm_stack_forward_host_async(handle, x: np.ndarray, y: np.ndarray, batch: int, steps: int,
+                                  stream=None):
+    """Enqueue without waiting; x must stay unchanged and y is valid only after
+    lstm_stack_host_sync.  x, y: C-contiguous float32 host arrays, pinned for
+    the copies to overlap the forward."""
+    assert x.dtype == np.float32 and y.dtype == np.float32
+    assert x.flags.c_contiguous and y.flags.c_contiguous
+    _check(load().lstm_stack_forward_host_async(handle, x.ctypes.data, x.size, y.ctypes.data,
+                                                y.size, batch, steps, _stream(stream)))
+
+
+def lstm_stack_host_sync(handle):
+    _check(load().lstm_stack_host_sync(handle))
 
 
 def lstm_stack_set_graphs(handle, enable: bool = True):

@@ -207,8 +207,20 @@ struct lstm_stack {
     float *bias[kLayers] = {};
     float *gates = nullptr;     // [max_rows][1024]
     float *ping[2] = {};        // [max_rows][256] each
-    float *x_stage = nullptr;   // [max_rows][60]   (forward_host)
-    float *y_stage = nullptr;   // [max_rows][256]  (forward_host)
+    // Host-memory entry points: two staging slots, used in turn, so that one
+    // call's output copy and the next call's input copy run while a forward
+    // computes.  Input copies run on copy_in, output copies on copy_out;
+    // per slot, `staged` marks its input copy done, `computed` its forward
+    // done, `returned` its output copy done.
+    float *x_stage[2] = {};     // [max_rows][60]
+    float *y_stage[2] = {};     // [max_rows][256]
+    cudaStream_t copy_in = nullptr;
+    cudaStream_t copy_out = nullptr;
+    cudaEvent_t staged[2] = {};
+    cudaEvent_t computed[2] = {};
+    cudaEvent_t returned[2] = {};
+    int next_slot = 0;
+    bool slot_pending[2] = {};  // enqueued since the last lstm_stack_host_sync
     ProjectionW map_w[kLayers];
     CUtensorMap map_ping[2];
     CUtensorMap map_x;
@@ -221,7 +233,7 @@ struct lstm_stack {
     bool timed_once = false;
     cudaEvent_t phase[kPhaseEvents] = {};
     unsigned *fault = nullptr;
-    unsigned *fault_host = nullptr;  // pinned copy of the fault word (forward_host)
+    unsigned *fault_host = nullptr;  // pinned [2]: the fault word after each slot's forward
     // CUDA-graph replay of the forward pass, one instantiated graph per
     // argument set (least recently used evicted)
     struct Graph {
@@ -306,10 +318,19 @@ extern "C" void lstm_stack_destroy(lstm_stack *s)
     cudaFree(s->gates);
     cudaFree(s->ping[0]);
     cudaFree(s->ping[1]);
-    cudaFree(s->x_stage);
-    cudaFree(s->y_stage);
+    for (int k = 0; k < 2; ++k) {
+        cudaFree(s->x_stage[k]);
+        cudaFree(s->y_stage[k]);
+        for (cudaEvent_t e : {s->staged[k], s->computed[k], s->returned[k]})
+            if (e)
+                cudaEventDestroy(e);
+    }
     if (s->fault_host)
         cudaFreeHost(s->fault_host);
+    if (s->copy_in)
+        cudaStreamDestroy(s->copy_in);
+    if (s->copy_out)
+        cudaStreamDestroy(s->copy_out);
     for (int l = 0; l < kLayers; ++l) {
         if (s->fork[l])
             cudaEventDestroy(s->fork[l]);
@@ -421,11 +442,14 @@ extern "C" int lstm_stack_create_ordered(const lstm_stack_weights *weights, int 
     if (st == LSTM_OK) st = alloc(&s->gates, max_rows * kGateColumns, "gate buffer");
     if (st == LSTM_OK) st = alloc(&s->ping[0], max_rows * kOutput, "layer buffer 0");
     if (st == LSTM_OK) st = alloc(&s->ping[1], max_rows * kOutput, "layer buffer 1");
-    if (st == LSTM_OK) st = alloc(&s->x_stage, max_rows * kFeatures, "input staging");
-    if (st == LSTM_OK) st = alloc(&s->y_stage, max_rows * kOutput, "output staging");
+    for (int k = 0; k < 2; ++k) {
+        if (st == LSTM_OK) st = alloc(&s->x_stage[k], max_rows * kFeatures, "input staging");
+        if (st == LSTM_OK) st = alloc(&s->y_stage[k], max_rows * kOutput, "output staging");
+    }
     if (st == LSTM_OK)
-        st = cuda_status(cudaMallocHost(reinterpret_cast<void **>(&s->fault_host), sizeof(unsigned)),
-                         "pinned fault word");
+        st = cuda_status(
+            cudaMallocHost(reinterpret_cast<void **>(&s->fault_host), 2 * sizeof(unsigned)),
+            "pinned fault words");
     if (st != LSTM_OK) {
         lstm_stack_destroy(s);
         return st;
@@ -444,6 +468,17 @@ extern "C" int lstm_stack_create_ordered(const lstm_stack_weights *weights, int 
     if (st == LSTM_OK)
         st = cuda_status(cudaStreamCreateWithFlags(&s->capture, cudaStreamNonBlocking),
                          "capture stream");
+    if (st == LSTM_OK)
+        st = cuda_status(cudaStreamCreateWithFlags(&s->copy_in, cudaStreamNonBlocking),
+                         "input copy stream");
+    if (st == LSTM_OK)
+        st = cuda_status(cudaStreamCreateWithFlags(&s->copy_out, cudaStreamNonBlocking),
+                         "output copy stream");
+    for (int k = 0; k < 2 && st == LSTM_OK; ++k) {
+        for (cudaEvent_t *e : {&s->staged[k], &s->computed[k], &s->returned[k]})
+            if (st == LSTM_OK)
+                st = cuda_status(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "event");
+    }
     for (int l = 0; l < kLayers && st == LSTM_OK; ++l) {
         st = cuda_status(cudaEventCreateWithFlags(&s->fork[l], cudaEventDisableTiming), "event");
         if (st == LSTM_OK)
@@ -647,9 +682,9 @@ extern "C" int lstm_stack_forward(lstm_stack *s, const float *x, size_t x_len, f
     return forward_replay(s, x, y, batch, steps, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_t x_len,
-                                       float *y_host, size_t y_len, int batch, int steps,
-                                       void *stream)
+extern "C" int lstm_stack_forward_host_async(lstm_stack *s, const float *x_host, size_t x_len,
+                                             float *y_host, size_t y_len, int batch, int steps,
+                                             void *stream)
 {
     int st = check_forward_args(s, x_host, x_len, y_host, y_len, batch, steps);
     if (st != LSTM_OK)
@@ -657,25 +692,65 @@ extern "C" int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_
     DeviceGuard guard(s->device);
     if (!guard.ok)
         return fail(LSTM_E_CUDA, "cannot make device %d current", s->device);
-    cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-    if ((st = cuda_status(cudaMemcpyAsync(s->x_stage, x_host, x_len * sizeof(float),
-                                          cudaMemcpyHostToDevice, st_),
-                          "input copy")))
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    if ((st = cuda_status(cudaStreamIsCapturing(cs, &capturing), "capture status")))
         return st;
-    if ((st = forward_replay(s, s->x_stage, s->y_stage, batch, steps, st_)))
+    if (capturing != cudaStreamCaptureStatusNone)
+        return fail(LSTM_E_INVALID,
+                    "forward_host_async: the stream is being captured (use lstm_stack_forward)");
+    const int k = s->next_slot;
+    // input: into slot k once the forward that last read it is done
+    if ((st = cuda_status(cudaStreamWaitEvent(s->copy_in, s->computed[k]), "event wait")) ||
+        (st = cuda_status(cudaMemcpyAsync(s->x_stage[k], x_host, x_len * sizeof(float),
+                                          cudaMemcpyHostToDevice, s->copy_in),
+                          "input copy")) ||
+        (st = cuda_status(cudaEventRecord(s->staged[k], s->copy_in), "event record")))
         return st;
-    if ((st = cuda_status(cudaMemcpyAsync(y_host, s->y_stage, y_len * sizeof(float),
-                                          cudaMemcpyDeviceToHost, st_),
-                          "output copy")))
+    // the forward: after its input copy, after the output copy that last read
+    // slot k, and after the other slot's forward (the scratch is shared)
+    if ((st = cuda_status(cudaStreamWaitEvent(cs, s->staged[k]), "event wait")) ||
+        (st = cuda_status(cudaStreamWaitEvent(cs, s->returned[k]), "event wait")) ||
+        (st = cuda_status(cudaStreamWaitEvent(cs, s->computed[k ^ 1]), "event wait")))
         return st;
-    // the kernels' fault word comes back with the result
-    if ((st = cuda_status(cudaMemcpyAsync(s->fault_host, s->fault, sizeof(unsigned),
-                                          cudaMemcpyDeviceToHost, st_),
-                          "fault word copy")))
+    if ((st = forward_replay(s, s->x_stage[k], s->y_stage[k], batch, steps, cs)))
         return st;
-    if ((st = cuda_status(cudaStreamSynchronize(st_), "forward_host synchronize")))
+    if ((st = cuda_status(cudaEventRecord(s->computed[k], cs), "event record")))
         return st;
-    if (const unsigned bits = *s->fault_host) {
+    // output, and the kernels' fault word with it
+    if ((st = cuda_status(cudaStreamWaitEvent(s->copy_out, s->computed[k]), "event wait")) ||
+        (st = cuda_status(cudaMemcpyAsync(y_host, s->y_stage[k], y_len * sizeof(float),
+                                          cudaMemcpyDeviceToHost, s->copy_out),
+                          "output copy")) ||
+        (st = cuda_status(cudaMemcpyAsync(&s->fault_host[k], s->fault, sizeof(unsigned),
+                                          cudaMemcpyDeviceToHost, s->copy_out),
+                          "fault word copy")) ||
+        (st = cuda_status(cudaEventRecord(s->returned[k], s->copy_out), "event record")))
+        return st;
+    s->slot_pending[k] = true;
+    s->next_slot = k ^ 1;
+    return LSTM_OK;
+}
+
+extern "C" int lstm_stack_host_sync(lstm_stack *s)
+{
+    if (!s)
+        return fail(LSTM_E_INVALID, "host_sync: null stack");
+    DeviceGuard guard(s->device);
+    if (!guard.ok)
+        return fail(LSTM_E_CUDA, "cannot make device %d current", s->device);
+    int st = cuda_status(cudaStreamSynchronize(s->copy_out), "output copies");
+    if (st == LSTM_OK)
+        st = cuda_status(cudaStreamSynchronize(s->copy_in), "input copies");
+    if (st != LSTM_OK)
+        return st;
+    unsigned bits = 0;
+    for (int k = 0; k < 2; ++k) {
+        if (s->slot_pending[k])
+            bits |= s->fault_host[k];
+        s->slot_pending[k] = false;
+    }
+    if (bits) {
         cudaMemset(s->fault, 0, sizeof(unsigned));
         return fail(LSTM_E_FAULT,
                     "forward_host: a kernel's bounded wait ran out (fault bits 0x%x); the "
@@ -683,6 +758,17 @@ extern "C" int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_
                     bits);
     }
     return LSTM_OK;
+}
+
+extern "C" int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_t x_len,
+                                       float *y_host, size_t y_len, int batch, int steps,
+                                       void *stream)
+{
+    const int st = lstm_stack_forward_host_async(s, x_host, x_len, y_host, y_len, batch, steps,
+                                                 stream);
+    if (st != LSTM_OK)
+        return st;
+    return lstm_stack_host_sync(s);
 }
 
 extern "C" int lstm_stack_enable_phase_timing(lstm_stack *s, int enable)

@@ -99,8 +99,9 @@ typedef struct {
 
 /* Packs the weights (lstm_pack_layer) and copies them to `device`, allocates
  * the device scratch for up to max_batch windows of up to max_steps steps
- * (gate buffer [rows][1024], two ping-pong layer buffers [rows][256], host
- * staging for lstm_stack_forward_host), creates the side stream and events.
+ * (gate buffer [rows][1024], two ping-pong layer buffers [rows][256], two
+ * staging slots [rows][60] + [rows][256] for the host-memory entry points),
+ * creates the side stream, the copy streams and the events.
  * On success *out owns all of it.  Errors: LSTM_E_INVALID (null, sizes <= 0),
  * LSTM_E_OVERFLOW (max_batch*max_steps*1024 beyond 2^31 rows*cols),
  * LSTM_E_DEVICE (device is not compute capability 10.3 or lacks cluster
@@ -145,10 +146,31 @@ int lstm_stack_create_ordered(const lstm_stack_weights *weights, int gate_order,
 int lstm_stack_forward(lstm_stack *s, const float *x, size_t x_len, float *y,
                        size_t y_len, int batch, int steps, void *stream);
 
-/* The same forward pass from and to host memory: copies x (host, x_len
- * floats) into the stack's device staging buffer on `stream`, runs
- * lstm_stack_forward, copies the result back into y (host, y_len floats) and
- * waits for `stream` before returning, so y is ready on return. */
+/* The same forward pass from and to host memory, without waiting for it:
+ * copies x (host, x_len floats) into one of the stack's two device staging
+ * slots on an internal input-copy stream, runs the forward on `stream`, and
+ * copies the result into y (host, y_len floats) on an internal output-copy
+ * stream.  Consecutive calls use the two slots in turn, so one call's output
+ * copy and the next call's input copy overlap the next forward; a call
+ * reuses a slot only after that slot's previous output copy, and starts its
+ * forward only after the previous call's forward (the stack's scratch is
+ * shared).  x must stay unchanged until the call's input copy is done and y
+ * is valid after lstm_stack_host_sync; both should be page-locked (pinned)
+ * for the copies to be asynchronous.  Not for a stream being captured
+ * (LSTM_E_INVALID; capture lstm_stack_forward instead).  Errors: those of
+ * lstm_stack_forward, LSTM_E_INVALID for a capturing stream. */
+int lstm_stack_forward_host_async(lstm_stack *s, const float *x_host, size_t x_len,
+                                  float *y_host, size_t y_len, int batch,
+                                  int steps, void *stream);
+
+/* Waits for every lstm_stack_forward_host_async call enqueued so far (their
+ * output copies, hence their forwards).  Returns LSTM_E_FAULT if a kernel of
+ * one of them reported a bounded wait that ran out (the results are not
+ * valid; the fault word is cleared), else LSTM_OK or LSTM_E_CUDA. */
+int lstm_stack_host_sync(lstm_stack *s);
+
+/* lstm_stack_forward_host_async followed by lstm_stack_host_sync: y is ready
+ * on return (LSTM_E_FAULT as there). */
 int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_t x_len,
                             float *y_host, size_t y_len, int batch, int steps,
                             void *stream);

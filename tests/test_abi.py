@@ -47,6 +47,13 @@ def test_forward_rejects_null_stack(lib):
     assert "null" in binding.lstm_stack_last_error()
 
 
+def test_host_entry_points_reject_null_stack(lib):
+    for fn in (lib.lstm_stack_forward_host, lib.lstm_stack_forward_host_async):
+        assert fn(None, None, 0, None, 0, 1, 1, None) == binding.LSTM_E_INVALID
+        assert "null" in binding.lstm_stack_last_error()
+    assert lib.lstm_stack_host_sync(None) == binding.LSTM_E_INVALID
+
+
 def test_create_rejects_null_weights(lib):
     h = ctypes.c_void_p()
     assert lib.lstm_stack_create(None, 1, 1, 0, ctypes.byref(h)) == binding.LSTM_E_INVALID

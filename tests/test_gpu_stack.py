@@ -75,6 +75,40 @@ def test_stack_is_deterministic_and_host_path_matches(stack):
     assert np.array_equal(y1.view(np.uint32), yh.view(np.uint32))
 
 
+def test_async_host_calls_in_flight(stack, layers):
+    # five calls in a row, different shapes and inputs, results collected at
+    # the end: the staging slots are reused (calls 3-5) while earlier output
+    # copies may still be in flight; every output equals the device path
+    import torch
+    shapes = [(3, 40), (5, 17), (2, 64), (4, 33), (1, 9)]
+    xs = [synthetic.random_matrix(300 + i, (b, t, 60)) for i, (b, t) in enumerate(shapes)]
+    xp = [torch.from_numpy(x).pin_memory() for x in xs]
+    yp = [torch.full((b, t, 256), float("nan")).pin_memory() for b, t in shapes]
+    for (b, t), xi, yi in zip(shapes, xp, yp):
+        binding.lstm_stack_forward_host_async(stack.handle, xi.numpy(), yi.numpy(), b, t)
+    binding.lstm_stack_host_sync(stack.handle)
+    for x, yi in zip(xs, yp):
+        ref = _forward(stack, x)
+        assert np.array_equal(ref.view(np.uint32), yi.numpy().view(np.uint32))
+    assert_within(yp[0].numpy(), oracle.lstm_stack(xs[0], layers), what="async host call")
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
+def test_async_host_call_rejects_a_capturing_stream(stack):
+    import torch
+    x = np.zeros((1, 4, 60), np.float32)
+    y = np.zeros((1, 4, 256), np.float32)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(binding.LSTMError) as e:
+        with torch.cuda.graph(g, stream=s):
+            binding.lstm_stack_forward_host_async(stack.handle, x, y, 1, 4, s)
+    assert e.value.code == binding.LSTM_E_INVALID
+    torch.cuda.synchronize()
+    # the stack still works afterwards
+    binding.lstm_stack_forward_host(stack.handle, x, y, 1, 4)
+
+
 def test_stack_phase_timing(stack):
     import torch
     x = cuda(synthetic.stack_input(synthetic.WORKLOADS["b1_t64"]))
