@@ -183,17 +183,16 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     const int u = static_cast<int>(rank) * U + ul;  // this thread's hidden unit
     const int wbase = wg * LW;                      // this slot's first window in the tile
     const int u0 = u & ~3;                          // first of the warp's four units
-    // windows of this tile inside the batch; padding windows are computed but
-    // their h is neither sent nor stored
-    // bytes of one step's h per barrier: the tile's windows inside the batch
-    // (chunk ch of every window group of the tile when chunk-major)
+    // Padding windows (past the batch) are computed, but their h is neither
+    // sent nor stored.  Bytes of one step's h per barrier: the tile's windows
+    // inside the batch (chunk ch of every window group when chunk-major).
     uint32_t bar_bytes[NBAR];
     if constexpr (CM) {
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
             int n = 0;
-            for (int g = 0; g < SPU; ++g)
-                n += max(0, min(NW, batch - (tile * TW + g * LW + ch * NW)));
+            for (int grp = 0; grp < SPU; ++grp)
+                n += max(0, min(NW, batch - (tile * TW + grp * LW + ch * NW)));
             bar_bytes[ch] = static_cast<uint32_t>(kHidden * n * 4);
         }
     } else {
