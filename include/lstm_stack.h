@@ -156,7 +156,9 @@ int lstm_stack_forward(lstm_stack *s, const float *x, size_t x_len, float *y,
  * forward only after the previous call's forward (the stack's scratch is
  * shared).  x must stay unchanged until the call's input copy is done and y
  * is valid after lstm_stack_host_sync; both should be page-locked (pinned)
- * for the copies to be asynchronous.  Not for a stream being captured
+ * for the copies to be asynchronous.  As with lstm_stack_forward, calls on
+ * one stack object must not overlap in time on the host.  Not for a stream
+ * being captured
  * (LSTM_E_INVALID; capture lstm_stack_forward instead).  Errors: those of
  * lstm_stack_forward, LSTM_E_INVALID for a capturing stream. */
 int lstm_stack_forward_host_async(lstm_stack *s, const float *x_host, size_t x_len,
