@@ -147,7 +147,13 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     constexpr int V = 4 * NW;            // partial sums per thread and chunk
     constexpr int HV = V >= 8 ? V / 8 : 1;  // values a lane holds after the reduction
     constexpr int REPL = V >= 8 ? 4 / HV : 8;  // lanes holding one window's cell
-    constexpr int PFD = NCH >= 4 ? 2 : PF;     // projection prefetch depth (steps)
+    // Projection prefetch depth (steps).  Measured per step (GB300,
+    // T = 589) against 4 steps ahead: 8 is 2 % faster at one window per chunk
+    // (at 32 windows; 2 steps is 8 % slower there), 1-2 % with 4 windows in
+    // one chunk, 4.5 % with two chunks of 2; it was 1 % slower with one chunk
+    // of 2 and 4 % slower chunk-major.  Four or more chunks: 2 (registers).
+    constexpr bool DEEP = NW == 1 || (NW == 4 && NCH == 1) || (NW == 2 && NCH == 2);
+    constexpr int PFD = NCH >= 4 ? 2 : (DEEP ? 2 * PF : PF);
     // Select-free butterfly (lane-dependent order of the partial sums) for
     // one window per chunk and for eight: measured faster there (GB300,
     // T = 589: 0.45 -> 0.40 us per step at one window, 2.61 -> 2.54 at 256
@@ -672,11 +678,11 @@ int max_active_clusters(const Variant &v, int *out);
 // (for both directions) as the device runs at once
 // (cudaOccupancyMaxActiveClusters, queried per device) and the full-load
 // step times are measured with both directions running (GB300, T = 589, us):
-//   narrow clusters of 8, 128 threads, one window per cluster      0.58
+//   narrow clusters of 8, 128 threads, one window per cluster      0.57
 //   the same with 2 windows per group                             0.73
 //   clusters of 4, one window per group                           0.58
-//   clusters of 4, 2 chunks of 2 windows per lane                 0.94
-//   narrow clusters of 8, 4 windows per group                     1.12
+//   clusters of 4, 2 chunks of 2 windows per lane                 0.90
+//   narrow clusters of 8, 4 windows per group                     1.10
 //   clusters of 4, 2 chunks of 4 windows (chunk-major)            1.33
 //   clusters of 4, 2 chunks of 8 windows (chunk-major)            2.22
 // (more windows per chunk: fewer gather shuffles per window and more
@@ -689,9 +695,9 @@ const Variant *choose_variant(int batch)
         int cluster, nw, nch, threads;
         float us_per_step;  // full load
     };
-    static const Candidate cand[] = {{8, 1, 1, 128, 0.58f}, {8, 2, 1, 128, 0.73f},
-                                     {4, 1, 1, 0, 0.58f},   {4, 2, 2, 0, 0.94f},
-                                     {8, 4, 1, 128, 1.12f}, {4, 4, 2, 0, 1.33f},
+    static const Candidate cand[] = {{8, 1, 1, 128, 0.57f}, {8, 2, 1, 128, 0.73f},
+                                     {4, 1, 1, 0, 0.58f},   {4, 2, 2, 0, 0.90f},
+                                     {8, 4, 1, 128, 1.10f}, {4, 4, 2, 0, 1.33f},
                                      {4, 8, 2, 0, 2.22f}};
     constexpr int N = sizeof(cand) / sizeof(cand[0]);
     static std::mutex mu;
