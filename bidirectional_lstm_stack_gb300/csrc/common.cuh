@@ -395,6 +395,28 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
                  : "memory");
     return ok != 0;
 }
+// Asynchronous 4-byte copy from global memory into this CTA's shared memory:
+// `bytes` = 4, or 0 to zero the word without reading the source.  Copies of
+// one thread complete in the order of their commit groups.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_arrive_release()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
