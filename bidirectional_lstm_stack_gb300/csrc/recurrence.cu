@@ -147,11 +147,15 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     constexpr int V = 4 * NW;            // partial sums per thread and chunk
     constexpr int HV = V >= 8 ? V / 8 : 1;  // values a lane holds after the reduction
     constexpr int REPL = V >= 8 ? 4 / HV : 8;  // lanes holding one window's cell
-    // Projection prefetch depth (steps).  Measured per step (GB300,
-    // T = 589) against 4 steps ahead: 8 is 2 % faster at one window per chunk
-    // (at 32 windows; 2 steps is 8 % slower there), 1-2 % with 4 windows in
-    // one chunk, 4.5 % with two chunks of 2; it was 1 % slower with one chunk
-    // of 2 and 4 % slower chunk-major.  Four or more chunks: 2 (registers).
+    // Steps per unrolled group (the buffer parity and the prefetch slot are
+    // compile-time within it), and the depth of the register ring of
+    // projection values where that ring is used (see SRING below).  Measured
+    // per step (GB300, T = 589) with the register ring, against 4 steps
+    // ahead: 8 is 2 % faster at one window per chunk (2 steps: 8 % slower),
+    // 1-2 % with 4 windows in one chunk, 4.5 % with two chunks of 2; it was
+    // 1 % slower with one chunk of 2 and 4 % slower chunk-major.  Four or more
+    // chunks: 2 (registers).  The shared-memory ring variants keep these
+    // group lengths (one window: 8 measured better than 4 there too).
     constexpr bool DEEP = NW == 1 || (NW == 4 && NCH == 1) || (NW == 2 && NCH == 2);
     constexpr int PFD = NCH >= 4 ? 2 : (DEEP ? 2 * PF : PF);
     // Select-free butterfly (lane-dependent order of the partial sums) for
@@ -171,19 +175,22 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     // chunks (the phases of one small chunk leave too little independent
     // work; four chunks of 4 windows: 4 % slower).
     constexpr bool CM = NCH == 2 && NW >= 4;
-    // One window in one chunk: the projection values travel through a ring
-    // in shared memory, filled by each lane's own asynchronous copies GD
-    // steps ahead (no registers held for the values in flight; measured per
-    // step against the register ring 8 steps ahead: 4 % faster at one window,
-    // 1.5 % at 32); otherwise through a register ring PFD steps ahead.
-    constexpr bool SRING = NW == 1 && NCH == 1;
-    constexpr int GD = THREADS <= 128 ? 32 : 16;
+    // One projection value per lane and chunk, at most two chunks: the values
+    // travel through a ring in shared memory (at most 32 KiB), filled by each
+    // lane's own asynchronous copies GD steps ahead (no registers held for
+    // the values in flight; measured per step against the register ring 8
+    // steps ahead: 4 % faster at one window, 1.5 % at 32 windows; with two
+    // windows per chunk 5.5 % faster than 4 or 8 steps ahead); otherwise
+    // through a register ring PFD steps ahead.
+    constexpr bool SRING = HV == 1 && NCH <= 2;
+    constexpr int GD_FIT = 32768 / (NCH * THREADS * 4);  // ring of at most 32 KiB
+    constexpr int GD = GD_FIT >= 64 ? 64 : GD_FIT >= 32 ? 32 : 16;
     constexpr int NBAR = CM ? NCH : 1;
 
     __shared__ __align__(16) float hbuf[2][TW][HROW];
     __shared__ __align__(8) uint64_t hbar[2][NBAR];
     __shared__ int abort_flag;
-    __shared__ __align__(16) float gring[SRING ? GD : 1][SRING ? THREADS : 1];
+    __shared__ __align__(16) float gring[SRING ? GD : 1][SRING ? NCH : 1][SRING ? THREADS : 1];
 
     const int tid = threadIdx.x;
     const int kc = tid & 7;
@@ -346,12 +353,15 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             }
         }
     };
-    // projection value of step s into ring slot s % GD (one window, one chunk)
+    // projection values of step s (one per chunk) into ring slot s % GD
     auto gissue = [&](int s) {
         const long t = direction ? steps - 1 - s : s;
-        const bool ok = bch0 + wv[0] < batch && s < steps;
-        const float *src = ok ? gch0[0] + t * kGateColumns : g;
-        ptx::cp_async_4(ptx::smem_u32(&gring[s & (GD - 1)][tid]), src, ok ? 4u : 0u);
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            const bool ok = bch0 + ch * NW + wv[0] < batch && s < steps;
+            const float *src = ok ? gch0[0] + (ch * row_stride + t) * kGateColumns : g;
+            ptx::cp_async_4(ptx::smem_u32(&gring[s & (GD - 1)][ch][tid]), src, ok ? 4u : 0u);
+        }
         ptx::cp_async_commit();
     };
     if constexpr (SRING) {
@@ -485,7 +495,9 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
         float gcur[NCH][HV];
         if constexpr (SRING) {
             ptx::cp_async_wait<GD - 1>();  // the copy issued GD steps ago
-            gcur[0][0] = gring[s & (GD - 1)][tid];
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+                gcur[ch][0] = gring[s & (GD - 1)][ch][tid];
         } else {
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch)
@@ -717,9 +729,9 @@ int max_active_clusters(const Variant &v, int *out);
 // (cudaOccupancyMaxActiveClusters, queried per device) and the full-load
 // step times are measured with both directions running (GB300, T = 589, us):
 //   narrow clusters of 8, 128 threads, one window per cluster      0.57
-//   the same with 2 windows per group                             0.73
+//   the same with 2 windows per group                             0.70
 //   clusters of 4, one window per group                           0.58
-//   clusters of 4, 2 chunks of 2 windows per lane                 0.90
+//   clusters of 4, 2 chunks of 2 windows per lane                 0.85
 //   narrow clusters of 8, 4 windows per group                     1.10
 //   clusters of 4, 2 chunks of 4 windows (chunk-major)            1.33
 //   clusters of 4, 2 chunks of 8 windows (chunk-major)            2.22
@@ -733,8 +745,8 @@ const Variant *choose_variant(int batch)
         int cluster, nw, nch, threads;
         float us_per_step;  // full load
     };
-    static const Candidate cand[] = {{8, 1, 1, 128, 0.57f}, {8, 2, 1, 128, 0.73f},
-                                     {4, 1, 1, 0, 0.58f},   {4, 2, 2, 0, 0.90f},
+    static const Candidate cand[] = {{8, 1, 1, 128, 0.57f}, {8, 2, 1, 128, 0.70f},
+                                     {4, 1, 1, 0, 0.58f},   {4, 2, 2, 0, 0.85f},
                                      {8, 4, 1, 128, 1.10f}, {4, 4, 2, 0, 1.33f},
                                      {4, 8, 2, 0, 2.22f}};
     constexpr int N = sizeof(cand) / sizeof(cand[0]);
