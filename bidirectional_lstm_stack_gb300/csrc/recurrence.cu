@@ -175,22 +175,28 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
     // chunks (the phases of one small chunk leave too little independent
     // work; four chunks of 4 windows: 4 % slower).
     constexpr bool CM = NCH == 2 && NW >= 4;
-    // One projection value per lane and chunk, at most two chunks: the values
-    // travel through a ring in shared memory (at most 32 KiB), filled by each
-    // lane's own asynchronous copies GD steps ahead (no registers held for
-    // the values in flight; measured per step against the register ring 8
-    // steps ahead: 4 % faster at one window, 1.5 % at 32 windows; with two
-    // windows per chunk 5.5 % faster than 4 or 8 steps ahead); otherwise
-    // through a register ring PFD steps ahead.
-    constexpr bool SRING = HV == 1 && NCH <= 2;
-    constexpr int GD_FIT = 32768 / (NCH * THREADS * 4);  // ring of at most 32 KiB
-    constexpr int GD = GD_FIT >= 64 ? 64 : GD_FIT >= 32 ? 32 : 16;
+    // At most two chunks, where at least 4 steps fit: the projection values
+    // travel through a ring in shared memory, filled by each lane's own
+    // asynchronous copies GD steps ahead (no registers held for the values
+    // in flight; measured per step against the register ring 8 steps ahead:
+    // 4 % faster at one window, 1.5 % at 32 windows; with two windows per
+    // chunk 5.5 % faster than 4 or 8 steps ahead); otherwise through a
+    // register ring PFD steps ahead.  GD_FIT: ring slots that fit beside the
+    // h buffers in 44 KiB of static shared memory (the static limit is
+    // 48 KiB).
+    constexpr int GD_FIT = (45056 - 2 * TW * HROW * 4) / (NCH * HV * THREADS * 4);
+    constexpr int GD = GD_FIT >= 64   ? 64
+                       : GD_FIT >= 32 ? 32
+                       : GD_FIT >= 16 ? 16
+                       : GD_FIT >= 8  ? 8
+                                      : 4;
+    constexpr bool SRING = NCH <= 2 && GD_FIT >= 4;
     constexpr int NBAR = CM ? NCH : 1;
 
     __shared__ __align__(16) float hbuf[2][TW][HROW];
     __shared__ __align__(8) uint64_t hbar[2][NBAR];
     __shared__ int abort_flag;
-    __shared__ __align__(16) float gring[SRING ? GD : 1][SRING ? NCH : 1][SRING ? THREADS : 1];
+    __shared__ __align__(16) float gring[SRING ? GD : 1][SRING ? NCH * HV : 1][SRING ? THREADS : 1];
 
     const int tid = threadIdx.x;
     const int kc = tid & 7;
@@ -358,9 +364,13 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
         const long t = direction ? steps - 1 - s : s;
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
-            const bool ok = bch0 + ch * NW + wv[0] < batch && s < steps;
-            const float *src = ok ? gch0[0] + (ch * row_stride + t) * kGateColumns : g;
-            ptx::cp_async_4(ptx::smem_u32(&gring[s & (GD - 1)][ch][tid]), src, ok ? 4u : 0u);
+#pragma unroll
+            for (int v = 0; v < HV; ++v) {
+                const bool ok = bch0 + ch * NW + wv[v] < batch && s < steps;
+                const float *src = ok ? gch0[v] + (ch * row_stride + t) * kGateColumns : g;
+                ptx::cp_async_4(ptx::smem_u32(&gring[s & (GD - 1)][ch * HV + v][tid]), src,
+                                ok ? 4u : 0u);
+            }
         }
         ptx::cp_async_commit();
     };
@@ -497,7 +507,9 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             ptx::cp_async_wait<GD - 1>();  // the copy issued GD steps ago
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch)
-                gcur[ch][0] = gring[s & (GD - 1)][ch][tid];
+#pragma unroll
+                for (int v = 0; v < HV; ++v)
+                    gcur[ch][v] = gring[s & (GD - 1)][ch * HV + v][tid];
         } else {
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch)
