@@ -852,7 +852,8 @@ int recurrence_args(const float *g, const float *rp, const float *bias, float *y
         return fail(LSTM_E_OVERFLOW, "lstm_recurrence: %d x %d rows exceed %ld", batch, steps,
                     65535L * 128);
     int st;
-    if ((st = check_aligned(rp, "rp")) || (st = pointer_device(g, dev)))
+    if ((st = check_aligned(g, "g")) || (st = check_aligned(rp, "rp")) ||
+        (st = check_aligned(y, "y")) || (st = pointer_device(g, dev)))
         return st;
     return prepare_device(*dev);
 }

@@ -267,8 +267,10 @@ int lstm_projection_math(const float *x, int rows, int in_width,
  * h and c start at zero for every window.  One thread-block cluster holds R
  * in its blocks' registers, split by hidden unit, and exchanges h through
  * distributed shared memory each step; the variant (cluster shape and
- * windows per cluster) is chosen from the batch size.  Errors: LSTM_E_INVALID,
- * LSTM_E_OVERFLOW, LSTM_E_DEVICE, LSTM_E_CUDA. */
+ * windows per cluster) is chosen from the batch size.  g, rp and y must be
+ * 16-byte aligned (h is stored four units at a time).  Errors:
+ * LSTM_E_INVALID (null, sizes, direction, alignment), LSTM_E_OVERFLOW,
+ * LSTM_E_DEVICE, LSTM_E_CUDA. */
 int lstm_recurrence(const float *g, const float *rp, const float *bias,
                     float *y, int batch, int steps, int direction,
                     void *stream);

@@ -76,6 +76,15 @@ def test_step_entry_points_reject_bad_arguments(lib):
     assert lib.lstm_fault_status(None) == binding.LSTM_E_INVALID
 
 
+def test_recurrence_rejects_unaligned_buffers(lib):
+    # checked on the host before any device call: g and y (h goes out four
+    # units at a time) must be 16-byte aligned, like rp
+    assert lib.lstm_recurrence(4, 16, 16, 16, 1, 1, 0, None) == binding.LSTM_E_INVALID
+    assert "g (" in binding.lstm_stack_last_error()
+    assert lib.lstm_recurrence(16, 16, 16, 20, 1, 1, 0, None) == binding.LSTM_E_INVALID
+    assert "y (" in binding.lstm_stack_last_error()
+
+
 def test_destroy_null_is_a_noop(lib):
     lib.lstm_stack_destroy(None)
 
