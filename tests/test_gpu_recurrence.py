@@ -117,6 +117,19 @@ def test_unknown_variant_is_rejected():
     assert e.value.code == binding.LSTM_E_INVALID
 
 
+@pytest.mark.parametrize("variant,batch", [((8, 1, 1, 128), 32), ((8, 2, 1, 128), 48),
+                                           ((4, 2, 2, 0), 64), ((8, 4, 1, 128), 80),
+                                           ((4, 4, 2, 0), 128), ((4, 8, 2, 0), 256)])
+def test_chosen_variants_run_in_one_wave(variant, batch):
+    # the batch sizes each variant is chosen for fit on the GPU at once, both
+    # directions together (more registers or shared memory per CTA would
+    # silently split them into two waves)
+    c, nw, nch, threads = variant
+    tile = ((threads or 256) // 8) // (128 // c) * nw * nch
+    need = 2 * -(-batch // tile)
+    assert binding.lstm_recurrence_max_clusters(*variant) >= need, (variant, need)
+
+
 def test_max_clusters_query():
     for v in VARIANTS:
         n = binding.lstm_recurrence_max_clusters(*v)
