@@ -51,9 +51,6 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # nominal dense rates (per GPU) used to scale the measured bf16 peak to TF32
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_TF32_TFLOPS = 1100.0
-# tcgen05 kind::tf32 rate measured on this GPU model by a microbenchmark
-# (back-to-back M128 N256 K8 MMAs on every SM: 128 cycles each), TF/s
-TF32_MICROBENCHMARK_TFLOPS = 1210.0
 # FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop per FMA at the SM clock
 SMS = 152
 FP32_LANES = 128
@@ -113,6 +110,66 @@ def time_heads(heads, y, steps, warmup, flush, stream):
             ends[i].record(stream)
     torch.cuda.synchronize()
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def time_recurrence_pair(fn, g, rp, bias, y, batch, steps, reps, warmup, flush, stream, side):
+    """Per-step device time (us) of one layer's two recurrences (forward on
+    `stream`, reverse on `side`, started together and joined, as the stack
+    runs them), through `fn` (lstm_recurrence or lstm_recurrence_floor), L2
+    flushed before each pair; the median over `reps` pairs."""
+    import torch
+
+    def pair():
+        fn(g, rp[0], bias[0], y, batch, steps, 0, stream)
+        fn(g, rp[1], bias[1], y, batch, steps, 1, side)
+
+    times = []
+    for i in range(warmup + reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        joined = torch.cuda.Event()
+        with torch.cuda.stream(stream):
+            flush.fill_(i)
+            e0.record(stream)
+        side.wait_event(e0)
+        pair()
+        joined.record(side)
+        stream.wait_event(joined)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= warmup:
+            times.append(e0.elapsed_time(e1) * 1e3 / steps)
+    return float(np.median(times))
+
+
+def recurrence_floor(layer, x, stream, side, flush, reps=5, warmup=3):
+    """The recurrence's per-step time and its latency floor on the same
+    launch shape, both directions running together: the layer's projection
+    of x feeds both; the floor is lstm_recurrence_floor (the same kernel with
+    the step's arithmetic replaced by a trivial dependence on the received h).
+    Returns (full us/step, floor us/step)."""
+    import torch
+    from bidirectional_lstm_stack_gb300 import binding
+    B, T, F = x.shape
+    kp = (F + 31) // 32 * 32
+    wp_hi, wp_lo, rp, bias = binding.lstm_pack_layer(layer["w"], layer["r"], layer["b"], F, kp)
+    dev = x.device
+    whi, wlo = torch.from_numpy(wp_hi).to(dev), torch.from_numpy(wp_lo).to(dev)
+    rp_d, bias_d = torch.from_numpy(rp).to(dev), torch.from_numpy(bias).to(dev)
+    g = torch.empty((B * T, 1024), device=dev)
+    y = torch.empty((B, T, 2 * H), device=dev)
+    binding.lstm_projection(x, B * T, F, whi, wlo, kp, g, stream)
+    torch.cuda.synchronize()
+    full = time_recurrence_pair(binding.lstm_recurrence, g, rp_d, bias_d, y, B, T, reps, warmup,
+                                flush, stream, side)
+    floor = time_recurrence_pair(binding.lstm_recurrence_floor, g, rp_d, bias_d, y, B, T, reps,
+                                 warmup, flush, stream, side)
+    # the floor's outputs are meaningless, but no wait of either kernel may
+    # have run out (that would void both times)
+    bits = binding.lstm_fault_status()
+    if bits:
+        raise RuntimeError(f"recurrence floor measurement: fault bits {bits:#x}")
+    return full, floor
 
 
 def flops_recurrence_launch(batch: int, steps: int) -> float:
@@ -201,7 +258,7 @@ def run_reference(args):
     wl = synthetic.WORKLOADS[args.workload]
     layers = synthetic.stack_weights()
     x = synthetic.stack_input(wl)
-    sample = min(wl.batch, args.reference_windows)
+    sample = min(wl.batch, args.reference_windows or wl.batch)
     xs = x[:sample]
     for _ in range(args.warmup):
         oracle.lstm_stack(xs[:1], layers)
@@ -350,6 +407,15 @@ def run_ours(args):
     heads.close()
     heads_ms = float(np.mean(ms_h))
 
+    # the recurrence against its latency floor (same kernel and launch shape,
+    # the step's arithmetic removed), both directions together, on the
+    # workload and on the one-window latency case; and the tensor cores'
+    # measured kind::tf32 rate, the projection's and the heads' denominator
+    side = torch.cuda.Stream()
+    rec_full_us, rec_floor_us = recurrence_floor(layers[0], x, stream, side, flush)
+    rec1_full_us, rec1_floor_us = recurrence_floor(layers[0], x1, stream, side, flush)
+    tf32_rate = binding.lstm_tf32_rate(dev)
+
     # end to end through the host-buffer entry point (pinned host memory)
     xp = torch.from_numpy(x_host).pin_memory()
     yp = torch.empty((wl.batch, wl.steps, 2 * H), dtype=torch.float32).pin_memory()
@@ -427,6 +493,9 @@ def run_ours(args):
                                      "recurrence_rev": [round(float(v), 4) for v in ph1[:, 2]]},
                        "gaps_ms": ph1_total - float(np.sum(ph1[:, 0]) +
                                                    np.sum(np.maximum(ph1[:, 1], ph1[:, 2]))),
+                       "recurrence_pair_us_per_step": rec1_full_us,
+                       "floor_us_per_step": rec1_floor_us,
+                       "vs_floor": rec1_full_us / rec1_floor_us,
                        "context": "pages: A100, TF32-projection stack, 3.21-4.13 ms per window"},
         "gaps_ms": phases_total - float(np.sum(phases[:, 0]) +
                                         np.sum(np.maximum(phases[:, 1], phases[:, 2]))),
@@ -440,7 +509,13 @@ def run_ours(args):
                      "traffic": ncu_traffic("recurrence", wl.batch * wl.steps),
                      "algorithmic_bytes": float(wl.batch * wl.steps * (512 + 128) * 4),
                      "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock",
-                     "us_per_step": rec_us_per_step},
+                     "us_per_step": rec_us_per_step,
+                     "pair_us_per_step": rec_full_us,
+                     "floor_us_per_step": rec_floor_us,
+                     "vs_floor": rec_full_us / rec_floor_us,
+                     "floor_source": "lstm_recurrence_floor: the same variant, grid, exchange "
+                                     "and waits with the step's arithmetic removed; both "
+                                     "directions together, L2 flushed, median of 5"},
         "roofline_projection": {"kernel": "projection (one layer, both directions)",
                                 "bound": "tensor", "achieved": proj_achieved, "peak": proj_peak,
                                 "unit": "TFLOP/s", "frac": proj_achieved / proj_peak,
@@ -448,8 +523,8 @@ def run_ours(args):
                                 "peak_source": f"{peak_kind} bf16 burst {p['bf16_tflops']} x "
                                                f"{NOMINAL_TF32_TFLOPS}/{NOMINAL_BF16_TFLOPS} "
                                                f"(TF32) / 3 (3xTF32)",
-                                "frac_of_tf32_microbenchmark":
-                                    proj_achieved / (TF32_MICROBENCHMARK_TFLOPS / 3.0)},
+                                "tf32_measured_tflops": tf32_rate,
+                                "frac_of_measured_tf32": proj_achieved / (tf32_rate / 3.0)},
         "tf32_mode": {"windows_per_s": wl.batch * world * args.steps / tf32_s,
                       "ms_per_step": tf32_s * 1e3 / args.steps,
                       "projection_ms": [round(float(v), 4) for v in ph_t[:, 0]]},
@@ -457,7 +532,9 @@ def run_ours(args):
                   "rows": wl.batch * wl.steps, "ms": heads_ms,
                   "achieved_tflops": flops_heads(wl.batch * wl.steps) / (heads_ms * 1e-3) / 1e12,
                   "frac_of_3xtf32_peak": flops_heads(wl.batch * wl.steps) / (heads_ms * 1e-3)
-                  / 1e12 / proj_peak},
+                  / 1e12 / proj_peak,
+                  "frac_of_measured_3xtf32": flops_heads(wl.batch * wl.steps) / (heads_ms * 1e-3)
+                  / 1e12 / (tf32_rate / 3.0)},
         "e2e": {"value": e2e_value, "unit": "windows/s",
                 "h2d_bytes_per_step": int(xn.nbytes), "d2h_bytes_per_step": int(yn.nbytes),
                 "mode": "forward_host_async, steps enqueued back to back (copies of one step "
@@ -483,8 +560,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synthetic.WORKLOADS))
-    ap.add_argument("--reference-windows", type=int, default=16,
-                    help="windows per step of the --impl reference run")
+    ap.add_argument("--reference-windows", type=int, default=0,
+                    help="windows per step of the --impl reference run (default: the "
+                         "workload's whole batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -96,6 +96,10 @@ def load():
             "lstm_test_fail_allocations": (i, [i, i]),
             "lstm_test_fail_launches": (i, [i, i]),
             "lstm_test_recurrence_timeout": (i, [i, ctypes.c_uint, i]),
+            "lstm_test_projection_timeout": (i, [i, ctypes.c_uint, i]),
+            "lstm_test_heads_timeout": (i, [i, ctypes.c_uint, i]),
+            "lstm_recurrence_floor": (i, [_vp, _vp, _vp, _vp, i, i, i, _vp]),
+            "lstm_tf32_rate": (i, [i, i, ctypes.POINTER(ctypes.c_double)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -163,6 +167,17 @@ def lstm_projection_math(x, rows: int, in_width: int, wp_hi, wp_lo, kp: int, g, 
 def lstm_recurrence(g, rp, bias, y, batch: int, steps: int, direction: int, stream=None):
     _check(load().lstm_recurrence(_ptr(g), _ptr(rp), _ptr(bias), _ptr(y), batch, steps,
                                   direction, _stream(stream, g.device)))
+
+
+def lstm_recurrence_floor(g, rp, bias, y, batch: int, steps: int, direction: int, stream=None):
+    _check(load().lstm_recurrence_floor(_ptr(g), _ptr(rp), _ptr(bias), _ptr(y), batch, steps,
+                                        direction, _stream(stream, g.device)))
+
+
+def lstm_tf32_rate(device: int = 0, iterations: int = 20000) -> float:
+    v = ctypes.c_double(0.0)
+    _check(load().lstm_tf32_rate(device, iterations, ctypes.byref(v)))
+    return float(v.value)
 
 
 def lstm_recurrence_variant(g, rp, bias, y, batch: int, steps: int, direction: int,

@@ -91,6 +91,43 @@ int check_launch_injection(const char *what)
     return LSTM_OK;
 }
 
+namespace {
+KernelTest g_kernel_test[kTestKernels][64];
+}  // namespace
+
+KernelTest kernel_test(int kernel)
+{
+    int dev = 0;
+    if (kernel < 0 || kernel >= kTestKernels || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
+        dev >= 64)
+        return KernelTest{};
+    return g_kernel_test[kernel][dev];
+}
+
+int set_kernel_test(int kernel, int withhold, unsigned long long wait_limit_ns)
+{
+    int dev = 0;
+    int st = cuda_status(cudaGetDevice(&dev), "current device");
+    if (st != LSTM_OK)
+        return st;
+    if (kernel < 0 || kernel >= kTestKernels || dev < 0 || dev >= 64)
+        return fail(LSTM_E_INVALID, "test setting: kernel %d, device %d out of range", kernel, dev);
+    g_kernel_test[kernel][dev].wait_limit_ns = wait_limit_ns;
+    g_kernel_test[kernel][dev].withhold = withhold;
+    return LSTM_OK;
+}
+
+bool kernel_test_active(int device)
+{
+    if (device < 0 || device >= 64)
+        return false;
+    for (int k = 0; k < kTestKernels; ++k)
+        if (g_kernel_test[k][device].withhold ||
+            g_kernel_test[k][device].wait_limit_ns != kDefaultWaitLimitNs)
+            return true;
+    return false;
+}
+
 unsigned *fault_word()
 {
     // one address per device; resolved with that device current
@@ -599,7 +636,7 @@ int forward_replay(lstm_stack *s, const float *x, float *y, int batch, int steps
     int st = cuda_status(cudaStreamIsCapturing(stream, &cs), "stream capture status");
     if (st != LSTM_OK)
         return st;
-    if (!s->use_graphs || cs != cudaStreamCaptureStatusNone || recurrence_test_active(s->device))
+    if (!s->use_graphs || cs != cudaStreamCaptureStatusNone || kernel_test_active(s->device))
         return forward_device(s, x, y, batch, steps, stream);
     lstm_stack::Graph *hit = nullptr, *victim = &s->graphs[0];
     for (auto &gr : s->graphs) {
@@ -874,6 +911,21 @@ extern "C" int lstm_recurrence(const float *g, const float *rp, const float *bia
                              static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int lstm_recurrence_floor(const float *g, const float *rp, const float *bias, float *y,
+                                     int batch, int steps, int direction, void *stream)
+{
+    int dev = 0;
+    int st = recurrence_args(g, rp, bias, y, batch, steps, direction, &dev);
+    if (st != LSTM_OK)
+        return st;
+    DeviceGuard guard(dev);
+    unsigned *fault = fault_word();
+    if (!fault)
+        return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
+    return launch_recurrence_floor(g, rp, bias, y, batch, steps, direction, fault,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
                                        float *y, int batch, int steps, int direction,
                                        int cluster_size, int windows_per_chunk, int chunks,
@@ -934,10 +986,12 @@ extern "C" int lstm_test_fail_launches(int skip, int count)
     return LSTM_OK;
 }
 
-extern "C" int lstm_test_recurrence_timeout(int withhold, unsigned int wait_limit_us, int device)
+namespace {
+int set_timeout_test(int kernel, const char *what, int withhold, unsigned int wait_limit_us,
+                     int device)
 {
     if (wait_limit_us > 2000000u)
-        return fail(LSTM_E_INVALID, "recurrence test: wait limit %u us above 2 s", wait_limit_us);
+        return fail(LSTM_E_INVALID, "%s test: wait limit %u us above 2 s", what, wait_limit_us);
     int st = prepare_device(device);
     if (st != LSTM_OK)
         return st;
@@ -945,6 +999,22 @@ extern "C" int lstm_test_recurrence_timeout(int withhold, unsigned int wait_limi
     if (!guard.ok)
         return fail(LSTM_E_CUDA, "cannot make device %d current", device);
     const unsigned long long limit =
-        wait_limit_us ? wait_limit_us * 1000ull : 2000000000ull;  // 0: the default 2 s
-    return recurrence_set_test(withhold != 0, limit);
+        wait_limit_us ? wait_limit_us * 1000ull : kDefaultWaitLimitNs;  // 0: the default 2 s
+    return set_kernel_test(kernel, withhold != 0, limit);
+}
+}  // namespace
+
+extern "C" int lstm_test_recurrence_timeout(int withhold, unsigned int wait_limit_us, int device)
+{
+    return set_timeout_test(kTestRecurrence, "recurrence", withhold, wait_limit_us, device);
+}
+
+extern "C" int lstm_test_projection_timeout(int withhold, unsigned int wait_limit_us, int device)
+{
+    return set_timeout_test(kTestProjection, "projection", withhold, wait_limit_us, device);
+}
+
+extern "C" int lstm_test_heads_timeout(int withhold, unsigned int wait_limit_us, int device)
+{
+    return set_timeout_test(kTestHeads, "heads", withhold, wait_limit_us, device);
 }

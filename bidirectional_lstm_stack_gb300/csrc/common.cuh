@@ -50,12 +50,24 @@ cudaError_t device_alloc(void **p, size_t bytes);
 // LSTM_E_CUDA (an injected launch failure) while the lstm_test_fail_launches
 // counter is positive, else LSTM_OK; every kernel launch asks first.
 int check_launch_injection(const char *what);
-// Recurrence failure test: CTA 0 of every cluster withholds its h pushes and
-// every wait gives up after wait_limit_ns (default: 2 s, no withholding).
-int recurrence_set_test(int withhold, unsigned long long wait_limit_ns);
-// Whether a failure-test setting is in force on `device` (the stack then
+// Failure-test settings of one kernel on one device, passed to its launches
+// as kernel parameters: every bounded wait gives up after wait_limit_ns, and
+// with `withhold` the kernel starves its own waits (the recurrence: CTA 0 of
+// every cluster pushes no h; the projection and the heads: the producer
+// loads nothing).  Defaults: 2 s, no withholding.
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+struct KernelTest {
+    unsigned long long wait_limit_ns = kDefaultWaitLimitNs;
+    int withhold = 0;
+};
+enum TestKernel { kTestRecurrence = 0, kTestProjection = 1, kTestHeads = 2, kTestKernels = 3 };
+// The settings of `kernel` on the current device.
+KernelTest kernel_test(int kernel);
+// Sets them on the current device.
+int set_kernel_test(int kernel, int withhold, unsigned long long wait_limit_ns);
+// Whether any failure-test setting is in force on `device` (the stack then
 // launches directly instead of replaying a graph captured without it).
-bool recurrence_test_active(int device);
+bool kernel_test_active(int device);
 // LSTM_E_INVALID unless p is 16-byte aligned.
 int check_aligned(const void *p, const char *what);
 // The device that owns device pointer p; LSTM_E_INVALID for host memory.
@@ -80,16 +92,16 @@ struct DeviceGuard {
 
 // ---- projection (projection.cu) ------------------------------------------
 // Rows per TMA box of the projection's operands: X rows, and the W gate rows
-// one CTA of a 2-CTA cluster loads (half of a 256-row W tile).
+// of one tile (256, or 128 for the narrow tiles).
 constexpr int kProjectionBoxRows = 128;
-constexpr int kProjectionWBoxRows = 128;
-constexpr int kProjectionNarrowWBoxRows = 64;  // half of a 128-row W tile
+constexpr int kProjectionWBoxRows = 256;
+constexpr int kProjectionNarrowWBoxRows = 128;
 // Encodes the tensor map of a row-major fp32 matrix [rows][cols] read in
 // boxes of 16 columns x box_rows rows with the 64-byte swizzle.
 int encode_matrix_map(CUtensorMap *map, const float *base, long rows, int cols,
                       int box_rows);
-// The tensor maps of one layer's packed W planes [1024][kp]: 128-row boxes
-// for the 256-column tiles, 64-row boxes for the 128-column tiles used when
+// The tensor maps of one layer's packed W planes [1024][kp]: 256-row boxes
+// for the 256-column tiles, 128-row boxes for the 128-column tiles used when
 // few rows would leave most SMs idle.
 struct ProjectionW {
     CUtensorMap hi, lo, hi_narrow, lo_narrow;
@@ -106,8 +118,8 @@ int projection_prepare(int device);
 int encode_store_map(CUtensorMap *map, float *base, long rows, int cols);
 
 // ---- dense heads of the segmentation model (heads.cu) ----------------------
-// W rows one CTA of a 2-CTA cluster loads: half of a 128-row W k-block.
-constexpr int kHeadWBoxRows = 64;
+// W rows of one k-block of the heads' weights (all 128 output columns).
+constexpr int kHeadWBoxRows = 128;
 
 // ---- recurrence (recurrence.cu) ------------------------------------------
 int launch_recurrence(const float *g, const float *rp, const float *bias,
@@ -117,6 +129,11 @@ int launch_recurrence_variant(const float *g, const float *rp, const float *bias
                               float *y, int batch, int steps, int direction,
                               int cluster, int nw, int nch, int threads, unsigned *fault,
                               cudaStream_t stream);
+// The default variant for `batch` in its FLOOR mode (the exchange alone:
+// the step's arithmetic replaced by a trivial dependence on the received h).
+int launch_recurrence_floor(const float *g, const float *rp, const float *bias, float *y,
+                            int batch, int steps, int direction, unsigned *fault,
+                            cudaStream_t stream);
 // Clusters of a variant the device can hold at once.
 int recurrence_max_clusters(int cluster, int nw, int nch, int threads, int *out);
 int recurrence_prepare(int device);
@@ -214,18 +231,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
                  : "memory");
 }
-// The same load delivered to the same shared-memory offset (and mbarrier
-// offset) of every CTA in `cta_mask` of this cluster.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map,
-                                                      uint64_t *bar, int x, int y,
-                                                      uint16_t cta_mask)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-                 ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y),
-                 "h"(cta_mask)
-                 : "memory");
-}
 // Shared memory -> global through the tensor map; the TMA engine writes only
 // the part of the box inside the tensor.  Tracked by bulk groups.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y)
@@ -312,15 +317,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
-                 : "memory");
-}
-// Arrives once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
-// when this thread's earlier tcgen05 operations have completed.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                 " [%0], %1;" ::"r"(smem_u32(bar)),
-                 "h"(cta_mask)
                  : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_nid_x()

@@ -6,9 +6,9 @@
 //     h1 = leaky(y W0 + b0),  h2 = leaky(h1 W1 + b1),
 //     out = log_softmax(h2 W2 + b2)  (7 classes).
 //
-// Design (sm_103a): one persistent kernel runs all three layers on 128-row
-// tiles, CTAs paired in clusters of two along the rows (each W k-block is
-// loaded half by each CTA and multicast into both):
+// Design (sm_103a): one persistent kernel, one CTA per SM, runs all three
+// layers on 128-row tiles (each CTA loads its own W k-blocks; the 384 KiB of
+// W planes stay in L2):
 //  * warp 8 (TMA producer) streams, per tile, 16 k-blocks of y with W0 and
 //    then 8 k-blocks of W1 through a 6-stage ring;
 //  * warps 0-3 split the y blocks into TF32 hi (in place) and lo;
@@ -54,9 +54,6 @@ constexpr int K1_BLOCKS = kMid / BK;        // 8: linear1
 constexpr int BLOCKS_PER_TILE = K0_BLOCKS + K1_BLOCKS;
 constexpr int A_BYTES = BM * BK * 4;        // 8 KiB
 constexpr int W_BYTES = kMid * BK * 4;      // 8 KiB: one W k-block, 128 rows
-constexpr int CLUSTER = 2;
-constexpr uint16_t PAIR_MASK = (1u << CLUSTER) - 1;
-constexpr int W_HALF_BYTES = W_BYTES / CLUSTER;
 constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * W_BYTES;  // A hi, A lo, W hi, W lo
 constexpr int A_LO = A_BYTES;
 constexpr int W_HI = 2 * A_BYTES;
@@ -78,7 +75,7 @@ constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
-static_assert(kMid / CLUSTER == kHeadWBoxRows, "W box rows");
+static_assert(kMid == kHeadWBoxRows, "W box rows");
 static_assert(RING_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "stage alignment");
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -87,7 +84,8 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
              const __grid_constant__ CUtensorMap w0lo_map,
              const __grid_constant__ CUtensorMap w1hi_map,
              const __grid_constant__ CUtensorMap w1lo_map, const float *__restrict__ params,
-             float slope, float *__restrict__ logp, int rows, int pairs, unsigned *fault)
+             float slope, float *__restrict__ logp, int rows, int tiles, unsigned *fault,
+             unsigned long long wait_limit_ns, int withhold)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -112,7 +110,7 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&conv[s], CONVERTERS);
-            ptx::mbar_init(&empty[s], CLUSTER);  // both CTAs' MMAs release a stage
+            ptx::mbar_init(&empty[s], 1);  // the MMAs that read the stage completed
         }
         ptx::mbar_init(acc1_full, 1);
         ptx::mbar_init(acc2_full, 1);
@@ -134,46 +132,39 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // the peer's barriers are initialised before any multicast reaches them
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait_acquire();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int rank = static_cast<int>(ptx::cluster_ctarank());
-    const int first = static_cast<int>(ptx::cluster_id_x());
-    const int stride = static_cast<int>(ptx::cluster_nid_x());
+    const int first = static_cast<int>(blockIdx.x);
+    const int stride = static_cast<int>(gridDim.x);
     long issued = 0;  // producer: stages whose loads were issued
 
     if (warp == PRODUCER_WARP) {
-        if (lane == 0) {
+        // failure test (`withhold`): nothing is loaded, so the converters'
+        // waits run out
+        if (lane == 0 && !withhold) {
             long kbi = 0;
-            for (int t = first; t < pairs && !*abort_flag; t += stride) {
-                const int m0 = (t * CLUSTER + rank) * BM;
+            for (int t = first; t < tiles && !*abort_flag; t += stride) {
+                const int m0 = t * BM;
                 bool ok = true;
                 for (int kb = 0; kb < BLOCKS_PER_TILE; ++kb, ++kbi) {
                     const int s = static_cast<int>(kbi % STAGES);
                     const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
                     if (n > 0 && !ptx::mbar_wait_bounded(&empty[s], (n - 1) & 1, abort_flag, fault,
-                                                         kFaultProducer, WAIT_LIMIT_NS)) {
+                                                         kFaultProducer, wait_limit_ns)) {
                         ok = false;
                         break;
                     }
                     uint8_t *st = smem + s * STAGE_BYTES;
-                    const int wrow = rank * (kMid / CLUSTER);  // this CTA's half of W
                     if (kb < K0_BLOCKS) {
                         ptx::mbar_arrive_expect_tx(&full[s], A_BYTES + 2 * W_BYTES);
                         ptx::tma_load_2d(st, &y_map, &full[s], kb * BK, m0);
-                        ptx::tma_load_2d_multicast(st + W_HI + rank * W_HALF_BYTES, &w0hi_map,
-                                                   &full[s], kb * BK, wrow, PAIR_MASK);
-                        ptx::tma_load_2d_multicast(st + W_LO + rank * W_HALF_BYTES, &w0lo_map,
-                                                   &full[s], kb * BK, wrow, PAIR_MASK);
+                        ptx::tma_load_2d(st + W_HI, &w0hi_map, &full[s], kb * BK, 0);
+                        ptx::tma_load_2d(st + W_LO, &w0lo_map, &full[s], kb * BK, 0);
                     } else {
                         const int k = (kb - K0_BLOCKS) * BK;
                         ptx::mbar_arrive_expect_tx(&full[s], 2 * W_BYTES);
-                        ptx::tma_load_2d_multicast(st + W_HI + rank * W_HALF_BYTES, &w1hi_map,
-                                                   &full[s], k, wrow, PAIR_MASK);
-                        ptx::tma_load_2d_multicast(st + W_LO + rank * W_HALF_BYTES, &w1lo_map,
-                                                   &full[s], k, wrow, PAIR_MASK);
+                        ptx::tma_load_2d(st + W_HI, &w1hi_map, &full[s], k, 0);
+                        ptx::tma_load_2d(st + W_LO, &w1lo_map, &full[s], k, 0);
                     }
                     issued = kbi + 1;
                 }
@@ -185,7 +176,7 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
         if (lane == 0) {
             long kbi = 0;
             int ti = 0;
-            for (int t = first; t < pairs && !*abort_flag; t += stride, ++ti) {
+            for (int t = first; t < tiles && !*abort_flag; t += stride, ++ti) {
                 bool ok = true;
                 // linear0 into accumulator 1 (the epilogue read it before it
                 // wrote the previous tile's h1, which linear1 waited for)
@@ -193,7 +184,7 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
                     const int s = static_cast<int>(kbi % STAGES);
                     const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
                     if (!ptx::mbar_wait_bounded(&conv[s], n & 1, abort_flag, fault, kFaultMma,
-                                                WAIT_LIMIT_NS)) {
+                                                wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -212,21 +203,21 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
                         ptx::mma_tf32(tmem + ACC1, ptx::sw64_desc(a_lo + off),
                                       ptx::sw64_desc(b_hi + off), IDESC, 1);
                     }
-                    ptx::mma_commit_multicast(&empty[s], PAIR_MASK);
+                    ptx::mma_commit(&empty[s]);
                 }
                 ptx::mma_commit(acc1_full);  // also when stopping: frees the epilogue
                 if (!ok)
                     break;
                 // linear1 into accumulator 2 once h1 of this tile is in place
                 if (!ptx::mbar_wait_bounded(ep1_done, ti & 1, abort_flag, fault, kFaultMma,
-                                            WAIT_LIMIT_NS))
+                                            wait_limit_ns))
                     break;
                 ptx::tc_fence_after();
                 for (int kb = 0; kb < K1_BLOCKS && ok; ++kb, ++kbi) {
                     const int s = static_cast<int>(kbi % STAGES);
                     const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
                     if (!ptx::mbar_wait_bounded(&conv[s], n & 1, abort_flag, fault, kFaultMma,
-                                                WAIT_LIMIT_NS)) {
+                                                wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -244,7 +235,7 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
                         ptx::mma_tf32_tmem_a(tmem + ACC2, tmem + H1LO + kcol,
                                              ptx::sw64_desc(b_hi + off), IDESC, 1);
                     }
-                    ptx::mma_commit_multicast(&empty[s], PAIR_MASK);
+                    ptx::mma_commit(&empty[s]);
                 }
                 ptx::mma_commit(acc2_full);
                 if (!ok)
@@ -259,13 +250,13 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
         // W1 stages only pass through
         const int tid = threadIdx.x;
         long kbi = 0;
-        for (int t = first; t < pairs && !*abort_flag; t += stride) {
+        for (int t = first; t < tiles && !*abort_flag; t += stride) {
             bool ok = true;
             for (int kb = 0; kb < BLOCKS_PER_TILE; ++kb, ++kbi) {
                 const int s = static_cast<int>(kbi % STAGES);
                 const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
                 if (!ptx::mbar_wait_bounded(&full[s], n & 1, abort_flag, fault, kFaultConverter,
-                                            WAIT_LIMIT_NS)) {
+                                            wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -292,10 +283,10 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
         const int q = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         int ti = 0;
-        for (int t = first; t < pairs; t += stride, ++ti) {
-            const long row = static_cast<long>(t * CLUSTER + rank) * BM + q * 32 + lane;
+        for (int t = first; t < tiles; t += stride, ++ti) {
+            const long row = static_cast<long>(t) * BM + q * 32 + lane;
             bool got = ptx::mbar_wait_bounded(acc1_full, ti & 1, abort_flag, fault, kFaultEpilogue,
-                                              WAIT_LIMIT_NS);
+                                              wait_limit_ns);
             // tcgen05.ld / st are warp-collective: continue only if every lane may
             if (!__all_sync(0xffffffffu, got) || *abort_flag)
                 break;
@@ -321,7 +312,7 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
             ptx::tc_fence_before();
             ptx::mbar_arrive(ep1_done);
             got = ptx::mbar_wait_bounded(acc2_full, ti & 1, abort_flag, fault, kFaultEpilogue,
-                                         WAIT_LIMIT_NS);
+                                         wait_limit_ns);
             if (!__all_sync(0xffffffffu, got) || *abort_flag)
                 break;
             ptx::tc_fence_after();
@@ -384,17 +375,12 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
-    // neither CTA leaves while the other may still multicast into it or
-    // release its stages
-    __syncwarp();
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait_acquire();
 }
 
-int g_max_clusters[64] = {};
+int g_max_ctas[64] = {};
 
 // Per-device set-up, with that device current: the kernel's shared-memory
-// attribute and the number of its clusters that run at once.
+// attribute and the number of its CTAs that run at once.
 int heads_prepare(int device)
 {
     static std::mutex mu;
@@ -408,23 +394,17 @@ int heads_prepare(int device)
                          "heads shared-memory attribute");
     if (st != LSTM_OK)
         return st;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CLUSTER);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    st = cuda_status(cudaOccupancyMaxActiveClusters(&n, heads_kernel, &cfg),
-                     "heads max active clusters");
+    int sms = 0, per_sm = 0;
+    st = cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
+                     "SM count");
     if (st != LSTM_OK)
         return st;
-    g_max_clusters[device] = n > 0 ? n : 74;
+    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_kernel, THREADS,
+                                                                   SMEM_BYTES),
+                     "heads occupancy");
+    if (st != LSTM_OK)
+        return st;
+    g_max_ctas[device] = per_sm > 0 ? per_sm * sms : sms;
     done[device] = true;
     return LSTM_OK;
 }
@@ -575,28 +555,22 @@ extern "C" int lstm_heads_forward(lstm_heads *h, const float *y, size_t y_len, f
         h->map_y_base = y;
         h->map_y_rows = rows;
     }
-    const long mtiles = (static_cast<long>(rows) + BM - 1) / BM;
-    const long pairs = (mtiles + CLUSTER - 1) / CLUSTER;
-    const int fit = g_max_clusters[h->device] > 0 ? g_max_clusters[h->device] : 74;
-    const long clusters = pairs < fit ? pairs : fit;
+    const long tiles = (static_cast<long>(rows) + BM - 1) / BM;
+    const int fit = g_max_ctas[h->device] > 0 ? g_max_ctas[h->device] : 148;
+    const long grid = tiles < fit ? tiles : fit;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     if ((st = check_launch_injection("heads launch")))
         return st;
-    const int npairs = static_cast<int>(pairs);
+    const int ntiles = static_cast<int>(tiles);
+    const KernelTest test = kernel_test(kTestHeads);
     return cuda_status(cudaLaunchKernelEx(&cfg, heads_kernel, h->map_y, h->map_w0hi, h->map_w0lo,
                                           h->map_w1hi, h->map_w1lo,
                                           static_cast<const float *>(h->params), h->slope, logp,
-                                          rows, npairs, h->fault),
+                                          rows, ntiles, h->fault, test.wait_limit_ns,
+                                          test.withhold),
                        "heads launch");
 }

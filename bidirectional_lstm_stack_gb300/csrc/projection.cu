@@ -5,21 +5,20 @@
 // `InputProjection::enqueue`), with the gate columns already in the packed,
 // unit-interleaved order (the packer reorders W's rows).
 //
-// Design (sm_103a), a persistent kernel, one CTA per SM, CTAs paired in
-// clusters of two along the rows:
-//  * a cluster walks pairs of 128 x 256 tiles of G (pair p: rows
-//    256*(p/4) + 128*rank, gate columns 256*(p%4)); both CTAs of a pair use
-//    the same W tile, so each loads half of it and multicasts that half into
-//    both CTAs' shared memory (half the W traffic from L2 per tile; clusters
-//    of four were measured slower);
+// Design (sm_103a), a persistent kernel, one CTA per SM:
+//  * CTA b walks tiles b, b + grid, ... of 128 rows x 256 gate columns of G
+//    (tile t: rows 128*(t/4), columns 256*(t%4)), so the CTAs running
+//    together read the same rows of X from L2; each CTA loads its whole W
+//    tile itself (W is 1-2 MiB per layer and stays in L2), so no CTA writes
+//    into another CTA's shared memory and the kernel needs no cluster;
 //  * K advances in blocks of 16 fp32 (64 bytes, 64-byte swizzle) through a
 //    192 KiB shared-memory ring: 4 stages of 48 KiB (X, X lo, W hi, W lo) in
 //    3xTF32, 8 stages of 24 KiB in the single-product mode; with few rows
 //    (the 256-column grid would fill at most half the SMs) the tiles are 128
 //    columns wide, twice as many CTAs;
-//  * warp 8 (TMA producer) loads the X block and its half of the TF32 hi and
-//    lo planes of Wp (split on the host) into the ring; a stage is reused
-//    only once the MMAs of both CTAs have released it;
+//  * warp 8 (TMA producer) loads the X block and the TF32 hi and lo planes of
+//    the W tile (split on the host) into the ring; a stage is reused only
+//    once the MMAs that read it have completed;
 //  * warps 0-3 split the X block in place into its TF32 hi part and a second
 //    buffer with the TF32 lo remainder;
 //  * one thread of warp 9 issues tcgen05.mma kind::tf32 (M=128, N=256, K=8)
@@ -61,8 +60,6 @@ constexpr int OUT_BYTES = 32 * OUT_COLS * 4;             // one warp's 32 rows: 
 constexpr int OUT_OFFSET = RING_BYTES;                   // staging: 4 warps x 2 slices
 constexpr size_t SMEM_BYTES = OUT_OFFSET + 4 * 2 * OUT_BYTES + 1024 + 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
-constexpr int CLUSTER = 2;                          // CTAs sharing a W tile
-constexpr uint16_t PAIR_MASK = (1u << CLUSTER) - 1;
 
 // One instantiation: tiles of BN gate columns, 3xTF32 or single products.
 template <int BN_, bool SINGLE_>
@@ -79,7 +76,6 @@ struct Shape {
     static constexpr int B_HI = SINGLE ? A_BYTES : 2 * A_BYTES;
     static constexpr int B_LO = B_HI + B_BYTES;                  // 3xTF32 only
     static constexpr uint32_t TX_BYTES = SINGLE ? A_BYTES + B_BYTES : A_BYTES + 2 * B_BYTES;
-    static constexpr int B_HALF_BYTES = B_BYTES / CLUSTER;      // W rows one CTA loads
     static constexpr uint32_t ACC_COLS = BN;                     // per accumulator
     static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
     static constexpr int TILES_N = kGateColumns / BN;
@@ -90,8 +86,8 @@ struct Shape {
 using GatesShape = Shape<256, false>;
 using GatesTf32Shape = Shape<256, true>;
 using GatesNarrowShape = Shape<128, false>;  // few rows: twice the tiles
-static_assert(GatesShape::BN / CLUSTER == kProjectionWBoxRows && BM == kProjectionBoxRows &&
-                  GatesNarrowShape::BN / CLUSTER == kProjectionNarrowWBoxRows,
+static_assert(GatesShape::BN == kProjectionWBoxRows && BM == kProjectionBoxRows &&
+                  GatesNarrowShape::BN == kProjectionNarrowWBoxRows,
               "TMA boxes");
 
 using ptx::sw64_desc;
@@ -108,8 +104,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 projection_kernel(const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap whi_map,
                   const __grid_constant__ CUtensorMap wlo_map,
-                  const __grid_constant__ CUtensorMap out_map, int rows, int kblocks, int pairs,
-                  unsigned *fault)
+                  const __grid_constant__ CUtensorMap out_map, int rows, int kblocks, int tiles,
+                  unsigned *fault, unsigned long long wait_limit_ns, int withhold)
 {
     using RG = S;
     constexpr bool SINGLE = S::SINGLE;
@@ -138,7 +134,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&conv[s], CONVERTERS);
-            ptx::mbar_init(&empty[s], CLUSTER);  // both CTAs' MMAs release a stage
+            ptx::mbar_init(&empty[s], 1);  // the MMAs that read the stage completed
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&acc_full[a], 1);
@@ -160,38 +156,33 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // the peer's barriers are initialised before any multicast reaches them
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait_acquire();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int rank = static_cast<int>(ptx::cluster_ctarank());
-    const int first = static_cast<int>(ptx::cluster_id_x());
-    const int stride = static_cast<int>(ptx::cluster_nid_x());
+    const int first = static_cast<int>(blockIdx.x);
+    const int stride = static_cast<int>(gridDim.x);
     long issued = 0;            // producer: K blocks whose loads were issued
     int committed_tiles = 0;    // MMA: accumulators committed
 
     if (warp == PRODUCER_WARP) {
-        if (lane == 0) {
+        // failure test (`withhold`): nothing is loaded, so the converters'
+        // waits run out
+        if (lane == 0 && !withhold) {
             long kbi = 0;
-            for (int t = first; t < pairs && !*abort_flag; t += stride) {
-                const int m0 = ((t / TILES_N) * CLUSTER + rank) * BM;
+            for (int t = first; t < tiles && !*abort_flag; t += stride) {
+                const int m0 = (t / TILES_N) * BM;
                 const int n0 = (t % TILES_N) * BN;
-                const int nh = n0 + rank * (BN / CLUSTER);  // this CTA's half of the W tile
                 for (int kb = 0; kb < kblocks; ++kb, ++kbi) {
                     const int s = static_cast<int>(kbi % STAGES);
                     const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
                     if (n > 0 && !ptx::mbar_wait_bounded(&empty[s], (n - 1) & 1, abort_flag, fault,
-                                                         kFaultProducer, WAIT_LIMIT_NS))
+                                                         kFaultProducer, wait_limit_ns))
                         break;
                     uint8_t *st = smem + s * STAGE_BYTES;
                     ptx::mbar_arrive_expect_tx(&full[s], RG::TX_BYTES);
                     ptx::tma_load_2d(st, &x_map, &full[s], kb * BK, m0);
-                    ptx::tma_load_2d_multicast(st + RG::B_HI + rank * S::B_HALF_BYTES, &whi_map,
-                                               &full[s], kb * BK, nh, PAIR_MASK);
+                    ptx::tma_load_2d(st + RG::B_HI, &whi_map, &full[s], kb * BK, n0);
                     if constexpr (!SINGLE)
-                        ptx::tma_load_2d_multicast(st + RG::B_LO + rank * S::B_HALF_BYTES, &wlo_map,
-                                                   &full[s], kb * BK, nh, PAIR_MASK);
+                        ptx::tma_load_2d(st + RG::B_LO, &wlo_map, &full[s], kb * BK, n0);
                     issued = kbi + 1;
                 }
             }
@@ -200,11 +191,11 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         if (lane == 0) {
             long kbi = 0;
             int ti = 0;
-            for (int t = first; t < pairs && !*abort_flag; t += stride, ++ti) {
+            for (int t = first; t < tiles && !*abort_flag; t += stride, ++ti) {
                 const int a = ti & 1;
                 const uint32_t use = static_cast<uint32_t>(ti >> 1);
                 if (use > 0 && !ptx::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, abort_flag,
-                                                       fault, kFaultMma, WAIT_LIMIT_NS))
+                                                       fault, kFaultMma, wait_limit_ns))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(a) * ACC_COLS;
@@ -213,7 +204,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     const int s = static_cast<int>(kbi % STAGES);
                     const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
                     if (!ptx::mbar_wait_bounded(&conv[s], n & 1, abort_flag, fault, kFaultMma,
-                                                WAIT_LIMIT_NS)) {
+                                                wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -234,7 +225,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                                           IDESC, 1);
                         }
                     }
-                    ptx::mma_commit_multicast(&empty[s], PAIR_MASK);
+                    ptx::mma_commit(&empty[s]);
                     *progress = static_cast<int>(kbi + 1);
                 }
                 ptx::mma_commit(&acc_full[a]);  // also when stopping early: frees the epilogue
@@ -248,13 +239,13 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         // single-product mode only rounds X to TF32 in place
         const int tid = threadIdx.x;
         long kbi = 0;
-        for (int t = first; t < pairs && !*abort_flag; t += stride) {
+        for (int t = first; t < tiles && !*abort_flag; t += stride) {
             bool ok = true;
             for (int kb = 0; kb < kblocks; ++kb, ++kbi) {
                 const int s = static_cast<int>(kbi % STAGES);
                 const uint32_t n = static_cast<uint32_t>(kbi / STAGES);
                 if (!ptx::mbar_wait_bounded(&full[s], n & 1, abort_flag, fault, kFaultConverter,
-                                            WAIT_LIMIT_NS)) {
+                                            wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -291,16 +282,16 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         uint8_t *stage_out = smem + OUT_OFFSET + q * 2 * OUT_BYTES;
         int slices = 0;  // store slices this warp issued
         int ti = 0;
-        for (int t = first; t < pairs; t += stride, ++ti) {
+        for (int t = first; t < tiles; t += stride, ++ti) {
             const int a = ti & 1;
             const uint32_t use = static_cast<uint32_t>(ti >> 1);
             bool got = ptx::mbar_wait_bounded(&acc_full[a], use & 1, abort_flag, fault,
-                                              kFaultEpilogue, WAIT_LIMIT_NS);
+                                              kFaultEpilogue, wait_limit_ns);
             // tcgen05.ld is warp-collective: continue only if every lane may
             if (!__all_sync(0xffffffffu, got) || *abort_flag)
                 break;
             ptx::tc_fence_after();
-            const int m0 = ((t / TILES_N) * CLUSTER + rank) * BM + q * 32;  // this warp's rows
+            const int m0 = (t / TILES_N) * BM + q * 32;  // this warp's rows
             const int n0 = (t % TILES_N) * BN;
             const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(a) * ACC_COLS;
             // Pace the stores: slice c of this tile goes out once the next
@@ -308,7 +299,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             // streams to memory under the next tile's compute instead of
             // every CTA writing its whole tile at once and stalling the loads.
             constexpr int NSLICE = BN / OUT_COLS;
-            const bool paced = t + stride < pairs;
+            const bool paced = t + stride < tiles;
             const long next_kb = static_cast<long>(ti + 1) * kblocks;
 #pragma unroll 1
             for (int c = 0; c < NSLICE; ++c, ++slices) {
@@ -317,7 +308,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     if (*progress < want && !*abort_flag) {
                         const uint64_t start = ptx::globaltimer();
                         while (*progress < want && !*abort_flag &&
-                               ptx::globaltimer() - start < WAIT_LIMIT_NS)
+                               ptx::globaltimer() - start < wait_limit_ns)
                             __nanosleep(64);
                     }
                 }
@@ -370,11 +361,6 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, S::TMEM_COLS);
     }
-    // neither CTA leaves while the other may still multicast into it or
-    // release its stages
-    __syncwarp();
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait_acquire();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -392,8 +378,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-int g_sm_count[64] = {};
-int g_max_clusters[64] = {};  // clusters of the projection a device runs at once
+int g_max_ctas[64] = {};  // CTAs of the projection a device runs at once
 
 } // namespace
 
@@ -440,9 +425,8 @@ const void *const kKernels[] = {
     reinterpret_cast<const void *>(&projection_kernel<GatesNarrowShape>),
 };
 
-// Persistent grid over the row tiles (pairs of 128-row tiles, one per CTA of
-// a 2-CTA cluster) times S::TILES_N column tiles, no larger than what runs at
-// once.
+// Persistent grid over the row tiles (128 rows) times S::TILES_N column
+// tiles, no larger than what runs at once.
 template <class S>
 int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
                  const CUtensorMap &wlo_map, const CUtensorMap &out_map, int rows, int kp,
@@ -451,35 +435,28 @@ int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     if (rows <= 0 || kp <= 0 || kp % 32 != 0)
         return fail(LSTM_E_INVALID, "tensor-core GEMM: rows %d, kp %d", rows, kp);
     const long mtiles = (static_cast<long>(rows) + BM - 1) / BM;
-    const long pairs = (mtiles + CLUSTER - 1) / CLUSTER * S::TILES_N;
-    if (pairs > 0x7fffffffL)
+    const long tiles = mtiles * S::TILES_N;
+    if (tiles > 0x7fffffffL)
         return fail(LSTM_E_OVERFLOW, "tensor-core GEMM: %d rows", rows);
     int dev = 0;
     int st = cuda_status(cudaGetDevice(&dev), "current device");
     if (st != LSTM_OK)
         return st;
-    const int fit = (dev >= 0 && dev < 64 && g_max_clusters[dev] > 0) ? g_max_clusters[dev]
-                                                                      : 148 / CLUSTER;
-    const long clusters = pairs < fit ? pairs : fit;
+    const int fit = (dev >= 0 && dev < 64 && g_max_ctas[dev] > 0) ? g_max_ctas[dev] : 148;
+    const long grid = tiles < fit ? tiles : fit;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const int kblocks = kp / BK;
-    const int npairs = static_cast<int>(pairs);
+    const int ntiles = static_cast<int>(tiles);
+    const KernelTest test = kernel_test(kTestProjection);
     if ((st = check_launch_injection("tensor-core GEMM launch")))
         return st;
     return cuda_status(cudaLaunchKernelEx(&cfg, projection_kernel<S>, x_map, whi_map, wlo_map,
-                                          out_map, rows, kblocks, npairs,
-                                          fault),
+                                          out_map, rows, kblocks, ntiles, fault,
+                                          test.wait_limit_ns, test.withhold),
                        "tensor-core GEMM launch");
 }
 }  // namespace
@@ -493,7 +470,6 @@ int projection_prepare(int device)
                          "SM count");
     if (st != LSTM_OK)
         return st;
-    g_sm_count[device] = sms;
     for (const void *fn : kKernels) {
         st = cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               static_cast<int>(SMEM_BYTES)),
@@ -503,23 +479,13 @@ int projection_prepare(int device)
     }
     // the persistent grid is no larger than what runs at once (every
     // instantiation has the same block and shared-memory size)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CLUSTER);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    st = cuda_status(cudaOccupancyMaxActiveClusters(&n, projection_kernel<GatesShape>, &cfg),
-                     "projection max active clusters");
+    int per_sm = 0;
+    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                         &per_sm, projection_kernel<GatesShape>, THREADS, SMEM_BYTES),
+                     "projection occupancy");
     if (st != LSTM_OK)
         return st;
-    g_max_clusters[device] = n > 0 ? n : sms / CLUSTER;
+    g_max_ctas[device] = per_sm > 0 ? per_sm * sms : sms;
     return LSTM_OK;
 }
 
@@ -550,15 +516,15 @@ int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, 
         return st;
     if (math == LSTM_MATH_TF32)
         return launch_tiles<GatesTf32Shape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream);
-    // With 256-column tiles a pair of row tiles is 4 cluster units; when those
-    // would fill at most half of the clusters that run at once, 128-column
-    // tiles give every CTA half the work on twice as many SMs.
+    // When the 256-column tiles would fill at most half of the CTAs that run
+    // at once, 128-column tiles give every CTA half the work on twice as many
+    // SMs.
     int dev = 0;
     if ((st = cuda_status(cudaGetDevice(&dev), "current device")))
         return st;
-    const int fit = (dev >= 0 && dev < 64 && g_max_clusters[dev] > 0) ? g_max_clusters[dev] : 74;
-    const long units = (static_cast<long>(rows) + 2 * BM - 1) / (2 * BM) * GatesShape::TILES_N;
-    if (2 * units <= fit)
+    const int fit = (dev >= 0 && dev < 64 && g_max_ctas[dev] > 0) ? g_max_ctas[dev] : 148;
+    const long tiles = (static_cast<long>(rows) + BM - 1) / BM * GatesShape::TILES_N;
+    if (2 * tiles <= fit)
         return launch_tiles<GatesNarrowShape>(x_map, w.hi_narrow, w.lo_narrow, g_map, rows, kp,
                                               fault, stream);
     return launch_tiles<GatesShape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream);

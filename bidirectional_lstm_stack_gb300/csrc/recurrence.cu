@@ -65,17 +65,7 @@ constexpr int KLEN = 16;              // columns per chunk
 constexpr int CHUNK_STRIDE = 20;      // padded chunk stride (conflict-free LDS.128)
 constexpr int HROW = KC * CHUNK_STRIDE;  // floats per window in the h buffer
 constexpr int PF = 4;                 // projection prefetch depth (steps)
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
-// Failure-test settings per device, passed to every launch as kernel
-// parameters: the per-wait limit, and whether CTA 0 of every cluster
-// withholds its h pushes (so its peers' waits run out).  Defaults: 2 s, no
-// withholding.
-struct RecurrenceTest {
-    unsigned long long wait_limit_ns = WAIT_LIMIT_NS;
-    int withhold = 0;
-};
-RecurrenceTest g_rec_test[64];
 
 // Activations through base-2 exponentials of pre-scaled arguments: the
 // recurrent weights, the bias and the projection value of gate q are
@@ -133,7 +123,13 @@ __device__ __forceinline__ bool unrolled_all(F &&f)
     return unrolled_all_impl(f, std::make_integer_sequence<int, N>{});
 }
 
-template <int C, int NW, int NCH = 1, int THREADS = threads_for<C>()>
+// FLOOR: the same kernel with the matrix-vector product, the reduction and
+// the cell update replaced by a trivial dependence of each new h on the
+// received h and on the projection value (same launch shape, projection
+// prefetch, h gathers, st.async pushes, y stores and bounded waits): its time
+// per step is the latency floor the exchange sets, which the bench reports
+// beside the real kernel's.  Its outputs are meaningless.
+template <int C, int NW, int NCH = 1, int THREADS = threads_for<C>(), bool FLOOR = false>
 __global__ void __launch_bounds__(THREADS, 1)
 recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                   const float *__restrict__ bias, float *__restrict__ y, int batch, int steps,
@@ -491,6 +487,13 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
         }
     };
 
+    // FLOOR: the new h of window wl depends on one received h value and on
+    // the projection value, nothing else
+    auto floor_h = [&](int par, int ch, const float (&gv)[HV]) -> float {
+        const float hv = hbuf[par][wbase + ch * NW + wl][kc * CHUNK_STRIDE];
+        return fmaf(hv, 0.5f, gv[0] * 0.001f);
+    };
+
     // One step s (= s0 + P, P the position in the unrolled group of PFD
     // steps, which selects the prefetch slot and the buffer parity); false
     // ends this thread's steps (a wait ran out).  TAIL: the next steps, the
@@ -529,10 +532,14 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                     if (tid == 0 && (!tail || s + 2 < steps))
                         ptx::mbar_arrive_expect_tx(&hbar[par][ch], bar_bytes[ch]);
                 }
-                float part[V], held[HV];
-                dots(par, ch, part);
-                reduce(part, held);
-                emit(par, ch, cell(ch, held, gcur[ch]), !tail || s + 1 < steps, t);
+                if constexpr (FLOOR) {
+                    emit(par, ch, floor_h(par, ch, gcur[ch]), !tail || s + 1 < steps, t);
+                } else {
+                    float part[V], held[HV];
+                    dots(par, ch, part);
+                    reduce(part, held);
+                    emit(par, ch, cell(ch, held, gcur[ch]), !tail || s + 1 < steps, t);
+                }
             }
         } else {
             // 0. h_{s-1} complete in buffer `par`
@@ -561,6 +568,12 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                     ptx::mbar_arrive_expect_tx(&hbar[par][0], bar_bytes[0]);
             }
 
+            float h[NCH];
+            if constexpr (FLOOR) {
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch)
+                    h[ch] = floor_h(par, ch, gcur[ch]);
+            } else {
             // The chunks are independent: each phase below runs over all of
             // them, so their latencies overlap.
             // 1. partial dot products over this lane's K chunk
@@ -604,7 +617,6 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
             }
 
             // 3. activations, gate gather, cell update
-            float h[NCH];
     #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
                 float act[HV];
@@ -624,6 +636,8 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp,
                 // one fused multiply-add after r
                 const float r = inv_one_plus_ex2(c[ch] * (-2.0f * kLog2e));
                 h[ch] = fmaf(2.0f * gate[3], r, -gate[3]);
+            }
+
             }
 
             // 4. gather the warp's four units of window wl, push them (16
@@ -699,13 +713,16 @@ struct Variant {
     int tile;     // windows per cluster
     int threads;  // per CTA
     const void *fn;
+    const void *floor_fn;  // the same variant in FLOOR mode
 };
 
 template <int C, int NW, int NCH = 1, int THREADS = threads_for<C>()>
 Variant variant()
 {
     return Variant{C, NW, NCH, THREADS / 8 / (kHidden / C) * NW * NCH, THREADS,
-                   reinterpret_cast<const void *>(&recurrence_kernel<C, NW, NCH, THREADS>)};
+                   reinterpret_cast<const void *>(&recurrence_kernel<C, NW, NCH, THREADS>),
+                   reinterpret_cast<const void *>(
+                       &recurrence_kernel<C, NW, NCH, THREADS, true>)};
 }
 
 // "Narrow" variants (one window group per CTA: 128 threads for clusters of
@@ -799,7 +816,8 @@ const Variant *choose_variant(int batch)
 }
 
 int launch_variant(const Variant &v, const float *g, const float *rp, const float *bias, float *y,
-                   int batch, int steps, int direction, unsigned *fault, cudaStream_t stream)
+                   int batch, int steps, int direction, unsigned *fault, cudaStream_t stream,
+                   bool floor = false)
 {
     const long tiles = (static_cast<long>(batch) + v.tile - 1) / v.tile;
     const long blocks = tiles * v.cluster;
@@ -817,49 +835,32 @@ int launch_variant(const Variant &v, const float *g, const float *rp, const floa
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int dev = 0;
-    int st = cuda_status(cudaGetDevice(&dev), "current device");
-    if (st != LSTM_OK)
-        return st;
-    RecurrenceTest test = (dev >= 0 && dev < 64) ? g_rec_test[dev] : RecurrenceTest{};
+    // failure-test settings (kernel parameters: reading them from a device
+    // variable at kernel start measured 3-7 % slower per step)
+    KernelTest test = kernel_test(kTestRecurrence);
+    int st;
     if ((st = check_launch_injection("recurrence launch")))
         return st;
     void *args[] = {const_cast<float **>(&g), const_cast<float **>(&rp),
                     const_cast<float **>(&bias), &y, &batch, &steps, &direction, &fault,
                     &test.wait_limit_ns, &test.withhold};
-    return cuda_status(cudaLaunchKernelExC(&cfg, v.fn, args), "recurrence launch");
+    return cuda_status(cudaLaunchKernelExC(&cfg, floor ? v.floor_fn : v.fn, args),
+                       "recurrence launch");
 }
 
 } // namespace
-
-int recurrence_set_test(int withhold, unsigned long long wait_limit_ns)
-{
-    int dev = 0;
-    int st = cuda_status(cudaGetDevice(&dev), "current device");
-    if (st != LSTM_OK)
-        return st;
-    if (dev < 0 || dev >= 64)
-        return fail(LSTM_E_INVALID, "device %d out of range", dev);
-    g_rec_test[dev].wait_limit_ns = wait_limit_ns;
-    g_rec_test[dev].withhold = withhold;
-    return LSTM_OK;
-}
-
-bool recurrence_test_active(int device)
-{
-    return device >= 0 && device < 64 &&
-           (g_rec_test[device].withhold || g_rec_test[device].wait_limit_ns != WAIT_LIMIT_NS);
-}
 
 int recurrence_prepare(int)
 {
     for (const Variant &v : kVariants) {
         if (v.cluster > 8) {
-            int st = cuda_status(
-                cudaFuncSetAttribute(v.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-                "recurrence cluster-size attribute");
-            if (st != LSTM_OK)
-                return st;
+            for (const void *fn : {v.fn, v.floor_fn}) {
+                int st = cuda_status(
+                    cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+                    "recurrence cluster-size attribute");
+                if (st != LSTM_OK)
+                    return st;
+            }
         }
     }
     return LSTM_OK;
@@ -870,6 +871,14 @@ int launch_recurrence(const float *g, const float *rp, const float *bias, float 
 {
     return launch_variant(*choose_variant(batch), g, rp, bias, y, batch, steps, direction, fault,
                           stream);
+}
+
+int launch_recurrence_floor(const float *g, const float *rp, const float *bias, float *y,
+                            int batch, int steps, int direction, unsigned *fault,
+                            cudaStream_t stream)
+{
+    return launch_variant(*choose_variant(batch), g, rp, bias, y, batch, steps, direction, fault,
+                          stream, true);
 }
 
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias, float *y,

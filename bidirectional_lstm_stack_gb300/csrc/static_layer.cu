@@ -73,16 +73,26 @@ extern "C" int lstm_layer_forward_static(const float *x, int batch, int steps, i
     int st;
     if ((st = check_aligned(x, "static layer input")) || (st = check_aligned(wp_hi, "wp_hi")) ||
         (st = check_aligned(wp_lo, "wp_lo")) || (st = check_aligned(rp, "rp")) ||
-        (st = check_aligned(y, "static layer output")))
+        (st = check_aligned(bias, "bias")) || (st = check_aligned(y, "static layer output")))
         return st;
-    int xdev = -1, current = -1;
-    if ((st = pointer_device(x, &xdev)))
-        return st;
+    int current = -1;
     if ((st = cuda_status(cudaGetDevice(&current), "current device")))
         return st;
-    if (xdev != current)
-        return fail(LSTM_E_INVALID, "lstm_layer_forward_static: x is on device %d, current device is %d",
-                    xdev, current);
+    // every buffer lives on the current device, where the kernels run
+    const struct {
+        const void *p;
+        const char *name;
+    } buffers[] = {{x, "x"}, {wp_hi, "wp_hi"}, {wp_lo, "wp_lo"}, {rp, "rp"},
+                   {bias, "bias"}, {y, "y"}};
+    for (const auto &b : buffers) {
+        int dev = -1;
+        if ((st = pointer_device(b.p, &dev)))
+            return st;
+        if (dev != current)
+            return fail(LSTM_E_INVALID,
+                        "lstm_layer_forward_static: %s is on device %d, current device is %d",
+                        b.name, dev, current);
+    }
     float *gates = nullptr;
     if ((st = static_setup(current, &gates)) != LSTM_OK)
         return st;

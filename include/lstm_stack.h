@@ -294,6 +294,34 @@ int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
                             int cluster_size, int windows_per_chunk, int chunks,
                             int threads_per_block, void *stream);
 
+/* Measurement: the recurrence's per-step latency floor.  Launches exactly
+ * what lstm_recurrence launches for this batch (same variant, grid, cluster
+ * and block shape, projection prefetch, distributed-shared-memory h
+ * exchange, y stores and bounded waits), with the step's arithmetic -- the
+ * 512 x 128 matrix-vector product, the reduction across lanes and the cell
+ * update (lstmproj.rs module docs: the work each step of the persistent
+ * recurrence does) -- replaced by a trivial dependence of each new h on one
+ * received h value and the projection value.  Its time per step is the
+ * latency the exchange alone sets, the floor the real kernel is measured
+ * against.  Arguments, layout and errors as lstm_recurrence; y receives
+ * meaningless values. */
+int lstm_recurrence_floor(const float *g, const float *rp, const float *bias,
+                          float *y, int batch, int steps, int direction,
+                          void *stream);
+
+/* Measurement: the dense rate of the tensor cores in the mode the projection
+ * and the dense heads use (tcgen05.mma kind::tf32, M = 128, N = 256, K = 8,
+ * fp32 accumulation in tensor memory).  One block per SM of `device` issues
+ * 2 * `iterations` back-to-back MMAs on operands resident in shared memory;
+ * the run is timed with CUDA events after a warm-up launch and *tflops
+ * receives the TF32 rate (2*M*N*K flops per MMA).  The projection's 3xTF32
+ * mode (three products per fp32 product, the split the pages choose for
+ * fp32-level accuracy on the TF32 tensor path, segdense.rs "3xTF32") is
+ * bound by a third of it.  Synchronises; allocates no device memory.
+ * Errors: LSTM_E_INVALID (null, iterations outside 1..10^7), LSTM_E_DEVICE,
+ * LSTM_E_CUDA, LSTM_E_FAULT (the kernel's bounded wait ran out). */
+int lstm_tf32_rate(int device, int iterations, double *tflops);
+
 /* How many clusters of a recurrence variant (as above) `device` can run at
  * once (cudaOccupancyMaxActiveClusters).  Errors: LSTM_E_INVALID (null,
  * unknown variant), LSTM_E_DEVICE, LSTM_E_CUDA. */
@@ -320,7 +348,7 @@ int lstm_recurrence_max_clusters(int cluster_size, int windows_per_chunk,
  * capture.  All calls share the array: calls that overlap on the GPU race
  * and must be ordered by the caller; it keeps the last call's contents, and
  * nothing in it needs clearing (each call writes every row it reads).
- * x must be on the current device; pointers 16-byte aligned.  Errors:
+ * Every buffer must be on the current device and 16-byte aligned.  Errors:
  * LSTM_E_INVALID, LSTM_E_DEVICE, LSTM_E_CUDA. */
 int lstm_layer_forward_static(const float *x, int batch, int steps,
                               int in_width, const float *wp_hi,
@@ -353,7 +381,8 @@ typedef struct lstm_heads lstm_heads; /* opaque; owned by the library */
  * as the pages store them):
  *   w0 : [256][128], b0 : [128],  w1 : [128][128], b1 : [128],
  *   w2 : [128][7],   b2 : [7]
- * and allocates the two [max_rows][128] intermediate buffers on `device`.
+ * into device memory on `device` (W0 and W1 as TF32 hi/lo planes); the
+ * forward keeps h1 and h2 on chip, so no activation buffer is allocated.
  * Errors: LSTM_E_INVALID (null, max_rows <= 0), LSTM_E_DEVICE, LSTM_E_CUDA,
  * LSTM_E_ALLOC.  Nothing is leaked on failure. */
 int lstm_heads_create(const float *w0, const float *b0, const float *w1,
@@ -397,6 +426,18 @@ int lstm_test_fail_launches(int skip, int count);
  * restores normal operation.  Errors: LSTM_E_INVALID, LSTM_E_DEVICE,
  * LSTM_E_CUDA. */
 int lstm_test_recurrence_timeout(int withhold, unsigned int wait_limit_us, int device);
+
+/* The same for the projection (lstm_projection, and every projection the
+ * stack runs): with withhold != 0 the kernel's TMA producer loads nothing, so
+ * the waits of the warps that consume its stages run out; every wait gives
+ * up after wait_limit_us (at most 2 s; 0 = 2 s).  A wait that runs out sets
+ * the fault word, every role of the kernel stops, drains what it issued,
+ * frees its tensor memory and returns.  (0, 0) restores normal operation.
+ * Errors as lstm_test_recurrence_timeout. */
+int lstm_test_projection_timeout(int withhold, unsigned int wait_limit_us, int device);
+
+/* The same for the dense heads (lstm_heads_forward). */
+int lstm_test_heads_timeout(int withhold, unsigned int wait_limit_us, int device);
 
 #ifdef __cplusplus
 }

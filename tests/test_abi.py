@@ -25,7 +25,7 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(lstm_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(lstm_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_stack_api():
@@ -171,3 +171,17 @@ def test_heads_create_rejects_null_weights(lib):
     assert lib.lstm_heads_create(*([w.ctypes.data] * 6), 0.01, 0, 0,
                                  ctypes.byref(out)) == binding.LSTM_E_INVALID
     lib.lstm_heads_destroy(None)
+
+
+def test_measurement_entry_points_reject_bad_arguments(lib):
+    import ctypes
+    v = ctypes.c_double(0.0)
+    assert lib.lstm_tf32_rate(0, 0, ctypes.byref(v)) == 1  # iterations outside 1..10^7
+    assert lib.lstm_tf32_rate(0, 100, None) == 1
+    assert lib.lstm_recurrence_floor(None, None, None, None, 1, 1, 0, None) == 1
+
+
+def test_timeout_hooks_reject_limits_above_two_seconds(lib):
+    for hook in (lib.lstm_test_recurrence_timeout, lib.lstm_test_projection_timeout,
+                 lib.lstm_test_heads_timeout):
+        assert hook(1, 2000001, 0) == 1

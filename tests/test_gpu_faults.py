@@ -1,8 +1,10 @@
 """Failure detection without a GPU fault: injected allocation and launch
-failures on the host, and recurrence waits made to run out on the GPU (CTA
-0 of every cluster withholds its hidden state, so its peers' bounded waits
-expire).  In every case the call reports the failure and the next call on the
-same objects works again."""
+failures on the host, and bounded waits made to run out on the GPU (the
+recurrence: CTA 0 of every cluster withholds its hidden state, so its peers'
+waits expire; the projection and the dense heads: the TMA producer loads
+nothing, so the waits of the warps that consume its stages expire).  In every
+case the call reports the failure and the next call on the same objects works
+again."""
 import numpy as np
 import pytest
 
@@ -13,6 +15,9 @@ from gpu_util import assert_within, cuda
 pytestmark = pytest.mark.gpu
 
 FAULT_RECURRENCE = 1 << 5
+# the roles of the projection and heads kernels whose waits can run out:
+# producer, converters, MMA issuer, epilogue (not the drain at teardown)
+FAULT_TILED_ROLES = (1 << 0) | (1 << 1) | (1 << 2) | (1 << 3)
 
 
 @pytest.fixture(scope="module")
@@ -27,6 +32,8 @@ def _clean():
     lib.lstm_test_fail_allocations(0, 0)
     lib.lstm_test_fail_launches(0, 0)
     lib.lstm_test_recurrence_timeout(0, 0, 0)
+    lib.lstm_test_projection_timeout(0, 0, 0)
+    lib.lstm_test_heads_timeout(0, 0, 0)
     binding.lstm_fault_status()
 
 
@@ -120,3 +127,69 @@ def test_forward_host_reports_a_timed_out_wait(layers):
         assert_within(y, oracle.lstm_stack(x, layers), what="forward_host after timeout")
     finally:
         s.close()
+
+
+def test_projection_wait_timeout_sets_fault_and_recovers(layers):
+    import torch
+    lib = binding.load()
+    rows = 700  # several 128-row tiles and a ragged tail
+    x_np = synthetic.random_matrix(21, (rows, 256))
+    x = cuda(x_np)
+    wp_hi, wp_lo, _, _ = binding.lstm_pack_layer(layers[1]["w"], layers[1]["r"], layers[1]["b"],
+                                                 256, 256)
+    whi, wlo = cuda(wp_hi), cuda(wp_lo)
+    g = torch.zeros((rows, 1024), device="cuda")
+    assert binding.lstm_fault_status() == 0
+    lib.lstm_test_projection_timeout(1, 20000, 0)  # producer loads nothing, 20 ms per wait
+    binding.lstm_projection(x, rows, 256, whi, wlo, 256, g)
+    torch.cuda.synchronize()
+    bits = binding.lstm_fault_status()
+    assert bits != 0 and (bits & ~FAULT_TILED_ROLES) == 0, hex(bits)
+    lib.lstm_test_projection_timeout(0, 0, 0)
+    binding.lstm_projection(x, rows, 256, whi, wlo, 256, g)
+    torch.cuda.synchronize()
+    assert binding.lstm_fault_status() == 0
+    ref = oracle.projection(x_np, layers[1]["w"])
+    assert_within(g.cpu().numpy(), ref, what="projection after timeout")
+
+
+def test_forward_host_reports_a_timed_out_projection_wait(layers):
+    lib = binding.load()
+    x = synthetic.stack_input(synthetic.WORKLOADS["b1_t64"])
+    s = binding.LSTMStack(layers, 1, 64)
+    try:
+        y = np.empty((1, 64, 256), np.float32)
+        lib.lstm_test_projection_timeout(1, 20000, 0)
+        with pytest.raises(binding.LSTMError) as e:
+            binding.lstm_stack_forward_host(s.handle, x, y, 1, 64)
+        assert e.value.code == binding.LSTM_E_FAULT
+        lib.lstm_test_projection_timeout(0, 0, 0)
+        binding.lstm_stack_forward_host(s.handle, x, y, 1, 64)
+        assert_within(y, oracle.lstm_stack(x, layers), what="forward_host after timeout")
+    finally:
+        s.close()
+
+
+def test_heads_wait_timeout_sets_fault_and_recovers():
+    import torch
+    lib = binding.load()
+    hw = synthetic.heads_weights()
+    rows = 300
+    y_np = synthetic.random_matrix(22, (rows, 256))
+    y = cuda(y_np)
+    heads = binding.LSTMHeads(hw, rows)
+    try:
+        assert binding.lstm_fault_status() == 0
+        lib.lstm_test_heads_timeout(1, 20000, 0)
+        heads(y)
+        torch.cuda.synchronize()
+        bits = binding.lstm_fault_status()
+        assert bits != 0 and (bits & ~FAULT_TILED_ROLES) == 0, hex(bits)
+        lib.lstm_test_heads_timeout(0, 0, 0)
+        logp = heads(y)
+        torch.cuda.synchronize()
+        assert binding.lstm_fault_status() == 0
+        ref = oracle.heads(y_np, hw["w0"], hw["b0"], hw["w1"], hw["b1"], hw["w2"], hw["b2"])
+        assert_within(logp.cpu().numpy(), ref, what="heads after timeout")
+    finally:
+        heads.close()

@@ -4,12 +4,16 @@ Callers that cannot call cudaMalloc (graph capture, frameworks that own all
 device memory, allocation-free hot loops) use lstm_layer_forward_static,
 whose gate buffer is a fixed array inside the library.  Its output must match
 the allocating step entry points (lstm_projection + lstm_recurrence with a
-caller-owned gate buffer) on two calls in a row that share that array.  This
-file is collected last so that a failure here leaves every other test run.
+caller-owned gate buffer) on two calls in a row that share that array: within
+the stack's tolerance, and in fact bit for bit, since both run the same
+kernels on the same inputs.  Both are also checked against the float64
+oracle's layer.  This file is collected last so that a failure here leaves
+every other test run.
 """
 import numpy as np
 import pytest
 
+import oracle
 from bidirectional_lstm_stack_gb300 import binding, synthetic
 from gpu_util import assert_within, cuda
 
@@ -43,7 +47,12 @@ def test_static_layer_matches_allocating_entry_points_twice():
         binding.lstm_layer_forward_static(x, batch, steps, in_width, d["wp_hi"], d["wp_lo"], kp,
                                           d["rp"], d["bias"], y)
         torch.cuda.synchronize()
-        assert_within(y.cpu().numpy(), ref, what=f"static layer b{batch} t{steps} k{in_width}")
+        got = y.cpu().numpy()
+        what = f"static layer b{batch} t{steps} k{in_width}"
+        assert_within(got, ref, what=what)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), what
+        x64 = x.cpu().numpy().astype(np.float64)
+        assert_within(got, oracle.lstm_stack(x64, [lay]), what=what + " vs oracle")
     assert binding.lstm_fault_status() == 0
 
 
