@@ -48,44 +48,63 @@ namespace {
 constexpr int BM = 128;  // rows per tile (MMA M)
 constexpr int BK = 16;   // fp32 per K block = 64 bytes
 constexpr int A_BYTES = BM * BK * 4;                     // 8 KiB
-constexpr int RING_BYTES = 192 * 1024;                   // the K-block stage ring
+// Shared memory: [resident W tile] [K-block stage ring] [the epilogue's
+// store staging: 4 warps x 2 slices of 4 KiB] [barriers]; 224 KiB of data.
+constexpr int DATA_BYTES = 224 * 1024;
+constexpr int OUT_COLS = 32;                             // columns per store slice
+constexpr int OUT_BYTES = 32 * OUT_COLS * 4;             // one warp's 32 rows: 4 KiB
+constexpr int OUT_OFFSET = DATA_BYTES - 4 * 2 * OUT_BYTES;
 constexpr int MAX_STAGES = 8;
 constexpr int CONVERTERS = 128;                          // warps 0-3
 constexpr int EPILOGUE = 128;                            // warps 4-7
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
-constexpr int OUT_COLS = 32;                             // columns per store slice
-constexpr int OUT_BYTES = 32 * OUT_COLS * 4;             // one warp's 32 rows: 4 KiB
-constexpr int OUT_OFFSET = RING_BYTES;                   // staging: 4 warps x 2 slices
-constexpr size_t SMEM_BYTES = OUT_OFFSET + 4 * 2 * OUT_BYTES + 1024 + 256;
+constexpr size_t SMEM_BYTES = DATA_BYTES + 1024 + 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+// K blocks a resident W tile holds: K <= 64 (the first layer's 60 inputs)
+constexpr int RESIDENT_KBLOCKS = 4;
 
 // One instantiation: tiles of BN gate columns, 3xTF32 or single products.
-template <int BN_, bool SINGLE_>
+// RESIDENT_W (K <= 64): a CTA's W tile stays in shared memory for all its
+// tiles and the ring carries only X.  With 4 K blocks per tile, reloading
+// the 128 KiB W tile (hi and lo) for every 128-row tile made the loads, not
+// the tensor pipe, the limit.  The grid is then a multiple of the column
+// tiles, so a CTA's tiles t, t + grid, ... share one column tile.
+template <int BN_, bool SINGLE_, bool RESIDENT_W_ = false>
 struct Shape {
     static constexpr int BN = BN_;  // MMA N: output columns per tile
     static constexpr bool SINGLE = SINGLE_;
+    static constexpr bool RESIDENT_W = RESIDENT_W_;
     static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int PLANES = SINGLE ? 1 : 2;                // W hi (and lo)
+    static constexpr int W_RES_BYTES = RESIDENT_W ? RESIDENT_KBLOCKS * PLANES * B_BYTES : 0;
+    static constexpr int RING_BYTES = OUT_OFFSET - W_RES_BYTES;
     // 3xTF32 keeps A hi, A lo, B hi, B lo per stage; the single-product
-    // mode only A hi and B hi, so the same ring holds twice the K blocks
-    static constexpr int STAGE_BYTES = SINGLE ? A_BYTES + B_BYTES : 2 * (A_BYTES + B_BYTES);
+    // mode only A hi and B hi, so the same ring holds twice the K blocks;
+    // with a resident W the stages hold only A
+    static constexpr int A_STAGE_BYTES = SINGLE ? A_BYTES : 2 * A_BYTES;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + (RESIDENT_W ? 0 : PLANES * B_BYTES);
     static constexpr int STAGES =
         RING_BYTES / STAGE_BYTES < MAX_STAGES ? RING_BYTES / STAGE_BYTES : MAX_STAGES;
     static constexpr int A_LO = A_BYTES;                         // 3xTF32 only
-    static constexpr int B_HI = SINGLE ? A_BYTES : 2 * A_BYTES;
+    static constexpr int B_HI = A_STAGE_BYTES;                   // in the stage (not RESIDENT_W)
     static constexpr int B_LO = B_HI + B_BYTES;                  // 3xTF32 only
-    static constexpr uint32_t TX_BYTES = SINGLE ? A_BYTES + B_BYTES : A_BYTES + 2 * B_BYTES;
+    static constexpr uint32_t TX_BYTES = A_BYTES + (RESIDENT_W ? 0 : PLANES * B_BYTES);
     static constexpr uint32_t ACC_COLS = BN;                     // per accumulator
     static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
     static constexpr int TILES_N = kGateColumns / BN;
     static constexpr uint32_t IDESC = ptx::tf32_idesc(BM, BN);
-    static_assert(STAGE_BYTES % 1024 == 0 && BN % 16 == 0 && BN <= 256 && STAGES >= 4,
+    static_assert(STAGE_BYTES % 1024 == 0 && BN % 16 == 0 && BN <= 256 && STAGES >= 4 &&
+                      W_RES_BYTES % 1024 == 0,
                   "tile shape");
 };
 using GatesShape = Shape<256, false>;
 using GatesTf32Shape = Shape<256, true>;
 using GatesNarrowShape = Shape<128, false>;  // few rows: twice the tiles
+using GatesResidentShape = Shape<256, false, true>;        // K <= 64
+using GatesTf32ResidentShape = Shape<256, true, true>;     // K <= 64
+using GatesNarrowResidentShape = Shape<128, false, true>;  // K <= 64
 static_assert(GatesShape::BN == kProjectionWBoxRows && BM == kProjectionBoxRows &&
                   GatesNarrowShape::BN == kProjectionNarrowWBoxRows,
               "TMA boxes");
@@ -118,12 +137,13 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + OUT_OFFSET + 4 * 2 * OUT_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + DATA_BYTES);
     uint64_t *conv = full + MAX_STAGES;
     uint64_t *empty = conv + MAX_STAGES;
     uint64_t *acc_full = empty + MAX_STAGES;  // [2]
     uint64_t *acc_empty = acc_full + 2;       // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *w_full = acc_empty + 2;         // the resident W tile landed (RESIDENT_W)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(w_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *progress = abort_flag + 1;  // K blocks whose MMAs were issued
 
@@ -140,6 +160,7 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             ptx::mbar_init(&acc_full[a], 1);
             ptx::mbar_init(&acc_empty[a], EPILOGUE);
         }
+        ptx::mbar_init(w_full, 1);
         *abort_flag = 0;
         *progress = 0;
         ptx::fence_mbar_init();
@@ -161,12 +182,26 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     const int first = static_cast<int>(blockIdx.x);
     const int stride = static_cast<int>(gridDim.x);
     long issued = 0;            // producer: K blocks whose loads were issued
+    bool w_issued = false;      // producer: the resident W tile's loads were issued
+    uint8_t *const ring = smem + S::W_RES_BYTES;
     int committed_tiles = 0;    // MMA: accumulators committed
 
     if (warp == PRODUCER_WARP) {
         // failure test (`withhold`): nothing is loaded, so the converters'
         // waits run out
         if (lane == 0 && !withhold) {
+            if constexpr (S::RESIDENT_W) {
+                // this CTA's column tile, all its K blocks, once
+                const int n0 = (first % TILES_N) * BN;
+                ptx::mbar_arrive_expect_tx(w_full, kblocks * S::PLANES * S::B_BYTES);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    ptx::tma_load_2d(smem + kb * S::B_BYTES, &whi_map, w_full, kb * BK, n0);
+                    if constexpr (!SINGLE)
+                        ptx::tma_load_2d(smem + (RESIDENT_KBLOCKS + kb) * S::B_BYTES, &wlo_map,
+                                         w_full, kb * BK, n0);
+                }
+                w_issued = true;
+            }
             long kbi = 0;
             for (int t = first; t < tiles && !*abort_flag; t += stride) {
                 const int m0 = (t / TILES_N) * BM;
@@ -177,12 +212,14 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     if (n > 0 && !ptx::mbar_wait_bounded(&empty[s], (n - 1) & 1, abort_flag, fault,
                                                          kFaultProducer, wait_limit_ns))
                         break;
-                    uint8_t *st = smem + s * STAGE_BYTES;
+                    uint8_t *st = ring + s * STAGE_BYTES;
                     ptx::mbar_arrive_expect_tx(&full[s], RG::TX_BYTES);
                     ptx::tma_load_2d(st, &x_map, &full[s], kb * BK, m0);
-                    ptx::tma_load_2d(st + RG::B_HI, &whi_map, &full[s], kb * BK, n0);
-                    if constexpr (!SINGLE)
-                        ptx::tma_load_2d(st + RG::B_LO, &wlo_map, &full[s], kb * BK, n0);
+                    if constexpr (!S::RESIDENT_W) {
+                        ptx::tma_load_2d(st + RG::B_HI, &whi_map, &full[s], kb * BK, n0);
+                        if constexpr (!SINGLE)
+                            ptx::tma_load_2d(st + RG::B_LO, &wlo_map, &full[s], kb * BK, n0);
+                    }
                     issued = kbi + 1;
                 }
             }
@@ -191,7 +228,12 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         if (lane == 0) {
             long kbi = 0;
             int ti = 0;
-            for (int t = first; t < tiles && !*abort_flag; t += stride, ++ti) {
+            // the resident W tile has landed (its wait, like every other, is
+            // bounded: a failure here skips the tile loop)
+            const bool w_ok = !S::RESIDENT_W ||
+                              ptx::mbar_wait_bounded(w_full, 0, abort_flag, fault, kFaultMma,
+                                                     wait_limit_ns);
+            for (int t = first; w_ok && t < tiles && !*abort_flag; t += stride, ++ti) {
                 const int a = ti & 1;
                 const uint32_t use = static_cast<uint32_t>(ti >> 1);
                 if (use > 0 && !ptx::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, abort_flag,
@@ -209,10 +251,16 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t a_hi = ptx::smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t a_hi = ptx::smem_u32(ring + s * STAGE_BYTES);
                     const uint32_t a_lo = a_hi + RG::A_LO;
-                    const uint32_t b_hi = a_hi + RG::B_HI;
-                    const uint32_t b_lo = a_hi + RG::B_LO;
+                    const uint32_t w_res = ptx::smem_u32(smem);
+                    const uint32_t b_hi = S::RESIDENT_W
+                                              ? w_res + static_cast<uint32_t>(kb * S::B_BYTES)
+                                              : a_hi + RG::B_HI;
+                    const uint32_t b_lo =
+                        S::RESIDENT_W
+                            ? w_res + static_cast<uint32_t>((RESIDENT_KBLOCKS + kb) * S::B_BYTES)
+                            : a_hi + RG::B_LO;
 #pragma unroll
                     for (int j = 0; j < BK / 8; ++j) {
                         const uint32_t off = j * 32;  // 8 TF32 = 32 bytes along K
@@ -249,8 +297,8 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
                     ok = false;
                     break;
                 }
-                float4 *a = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES);
-                float4 *alo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + RG::A_LO);
+                float4 *a = reinterpret_cast<float4 *>(ring + s * STAGE_BYTES);
+                float4 *alo = reinterpret_cast<float4 *>(ring + s * STAGE_BYTES + RG::A_LO);
                 if constexpr (SINGLE) {
 #pragma unroll
                     for (int i = 0; i < A_BYTES / 16 / CONVERTERS; ++i) {
@@ -350,6 +398,8 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
         // every issued TMA load has landed before the CTA's shared memory goes away
         for (long kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
             drain_wait(&full[kb % STAGES], static_cast<uint32_t>(kb / STAGES) & 1, fault);
+        if (w_issued)
+            drain_wait(w_full, 0, fault);
     }
     if (warp == MMA_WARP) {
         if (lane == 0) {
@@ -423,6 +473,9 @@ const void *const kKernels[] = {
     reinterpret_cast<const void *>(&projection_kernel<GatesShape>),
     reinterpret_cast<const void *>(&projection_kernel<GatesTf32Shape>),
     reinterpret_cast<const void *>(&projection_kernel<GatesNarrowShape>),
+    reinterpret_cast<const void *>(&projection_kernel<GatesResidentShape>),
+    reinterpret_cast<const void *>(&projection_kernel<GatesTf32ResidentShape>),
+    reinterpret_cast<const void *>(&projection_kernel<GatesNarrowResidentShape>),
 };
 
 // Persistent grid over the row tiles (128 rows) times S::TILES_N column
@@ -442,7 +495,13 @@ int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     int st = cuda_status(cudaGetDevice(&dev), "current device");
     if (st != LSTM_OK)
         return st;
-    const int fit = (dev >= 0 && dev < 64 && g_max_ctas[dev] > 0) ? g_max_ctas[dev] : 148;
+    int fit = (dev >= 0 && dev < 64 && g_max_ctas[dev] > 0) ? g_max_ctas[dev] : 148;
+    if (S::RESIDENT_W) {
+        // a CTA's tiles (first, first + grid, ...) must share a column tile
+        if (kp > RESIDENT_KBLOCKS * BK)
+            return fail(LSTM_E_INVALID, "tensor-core GEMM: kp %d above the resident W tile", kp);
+        fit -= fit % S::TILES_N;
+    }
     const long grid = tiles < fit ? tiles : fit;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -514,8 +573,13 @@ int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, 
     int st = encode_store_map(&g_map, g, rows, kGateColumns);
     if (st != LSTM_OK)
         return st;
+    // few K blocks per tile: the W tile stays resident (see Shape)
+    const bool resident = kp <= RESIDENT_KBLOCKS * BK;
     if (math == LSTM_MATH_TF32)
-        return launch_tiles<GatesTf32Shape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream);
+        return resident ? launch_tiles<GatesTf32ResidentShape>(x_map, w.hi, w.lo, g_map, rows, kp,
+                                                                fault, stream)
+                        : launch_tiles<GatesTf32Shape>(x_map, w.hi, w.lo, g_map, rows, kp, fault,
+                                                       stream);
     // When the 256-column tiles would fill at most half of the CTAs that run
     // at once, 128-column tiles give every CTA half the work on twice as many
     // SMs.
@@ -525,9 +589,13 @@ int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, 
     const int fit = (dev >= 0 && dev < 64 && g_max_ctas[dev] > 0) ? g_max_ctas[dev] : 148;
     const long tiles = (static_cast<long>(rows) + BM - 1) / BM * GatesShape::TILES_N;
     if (2 * tiles <= fit)
-        return launch_tiles<GatesNarrowShape>(x_map, w.hi_narrow, w.lo_narrow, g_map, rows, kp,
-                                              fault, stream);
-    return launch_tiles<GatesShape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream);
+        return resident ? launch_tiles<GatesNarrowResidentShape>(x_map, w.hi_narrow, w.lo_narrow,
+                                                                 g_map, rows, kp, fault, stream)
+                        : launch_tiles<GatesNarrowShape>(x_map, w.hi_narrow, w.lo_narrow, g_map,
+                                                         rows, kp, fault, stream);
+    return resident ? launch_tiles<GatesResidentShape>(x_map, w.hi, w.lo, g_map, rows, kp, fault,
+                                                       stream)
+                    : launch_tiles<GatesShape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream);
 }
 
 } // namespace lstm

@@ -45,6 +45,32 @@ def test_projection_matches_oracle(weights, in_width, rows):
     assert binding.lstm_fault_status() == 0
 
 
+@pytest.mark.parametrize("in_width,kp,rows", [(60, 64, 20011), (20, 32, 20011), (60, 64, 150)])
+def test_projection_resident_w_tiles(weights, in_width, kp, rows):
+    # K <= 64 keeps each CTA's W tile resident in shared memory across all of
+    # its row tiles: rows enough for several tiles per CTA (and a ragged
+    # last tile), one or two K blocks of 16 per 32 columns, and a grid
+    # smaller than the device
+    import torch
+    rng = np.random.default_rng(rows + in_width)
+    if in_width == 60:
+        w = weights[0]["w"]
+    else:
+        w = rng.uniform(-0.1, 0.1, (2, 512, in_width)).astype(np.float32)
+    r = np.zeros((2, 512, 128), np.float32)
+    b = np.zeros((2, 1024), np.float32)
+    wp_hi, wp_lo, _, _ = binding.lstm_pack_layer(w, r, b, in_width, kp)
+    x = synthetic.random_matrix(rows + 5, (rows, in_width))
+    g_all = torch.full((rows + 3, 1024), float("nan"), device="cuda")
+    g = g_all[:rows]
+    binding.lstm_projection(cuda(x), rows, in_width, cuda(wp_hi), cuda(wp_lo), kp, g)
+    torch.cuda.synchronize()
+    assert torch.isnan(g_all[rows:]).all()
+    assert_within(g.cpu().numpy(), oracle.projection(x, w), atol=1e-5, rtol=1e-5,
+                  what=f"resident-W projection {in_width}x{rows}")
+    assert binding.lstm_fault_status() == 0
+
+
 def test_projection_large_inputs_exercise_the_lo_plane(weights):
     # inputs of magnitude ~100 make the dropped lo terms visible if any product
     # of the split were missing
