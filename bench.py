@@ -112,29 +112,21 @@ def time_heads(heads, y, steps, warmup, flush, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def time_recurrence_pair(fn, g, rp, bias, y, batch, steps, reps, warmup, flush, stream, side):
-    """Per-step device time (us) of one layer's two recurrences (forward on
-    `stream`, reverse on `side`, started together and joined, as the stack
-    runs them), through `fn` (lstm_recurrence or lstm_recurrence_floor), L2
-    flushed before each pair; the median over `reps` pairs."""
+def time_recurrence_layer(fn, g, rp, bias, y, batch, steps, reps, warmup, flush, stream):
+    """Per-step device time (us) of one layer's recurrence, both directions
+    in one launch as the stack runs them, through `fn` (lstm_recurrence or
+    lstm_recurrence_floor), L2 flushed before each launch; the median over
+    `reps` launches."""
     import torch
-
-    def pair():
-        fn(g, rp[0], bias[0], y, batch, steps, 0, stream)
-        fn(g, rp[1], bias[1], y, batch, steps, 1, side)
-
+    from bidirectional_lstm_stack_gb300 import binding
     times = []
     for i in range(warmup + reps):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        joined = torch.cuda.Event()
         with torch.cuda.stream(stream):
             flush.fill_(i)
             e0.record(stream)
-        side.wait_event(e0)
-        pair()
-        joined.record(side)
-        stream.wait_event(joined)
+        fn(g, rp, bias, y, batch, steps, binding.LSTM_BOTH_DIRECTIONS, stream)
         e1.record(stream)
         e1.synchronize()
         if i >= warmup:
@@ -142,7 +134,7 @@ def time_recurrence_pair(fn, g, rp, bias, y, batch, steps, reps, warmup, flush, 
     return float(np.median(times))
 
 
-def recurrence_floor(layer, x, stream, side, flush, reps=5, warmup=3):
+def recurrence_floor(layer, x, stream, flush, reps=5, warmup=3):
     """The recurrence's per-step time and its latency floor on the same
     launch shape, both directions running together: the layer's projection
     of x feeds both; the floor is lstm_recurrence_floor (the same kernel with
@@ -160,10 +152,10 @@ def recurrence_floor(layer, x, stream, side, flush, reps=5, warmup=3):
     y = torch.empty((B, T, 2 * H), device=dev)
     binding.lstm_projection(x, B * T, F, whi, wlo, kp, g, stream)
     torch.cuda.synchronize()
-    full = time_recurrence_pair(binding.lstm_recurrence, g, rp_d, bias_d, y, B, T, reps, warmup,
-                                flush, stream, side)
-    floor = time_recurrence_pair(binding.lstm_recurrence_floor, g, rp_d, bias_d, y, B, T, reps,
-                                 warmup, flush, stream, side)
+    full = time_recurrence_layer(binding.lstm_recurrence, g, rp_d, bias_d, y, B, T, reps, warmup,
+                                 flush, stream)
+    floor = time_recurrence_layer(binding.lstm_recurrence_floor, g, rp_d, bias_d, y, B, T, reps,
+                                  warmup, flush, stream)
     # the floor's outputs are meaningless, but no wait of either kernel may
     # have run out (that would void both times)
     bits = binding.lstm_fault_status()
@@ -172,10 +164,11 @@ def recurrence_floor(layer, x, stream, side, flush, reps=5, warmup=3):
     return full, floor
 
 
-def flops_recurrence_launch(batch: int, steps: int) -> float:
-    """Algorithmic flops of one recurrence launch (one direction, one layer):
-    the 512 x 128 matrix-vector product per window and step."""
-    return 2.0 * batch * steps * 4 * H * H
+def flops_recurrence_launch(batch: int, steps: int, directions: int = 2) -> float:
+    """Algorithmic flops of one recurrence launch (one layer; the stack runs
+    both directions in one launch): the 512 x 128 matrix-vector product per
+    window, step and direction."""
+    return 2.0 * batch * steps * 4 * H * H * directions
 
 
 class ClockSampler:
@@ -411,9 +404,8 @@ def run_ours(args):
     # the step's arithmetic removed), both directions together, on the
     # workload and on the one-window latency case; and the tensor cores'
     # measured kind::tf32 rate, the projection's and the heads' denominator
-    side = torch.cuda.Stream()
-    rec_full_us, rec_floor_us = recurrence_floor(layers[0], x, stream, side, flush)
-    rec1_full_us, rec1_floor_us = recurrence_floor(layers[0], x1, stream, side, flush)
+    rec_full_us, rec_floor_us = recurrence_floor(layers[0], x, stream, flush)
+    rec1_full_us, rec1_floor_us = recurrence_floor(layers[0], x1, stream, flush)
     tf32_rate = binding.lstm_tf32_rate(dev)
 
     # end to end through the host-buffer entry point (pinned host memory)
@@ -453,7 +445,7 @@ def run_ours(args):
     # dominant kernel: the recurrence (per launch = one direction of one layer)
     p, peak_kind = peaks()
     clk = clocks.summary()
-    rec_ms = float(np.mean(phases[:, 1:]))   # mean over layers and both directions
+    rec_ms = float(np.mean(phases[:, 1]))    # mean over layers (one launch, both directions)
     proj_ms = float(np.mean(phases[:, 0]))
     sm_mhz = clk.get("sm_mhz") or 2070.0
     fp32_peak_tflops = SMS * FP32_LANES * 2 * (clk.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
@@ -487,27 +479,26 @@ def run_ours(args):
         "latency_b1": {"workload": lat.name, "ms_per_window": ms1_step,
                        "windows_per_s": 1e3 / ms1_step,
                        "us_per_step": ms1_step * 1e3 / (LAYERS * lat.steps),
-                       "recurrence_us_per_step": float(np.mean(ph1[:, 1:])) * 1e3 / lat.steps,
+                       "recurrence_us_per_step": float(np.mean(ph1[:, 1])) * 1e3 / lat.steps,
                        "phases_ms": {"projection": [round(float(v), 4) for v in ph1[:, 0]],
-                                     "recurrence_fwd": [round(float(v), 4) for v in ph1[:, 1]],
-                                     "recurrence_rev": [round(float(v), 4) for v in ph1[:, 2]]},
+                                     "recurrence": [round(float(v), 4) for v in ph1[:, 1]]},
                        "gaps_ms": ph1_total - float(np.sum(ph1[:, 0]) +
-                                                   np.sum(np.maximum(ph1[:, 1], ph1[:, 2]))),
+                                                   np.sum(ph1[:, 1])),
                        "recurrence_pair_us_per_step": rec1_full_us,
                        "floor_us_per_step": rec1_floor_us,
                        "vs_floor": rec1_full_us / rec1_floor_us,
                        "context": "pages: A100, TF32-projection stack, 3.21-4.13 ms per window"},
         "gaps_ms": phases_total - float(np.sum(phases[:, 0]) +
-                                        np.sum(np.maximum(phases[:, 1], phases[:, 2]))),
+                                        np.sum(phases[:, 1])),
         "phases_pass_ms_per_step": phases_total,
         "phases_ms": {"projection": [round(float(v), 4) for v in phases[:, 0]],
-                      "recurrence_fwd": [round(float(v), 4) for v in phases[:, 1]],
-                      "recurrence_rev": [round(float(v), 4) for v in phases[:, 2]]},
-        "roofline": {"kernel": "recurrence (one direction, one layer)", "bound": "alu",
+                      "recurrence": [round(float(v), 4) for v in phases[:, 1]]},
+        "roofline": {"kernel": "recurrence (one layer, both directions in one launch)",
+                     "bound": "alu",
                      "achieved": rec_achieved, "peak": fp32_peak_tflops, "unit": "TFLOP/s",
                      "frac": rec_achieved / fp32_peak_tflops,
                      "traffic": ncu_traffic("recurrence", wl.batch * wl.steps),
-                     "algorithmic_bytes": float(wl.batch * wl.steps * (512 + 128) * 4),
+                     "algorithmic_bytes": float(2 * wl.batch * wl.steps * (512 + 128) * 4),
                      "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock",
                      "us_per_step": rec_us_per_step,
                      "pair_us_per_step": rec_full_us,
@@ -515,7 +506,7 @@ def run_ours(args):
                      "vs_floor": rec_full_us / rec_floor_us,
                      "floor_source": "lstm_recurrence_floor: the same variant, grid, exchange "
                                      "and waits with the step's arithmetic removed; both "
-                                     "directions together, L2 flushed, median of 5"},
+                                     "directions in one launch, L2 flushed, median of 5"},
         "roofline_projection": {"kernel": "projection (one layer, both directions)",
                                 "bound": "tensor", "achieved": proj_achieved, "peak": proj_peak,
                                 "unit": "TFLOP/s", "frac": proj_achieved / proj_peak,
@@ -540,7 +531,7 @@ def run_ours(args):
                 "mode": "forward_host_async, steps enqueued back to back (copies of one step "
                         "overlap the next forward), host clock around all steps",
                 "serial_value": e2e_serial},
-        "gpu_launches": 12 * args.steps,
+        "gpu_launches": 8 * args.steps,  # per forward: 4 projections, 4 two-direction recurrences
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -33,6 +33,7 @@ LSTM_MATH_3XTF32 = 0
 LSTM_MATH_TF32 = 1
 LSTM_GATES_IFGO = 0
 LSTM_GATES_IOFC = 1
+LSTM_BOTH_DIRECTIONS = 2
 
 _c_float_p = ctypes.POINTER(ctypes.c_float)
 _vp = ctypes.c_void_p

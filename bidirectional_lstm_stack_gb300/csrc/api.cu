@@ -7,9 +7,14 @@
 // per layer, the projection and then both directions' recurrences, the
 // reverse one on a side stream joined back before the next layer).  What
 // differs: the projection runs once per layer for both directions (N = 1024),
-// the layers ping-pong between two scratch buffers instead of overwriting the
-// output in place, and there is no exchange buffer to clear (the recurrence
-// exchanges h through distributed shared memory).
+// both directions' recurrences are one launch (their clusters alternate in
+// one grid) on the caller's stream, so a forward is one chain of eight
+// kernels instead of a fork and join per layer, each projection allowed to
+// start while the recurrence before it ends (programmatic dependent
+// launch); the layers
+// ping-pong between two scratch buffers instead of overwriting the output in
+// place; and there is no exchange buffer to clear (the recurrence exchanges h
+// through distributed shared memory).
 #include <stdarg.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -263,9 +268,6 @@ struct lstm_stack {
     CUtensorMap map_x;
     const float *map_x_base = nullptr;
     long map_x_rows = -1;
-    cudaStream_t side = nullptr;
-    cudaEvent_t fork[kLayers] = {};
-    cudaEvent_t join[kLayers] = {};
     bool timing = false;
     bool timed_once = false;
     cudaEvent_t phase[kPhaseEvents] = {};
@@ -368,12 +370,6 @@ extern "C" void lstm_stack_destroy(lstm_stack *s)
         cudaStreamDestroy(s->copy_in);
     if (s->copy_out)
         cudaStreamDestroy(s->copy_out);
-    for (int l = 0; l < kLayers; ++l) {
-        if (s->fork[l])
-            cudaEventDestroy(s->fork[l]);
-        if (s->join[l])
-            cudaEventDestroy(s->join[l]);
-    }
     for (int i = 0; i < kPhaseEvents; ++i)
         if (s->phase[i])
             cudaEventDestroy(s->phase[i]);
@@ -382,8 +378,6 @@ extern "C" void lstm_stack_destroy(lstm_stack *s)
             cudaGraphExecDestroy(gr.exec);
     if (s->capture)
         cudaStreamDestroy(s->capture);
-    if (s->side)
-        cudaStreamDestroy(s->side);
     delete s;
 }
 
@@ -501,8 +495,6 @@ extern "C" int lstm_stack_create_ordered(const lstm_stack_weights *weights, int 
     for (int i = 0; i < 2 && st == LSTM_OK; ++i)
         st = encode_matrix_map(&s->map_ping[i], s->ping[i], max_rows, kOutput, kProjectionBoxRows);
     if (st == LSTM_OK)
-        st = cuda_status(cudaStreamCreateWithFlags(&s->side, cudaStreamNonBlocking), "side stream");
-    if (st == LSTM_OK)
         st = cuda_status(cudaStreamCreateWithFlags(&s->capture, cudaStreamNonBlocking),
                          "capture stream");
     if (st == LSTM_OK)
@@ -515,11 +507,6 @@ extern "C" int lstm_stack_create_ordered(const lstm_stack_weights *weights, int 
         for (cudaEvent_t *e : {&s->staged[k], &s->computed[k], &s->returned[k]})
             if (st == LSTM_OK)
                 st = cuda_status(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "event");
-    }
-    for (int l = 0; l < kLayers && st == LSTM_OK; ++l) {
-        st = cuda_status(cudaEventCreateWithFlags(&s->fork[l], cudaEventDisableTiming), "event");
-        if (st == LSTM_OK)
-            st = cuda_status(cudaEventCreateWithFlags(&s->join[l], cudaEventDisableTiming), "event");
     }
     for (int i = 0; i < kPhaseEvents && st == LSTM_OK; ++i)
         st = cuda_status(cudaEventCreate(&s->phase[i]), "phase event");
@@ -568,51 +555,34 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
         s->map_x_rows = rows;
     }
     // phase events are recorded as external events, so they also fire when the
-    // pass is replayed from a captured graph
+    // pass is replayed from a captured graph; the recurrence of both
+    // directions is one launch, so its time fills both recurrence slots
     auto ev = [&](int layer, int part, int end) { return s->phase[(layer * 3 + part) * 2 + end]; };
+    auto mark = [&](int layer, int part, int end) -> int {
+        if (!s->timing)
+            return LSTM_OK;
+        return cuda_status(cudaEventRecordWithFlags(ev(layer, part, end), stream,
+                                                    cudaEventRecordExternal),
+                           "event");
+    };
     for (int l = 0; l < kLayers; ++l) {
         const CUtensorMap &src = l == 0 ? s->map_x : s->map_ping[(l - 1) & 1];
         float *dst = l == kLayers - 1 ? y : s->ping[l & 1];
-        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 0, 0), stream, cudaEventRecordExternal), "event")))
+        if ((st = mark(l, 0, 0)))
             return st;
         st = launch_projection(src, s->map_w[l], s->gates, static_cast<int>(rows), s->kp[l],
                                s->math, s->fault, stream);
         if (st != LSTM_OK)
             return st;
-        if (s->timing && (st = cuda_status(cudaEventRecordWithFlags(ev(l, 0, 1), stream, cudaEventRecordExternal), "event")))
+        if ((st = mark(l, 0, 1)) || (st = mark(l, 1, 0)) || (st = mark(l, 2, 0)))
             return st;
-        if ((st = cuda_status(cudaEventRecord(s->fork[l], stream), "fork record")) ||
-            (st = cuda_status(cudaStreamWaitEvent(s->side, s->fork[l], 0), "fork wait")))
+        // forward and reverse in one grid on the caller's stream: the next
+        // layer's projection follows it on the same stream
+        if ((st = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps,
+                                    kBothDirections, s->fault, stream)))
             return st;
-        // The side stream is forked from here: whatever fails below, it is
-        // joined back before returning (a capture must end joined, and the
-        // caller's stream must not run ahead of work on the side stream).
-        auto directions = [&]() -> int {
-            int r;
-            if (s->timing && (r = cuda_status(cudaEventRecordWithFlags(ev(l, 1, 0), stream, cudaEventRecordExternal), "event")))
-                return r;
-            if ((r = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps, 0,
-                                       s->fault, stream)))
-                return r;
-            if (s->timing && (r = cuda_status(cudaEventRecordWithFlags(ev(l, 1, 1), stream, cudaEventRecordExternal), "event")))
-                return r;
-            if (s->timing && (r = cuda_status(cudaEventRecordWithFlags(ev(l, 2, 0), s->side, cudaEventRecordExternal), "event")))
-                return r;
-            if ((r = launch_recurrence(s->gates, s->rp[l] + kGates * kHidden, s->bias[l] + kGates,
-                                       dst, batch, steps, 1, s->fault, s->side)))
-                return r;
-            if (s->timing && (r = cuda_status(cudaEventRecordWithFlags(ev(l, 2, 1), s->side, cudaEventRecordExternal), "event")))
-                return r;
-            return LSTM_OK;
-        };
-        st = directions();
-        int jst = cuda_status(cudaEventRecord(s->join[l], s->side), "join record");
-        if (jst == LSTM_OK)
-            jst = cuda_status(cudaStreamWaitEvent(stream, s->join[l], 0), "join wait");
-        if (st != LSTM_OK)
+        if ((st = mark(l, 1, 1)) || (st = mark(l, 2, 1)))
             return st;
-        if (jst != LSTM_OK)
-            return jst;
     }
     if (s->timing)
         s->timed_once = true;
@@ -625,7 +595,7 @@ namespace {
 
 // Runs the forward pass on `stream` by replaying a CUDA graph of it: the
 // first call with a given (x, y, batch, steps, timing, math) records the launches
-// and the fork/join events on a private stream and instantiates the graph;
+// on a private stream and instantiates the graph;
 // later calls only launch it.  When `stream` is itself being captured (the
 // caller is building a graph) or replay is off, the launches are enqueued
 // directly.
@@ -883,8 +853,10 @@ int recurrence_args(const float *g, const float *rp, const float *bias, float *y
         return fail(LSTM_E_INVALID, "lstm_recurrence: null pointer");
     if (batch <= 0 || steps <= 0)
         return fail(LSTM_E_INVALID, "lstm_recurrence: batch %d, steps %d", batch, steps);
-    if (direction != 0 && direction != 1)
-        return fail(LSTM_E_INVALID, "lstm_recurrence: direction %d (0 forward, 1 reverse)", direction);
+    if (direction != 0 && direction != 1 && direction != LSTM_BOTH_DIRECTIONS)
+        return fail(LSTM_E_INVALID,
+                    "lstm_recurrence: direction %d (0 forward, 1 reverse, %d both)", direction,
+                    LSTM_BOTH_DIRECTIONS);
     if (static_cast<long>(batch) * steps > 65535L * 128)
         return fail(LSTM_E_OVERFLOW, "lstm_recurrence: %d x %d rows exceed %ld", batch, steps,
                     65535L * 128);
@@ -893,6 +865,12 @@ int recurrence_args(const float *g, const float *rp, const float *bias, float *y
         (st = check_aligned(y, "y")) || (st = pointer_device(g, dev)))
         return st;
     return prepare_device(*dev);
+}
+
+// The public direction (0, 1, LSTM_BOTH_DIRECTIONS) as the launchers take it.
+int launch_direction(int direction)
+{
+    return direction == LSTM_BOTH_DIRECTIONS ? kBothDirections : direction;
 }
 }  // namespace
 
@@ -907,7 +885,7 @@ extern "C" int lstm_recurrence(const float *g, const float *rp, const float *bia
     unsigned *fault = fault_word();
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
-    return launch_recurrence(g, rp, bias, y, batch, steps, direction, fault,
+    return launch_recurrence(g, rp, bias, y, batch, steps, launch_direction(direction), fault,
                              static_cast<cudaStream_t>(stream));
 }
 
@@ -922,7 +900,7 @@ extern "C" int lstm_recurrence_floor(const float *g, const float *rp, const floa
     unsigned *fault = fault_word();
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
-    return launch_recurrence_floor(g, rp, bias, y, batch, steps, direction, fault,
+    return launch_recurrence_floor(g, rp, bias, y, batch, steps, launch_direction(direction), fault,
                                    static_cast<cudaStream_t>(stream));
 }
 
@@ -939,7 +917,7 @@ extern "C" int lstm_recurrence_variant(const float *g, const float *rp, const fl
     unsigned *fault = fault_word();
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
-    return launch_recurrence_variant(g, rp, bias, y, batch, steps, direction, cluster_size,
+    return launch_recurrence_variant(g, rp, bias, y, batch, steps, launch_direction(direction), cluster_size,
                                      windows_per_chunk, chunks, threads_per_block, fault,
                                      static_cast<cudaStream_t>(stream));
 }

@@ -122,6 +122,10 @@ int encode_store_map(CUtensorMap *map, float *base, long rows, int cols);
 constexpr int kHeadWBoxRows = 128;
 
 // ---- recurrence (recurrence.cu) ------------------------------------------
+// direction 0 (forward), 1 (reverse), or kBothDirections: one launch for
+// both, rp [2][512][128] and bias [2][512], forward and reverse clusters
+// alternating in the grid.
+constexpr int kBothDirections = -1;
 int launch_recurrence(const float *g, const float *rp, const float *bias,
                       float *y, int batch, int steps, int direction,
                       unsigned *fault, cudaStream_t stream);
@@ -412,6 +416,18 @@ __device__ __forceinline__ void cp_async_wait()
 __device__ __forceinline__ void cp_async_wait_all()
 {
     asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// Programmatic dependent launch: wait until the grid this one depends on
+// has completed and its memory is visible (returns at once when the kernel
+// was launched without the dependency), and let the grid that depends on this
+// one be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_arrive_release()
 {

@@ -178,6 +178,10 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    // Programmatic dependent launch: the set-up above overlaps the tail of
+    // the kernel before this one; X (that kernel's output) and G (which it
+    // may still read) are touched only after it has completed.
+    ptx::griddep_wait();
     const uint32_t tmem = *tmem_slot;
     const int first = static_cast<int>(blockIdx.x);
     const int stride = static_cast<int>(gridDim.x);
@@ -508,6 +512,11 @@ int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     const int kblocks = kp / BK;
     const int ntiles = static_cast<int>(tiles);
     const KernelTest test = kernel_test(kTestProjection);

@@ -108,8 +108,5 @@ extern "C" int lstm_layer_forward_static(const float *x, int batch, int steps, i
     if ((st = launch_projection(xm, w, gates, static_cast<int>(rows), kp, LSTM_MATH_3XTF32, fault,
                                 s)))
         return st;
-    if ((st = launch_recurrence(gates, rp, bias, y, batch, steps, 0, fault, s)))
-        return st;
-    return launch_recurrence(gates, rp + kGates * kHidden, bias + kGates, y, batch, steps, 1, fault,
-                             s);
+    return launch_recurrence(gates, rp, bias, y, batch, steps, kBothDirections, fault, s);
 }

@@ -101,7 +101,7 @@ typedef struct {
  * the device scratch for up to max_batch windows of up to max_steps steps
  * (gate buffer [rows][1024], two ping-pong layer buffers [rows][256], two
  * staging slots [rows][60] + [rows][256] for the host-memory entry points),
- * creates the side stream, the copy streams and the events.
+ * creates the copy streams and the events.
  * On success *out owns all of it.  Errors: LSTM_E_INVALID (null, sizes <= 0),
  * LSTM_E_OVERFLOW (max_batch*max_steps*1024 beyond 2^31 rows*cols),
  * LSTM_E_DEVICE (device is not compute capability 10.3 or lacks cluster
@@ -132,9 +132,11 @@ int lstm_stack_create_ordered(const lstm_stack_weights *weights, int gate_order,
  *       y[b][t][0:128] forward h, y[b][t][128:256] reverse h
  * x and y must not overlap each other or the stack's scratch.  Enqueued on
  * `stream`; never allocates device memory and does not synchronise.  Each
- * layer runs its projection, then the forward recurrence and, concurrently,
- * the reverse one (forked onto the stack's side stream and joined back
- * before the next layer).  The work is replayed from a CUDA graph: the first
+ * layer runs its projection, then the forward and the reverse recurrence
+ * together in one launch (the pages run the reverse one on a side stream
+ * beside the forward one, `recur`); each projection may start while the
+ * kernel before it ends and waits for it before touching its output
+ * (programmatic dependent launch).  The work is replayed from a CUDA graph: the first
  * call with a given (x, y, batch, steps) records and instantiates the graph
  * (driver-side host resources; up to 8 argument sets are kept, least
  * recently used evicted), later calls launch it.  If `stream` is being
@@ -178,11 +180,13 @@ int lstm_stack_forward_host(lstm_stack *s, const float *x_host, size_t x_len,
                             void *stream);
 
 /* Opt-in per-phase timing (the pages' `LstmPhases` hooks): when enabled,
- * every forward records CUDA events around each layer's projection (on the
- * caller's stream) and around each direction's recurrence (on the stream it
- * runs on).  lstm_stack_phase_times then waits for the last forward and
- * writes 12 milliseconds into ms[12]: for layer l, ms[3l] projection,
- * ms[3l+1] forward recurrence, ms[3l+2] reverse recurrence. */
+ * every forward records CUDA events around each layer's projection and
+ * around its recurrence (both on the caller's stream).  lstm_stack_phase_times
+ * then waits for the last forward and writes 12 milliseconds into ms[12]: for
+ * layer l, ms[3l] projection, ms[3l+1] and ms[3l+2] the recurrence (both
+ * directions run in one launch, so the two slots hold the same time).  The
+ * events sit between kernels that otherwise overlap their set-up with the
+ * previous kernel's tail, so a timed forward runs a little slower. */
 int lstm_stack_enable_phase_timing(lstm_stack *s, int enable);
 int lstm_stack_phase_times(lstm_stack *s, float *ms);
 
@@ -257,13 +261,21 @@ int lstm_projection_math(const float *x, int rows, int in_width,
                          const float *wp_hi, const float *wp_lo, int kp, float *g,
                          int math, void *stream);
 
+/* The direction argument of the recurrence entry points: 0 forward, 1
+ * reverse, or both in one launch (the stack's choice: forward and reverse
+ * clusters alternate in one grid). */
+#define LSTM_BOTH_DIRECTIONS 2
+
 /* Step 3, device: one direction's recurrence over one layer.
  *   g    : device [batch*steps][1024] projection from lstm_projection
  *          (row b*steps + t); this direction reads columns d*512 .. d*512+511
  *   rp   : device [512][128]  this direction's packed R (lstm_pack_layer)
  *   bias : device [512]       this direction's packed bias
  *   y    : device [batch][steps][256]; writes columns d*128 .. d*128+127 only
- *   direction : 0 forward (t = 0..steps-1), 1 reverse (t = steps-1..0)
+ *   direction : 0 forward (t = 0..steps-1), 1 reverse (t = steps-1..0), or
+ *          LSTM_BOTH_DIRECTIONS: both in one launch, rp then [2][512][128]
+ *          and bias [2][512] (both directions as lstm_pack_layer writes them)
+ *          and all 256 columns of y written
  * h and c start at zero for every window.  One thread-block cluster holds R
  * in its blocks' registers, split by hidden unit, and exchanges h through
  * distributed shared memory each step; the variant (cluster shape and
@@ -413,8 +425,7 @@ int lstm_test_fail_allocations(int skip, int count);
 
 /* After `skip` more kernel launches by the library, the next `count` fail
  * with LSTM_E_CUDA ("injected launch failure") instead of launching; the
- * call that hits one still joins its side stream, so the stack stays usable.
- * count 0 turns it off. */
+ * stack stays usable.  count 0 turns it off. */
 int lstm_test_fail_launches(int skip, int count);
 
 /* On `device`: with withhold != 0, CTA 0 of every recurrence cluster stops

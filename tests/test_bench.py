@@ -53,8 +53,10 @@ def test_warmup_below_three_is_refused():
 def test_flop_counts():
     # 2 * rows * 1024 * K over the four layers' K = 60, 256, 256, 256
     assert bench.flops_projection(10) == 2.0 * 10 * 1024 * (60 + 3 * 256)
-    # the 512 x 128 matrix-vector product per window and step
-    assert bench.flops_recurrence_launch(3, 7) == 2.0 * 3 * 7 * 512 * 128
+    # the 512 x 128 matrix-vector product per window, step and direction (one
+    # launch runs both directions)
+    assert bench.flops_recurrence_launch(3, 7) == 2.0 * 3 * 7 * 512 * 128 * 2
+    assert bench.flops_recurrence_launch(3, 7, directions=1) == 2.0 * 3 * 7 * 512 * 128
     assert bench.flops_heads(5) == 2.0 * 5 * (256 * 128 + 128 * 128 + 128 * 7)
 
 

@@ -106,6 +106,22 @@ def test_variants_are_bitwise_identical():
         assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)), v
 
 
+@pytest.mark.parametrize("batch,steps", [(1, 37), (5, 40), (33, 11), (130, 9)])
+def test_both_directions_in_one_launch(batch, steps):
+    # the stack's launch: forward and reverse clusters alternate in one grid;
+    # bitwise equal to the two directions launched one by one
+    import torch
+    lay, G, rp, bias = _layer_inputs(batch, steps, layer_index=1, seed=batch + steps)
+    one_by_one = _run(G, rp, bias, batch, steps)
+    g, rpt, bt = cuda(G), cuda(rp), cuda(bias)
+    y = torch.full((batch, steps, 256), float("nan"), device="cuda")
+    binding.lstm_recurrence(g, rpt, bt, y, batch, steps, binding.LSTM_BOTH_DIRECTIONS)
+    torch.cuda.synchronize()
+    both = y.cpu().numpy()
+    assert np.array_equal(both.view(np.uint32), one_by_one.view(np.uint32))
+    assert binding.lstm_fault_status() == 0
+
+
 def test_unknown_variant_is_rejected():
     import torch
     g = torch.zeros((4, 1024), device="cuda")
