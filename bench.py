@@ -164,6 +164,32 @@ def recurrence_floor(layer, x, stream, flush, reps=5, warmup=3):
     return full, floor
 
 
+FLOOR_TABLE_BATCHES = (1, 8, 32, 48, 64, 80, 128, 192, 256)
+
+
+def run_floor_table(args):
+    """The recurrence against its per-step latency floor at every batch size
+    of FLOOR_TABLE_BATCHES (T = 589, the default variant per batch, both
+    directions in one launch, L2 flushed); one JSON line."""
+    import torch
+    from bidirectional_lstm_stack_gb300 import binding
+    torch.cuda.set_device(0)
+    layers = synthetic.stack_weights()
+    stream = torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    steps = synthetic.WORKLOADS[WORKLOAD].steps
+    rows = []
+    for batch in FLOOR_TABLE_BATCHES:
+        x = torch.from_numpy(synthetic.random_matrix(batch, (batch, steps, 60))).cuda()
+        full, floor = recurrence_floor(layers[0], x, stream, flush)
+        rows.append({"batch": batch, "us_per_step": full, "floor_us_per_step": floor,
+                     "vs_floor": full / floor})
+    print(json.dumps({"floor_table": rows, "steps": steps,
+                      "note": "lstm_recurrence vs lstm_recurrence_floor, both directions in "
+                              "one launch, median of 5 after 3 warm-up launches"}))
+    return 0
+
+
 def flops_recurrence_launch(batch: int, steps: int, directions: int = 2) -> float:
     """Algorithmic flops of one recurrence launch (one layer; the stack runs
     both directions in one launch): the 512 x 128 matrix-vector product per
@@ -555,11 +581,16 @@ def main(argv=None):
                     help="windows per step of the --impl reference run (default: the "
                          "workload's whole batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--floor-table", action="store_true",
+                    help="print the recurrence's per-step time against its latency floor "
+                         "for a range of batch sizes instead of the benchmark line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.floor_table:
+        return run_floor_table(args)
     return run_ours(args)
 
 

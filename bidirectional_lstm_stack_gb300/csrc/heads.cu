@@ -20,9 +20,10 @@
 //    read accumulator 1, add b0, apply LeakyReLU, split h1 and write both
 //    halves back into tensor memory for linear1; then read accumulator 2, add
 //    b1, apply LeakyReLU and, still in registers, multiply h2 by the
-//    classifier's 128 x 7 weights (fp32 FMAs, weights broadcast from shared
-//    memory: a 16-column MMA would sit at its per-instruction floor), add b2
-//    and write the log-softmax of the 7 logits.
+//    classifier's 128 x 7 weights (fp32 FMAs whose weight operands come
+//    straight from the constant bank: b0, b1, W2 and b2 are one kernel
+//    parameter; a 16-column MMA would sit at its per-instruction floor), add
+//    b2 and write the log-softmax of the 7 logits.
 // Tensor memory (512 columns): accumulator 1 [0, 128), h1 hi [128, 256),
 // h1 lo [256, 384), accumulator 2 [384, 512).  The MMA thread starts linear1
 // of a tile once the epilogue has written its h1 (which also means it has
@@ -60,13 +61,20 @@ constexpr int W_HI = 2 * A_BYTES;
 constexpr int W_LO = W_HI + W_BYTES;
 constexpr int STAGES = 6;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;  // 192 KiB
-// parameters in shared memory: b0, b1, W2 (rows padded to 8), b2 (padded)
-constexpr int P_B0 = 0;
-constexpr int P_B1 = P_B0 + kMid;
-constexpr int P_W2 = P_B1 + kMid;
-constexpr int P_B2 = P_W2 + kMid * kClsPad;
-constexpr int P_FLOATS = P_B2 + kClsPad;
-constexpr size_t SMEM_BYTES = RING_BYTES + P_FLOATS * 4 + 256 + 1024;
+constexpr size_t SMEM_BYTES = RING_BYTES + 256 + 1024;
+
+// The epilogues' parameters, passed by value as one kernel parameter (4.6
+// KiB): with every index a compile-time constant (the epilogue loops are
+// unrolled), each use is an operand read straight from the constant bank,
+// with no load instruction.  From shared memory the classifier alone took
+// two 128-bit loads per hidden unit and row, each costing four issue cycles
+// though all lanes read the same address.
+struct HeadsParams {
+    float b0[kMid];
+    float b1[kMid];
+    float w2[kMid][kClsPad];  // row k: the 7 class weights of hidden unit k, padded
+    float b2[kClsPad];
+};
 constexpr uint32_t ACC1 = 0, H1HI = 128, H1LO = 256, ACC2 = 384, TMEM_COLS = 512;
 constexpr uint32_t IDESC = ptx::tf32_idesc(BM, kMid);
 constexpr int CONVERTERS = 128;
@@ -83,15 +91,14 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
              const __grid_constant__ CUtensorMap w0hi_map,
              const __grid_constant__ CUtensorMap w0lo_map,
              const __grid_constant__ CUtensorMap w1hi_map,
-             const __grid_constant__ CUtensorMap w1lo_map, const float *__restrict__ params,
+             const __grid_constant__ CUtensorMap w1lo_map, const __grid_constant__ HeadsParams hp,
              float slope, float *__restrict__ logp, int rows, int tiles, unsigned *fault,
              unsigned long long wait_limit_ns, int withhold)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *par = reinterpret_cast<float *>(smem + RING_BYTES);
-    uint64_t *full = reinterpret_cast<uint64_t *>(par + P_FLOATS);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + RING_BYTES);
     uint64_t *conv = full + STAGES;
     uint64_t *empty = conv + STAGES;
     uint64_t *acc1_full = empty + STAGES;
@@ -104,8 +111,6 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    for (int i = threadIdx.x; i < P_FLOATS; i += THREADS)
-        par[i] = params[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
@@ -292,14 +297,14 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
                 break;
             ptx::tc_fence_after();
             // h1 = leaky(acc1 + b0), written back as TF32 hi/lo columns
-#pragma unroll 1
+#pragma unroll
             for (int c = 0; c < kMid / 32; ++c) {
                 uint32_t r[32], hi[32], lo[32];
                 ptx::tmem_ld_32x32b_x32(tmem + lane_base + ACC1 + c * 32, r);
                 ptx::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    float v = __uint_as_float(r[j]) + par[P_B0 + c * 32 + j];
+                    float v = __uint_as_float(r[j]) + hp.b0[c * 32 + j];
                     v = v >= 0.0f ? v : slope * v;
                     const float h = ptx::tf32_rna(v);
                     hi[j] = __float_as_uint(h);
@@ -321,25 +326,18 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
 #pragma unroll
             for (int j = 0; j < kClsPad; ++j)
                 z[j] = 0.0f;
-#pragma unroll 1
+#pragma unroll
             for (int c = 0; c < kMid / 32; ++c) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(tmem + lane_base + ACC2 + c * 32, r);
                 ptx::tmem_ld_wait();
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    float v = __uint_as_float(r[k]) + par[P_B1 + c * 32 + k];
+                    float v = __uint_as_float(r[k]) + hp.b1[c * 32 + k];
                     v = v >= 0.0f ? v : slope * v;
-                    const float4 *w = reinterpret_cast<const float4 *>(
-                        par + P_W2 + (c * 32 + k) * kClsPad);
-                    const float4 w0 = w[0], w1 = w[1];
-                    z[0] = fmaf(v, w0.x, z[0]);
-                    z[1] = fmaf(v, w0.y, z[1]);
-                    z[2] = fmaf(v, w0.z, z[2]);
-                    z[3] = fmaf(v, w0.w, z[3]);
-                    z[4] = fmaf(v, w1.x, z[4]);
-                    z[5] = fmaf(v, w1.y, z[5]);
-                    z[6] = fmaf(v, w1.z, z[6]);
+#pragma unroll
+                    for (int j = 0; j < kCls; ++j)
+                        z[j] = fmaf(v, hp.w2[c * 32 + k][j], z[j]);
                 }
             }
             ptx::tc_fence_before();
@@ -347,7 +345,7 @@ heads_kernel(const __grid_constant__ CUtensorMap y_map,
                 float zmax = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < kCls; ++j) {
-                    z[j] += par[P_B2 + j];
+                    z[j] += hp.b2[j];
                     zmax = fmaxf(zmax, z[j]);
                 }
                 float sum = 0.0f;
@@ -414,9 +412,9 @@ struct lstm_heads {
     int device = 0;
     long max_rows = 0;
     float slope = 0.01f;
-    float *weights = nullptr;  // one allocation: packed planes and the parameters
+    float *weights = nullptr;  // one allocation: the packed W0 and W1 planes
     float *w0_hi = nullptr, *w0_lo = nullptr, *w1_hi = nullptr, *w1_lo = nullptr;
-    float *params = nullptr;   // b0, b1, W2 (rows padded to 8), b2 (padded)
+    HeadsParams params = {};   // b0, b1, W2 (rows padded to 8), b2: a kernel parameter
     CUtensorMap map_w0hi, map_w0lo, map_w1hi, map_w1lo;
     CUtensorMap map_y;
     const float *map_y_base = nullptr;
@@ -466,11 +464,11 @@ extern "C" int lstm_heads_create(const float *w0, const float *b0, const float *
     }
 
     // W0 [256][128] and W1 [128][128] (row-major [k, n]) become K-major
-    // [n][k] TF32 hi/lo planes; W2 [128][7] stays fp32, rows padded to 8
+    // [n][k] TF32 hi/lo planes; W2 [128][7] stays fp32, rows padded to 8, in
+    // the kernel parameter with the biases
     const long n0 = static_cast<long>(kMid) * kIn, n1 = static_cast<long>(kMid) * kMid;
     const long o_w0hi = 0, o_w0lo = o_w0hi + n0, o_w1hi = o_w0lo + n0, o_w1lo = o_w1hi + n1;
-    const long o_par = o_w1lo + n1;
-    const long total = (o_par + P_FLOATS + 63) / 64 * 64;
+    const long total = (o_w1lo + n1 + 63) / 64 * 64;
     float *host = static_cast<float *>(calloc(total, sizeof(float)));
     if (!host) {
         lstm_heads_destroy(h);
@@ -487,14 +485,14 @@ extern "C" int lstm_heads_create(const float *w0, const float *b0, const float *
         for (int k = 0; k < kMid; ++k)
             split(w1[static_cast<long>(k) * kMid + n], &host[o_w1hi + n * kMid + k],
                   &host[o_w1lo + n * kMid + k]);
-        host[o_par + P_B0 + n] = b0[n];
-        host[o_par + P_B1 + n] = b1[n];
+        h->params.b0[n] = b0[n];
+        h->params.b1[n] = b1[n];
     }
     for (int k = 0; k < kMid; ++k)
         for (int j = 0; j < kCls; ++j)
-            host[o_par + P_W2 + k * kClsPad + j] = w2[k * kCls + j];
+            h->params.w2[k][j] = w2[k * kCls + j];
     for (int j = 0; j < kCls; ++j)
-        host[o_par + P_B2 + j] = b2[j];
+        h->params.b2[j] = b2[j];
     cudaError_t e = device_alloc(reinterpret_cast<void **>(&h->weights), total * sizeof(float));
     if (e == cudaSuccess)
         e = cudaMemcpy(h->weights, host, total * sizeof(float), cudaMemcpyHostToDevice);
@@ -509,7 +507,6 @@ extern "C" int lstm_heads_create(const float *w0, const float *b0, const float *
     h->w0_lo = h->weights + o_w0lo;
     h->w1_hi = h->weights + o_w1hi;
     h->w1_lo = h->weights + o_w1lo;
-    h->params = h->weights + o_par;
     if ((st = encode_matrix_map(&h->map_w0hi, h->w0_hi, kMid, kIn, kHeadWBoxRows)) ||
         (st = encode_matrix_map(&h->map_w0lo, h->w0_lo, kMid, kIn, kHeadWBoxRows)) ||
         (st = encode_matrix_map(&h->map_w1hi, h->w1_hi, kMid, kMid, kHeadWBoxRows)) ||
@@ -569,7 +566,7 @@ extern "C" int lstm_heads_forward(lstm_heads *h, const float *y, size_t y_len, f
     const KernelTest test = kernel_test(kTestHeads);
     return cuda_status(cudaLaunchKernelEx(&cfg, heads_kernel, h->map_y, h->map_w0hi, h->map_w0lo,
                                           h->map_w1hi, h->map_w1lo,
-                                          static_cast<const float *>(h->params), h->slope, logp,
+                                          h->params, h->slope, logp,
                                           rows, ntiles, h->fault, test.wait_limit_ns,
                                           test.withhold),
                        "heads launch");
