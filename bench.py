@@ -413,6 +413,12 @@ def run_ours(args):
                                           stream)
     ms1_step = max_over_ranks(float(np.mean(ms1)), device=torch.device("cuda", dev))
 
+    # the one-window case with the projection fused into the recurrence
+    binding.lstm_stack_set_fused_batches(stack.handle, 1)
+    ms1f, (ph1f, _), _ = time_stack(stack, x1, max(args.steps, 10), args.warmup, flush, stream)
+    binding.lstm_stack_set_fused_batches(stack.handle, 0)
+    ms1f_step = max_over_ranks(float(np.mean(ms1f)), device=torch.device("cuda", dev))
+
     # the opt-in single-product TF32 projection mode on the same workload (the
     # fp32-accurate 3xTF32 mode above is the headline)
     binding.lstm_stack_set_math(stack.handle, binding.LSTM_MATH_TF32)
@@ -513,6 +519,11 @@ def run_ours(args):
                        "recurrence_pair_us_per_step": rec1_full_us,
                        "floor_us_per_step": rec1_floor_us,
                        "vs_floor": rec1_full_us / rec1_floor_us,
+                       "fused_projection": {
+                           "ms_per_window": ms1f_step, "windows_per_s": 1e3 / ms1f_step,
+                           "recurrence_ms": [round(float(v), 4) for v in ph1f[:, 1]],
+                           "mode": "lstm_stack_set_fused_batches: each layer one launch, the "
+                                   "input projection computed inside the recurrence"},
                        "context": "pages: A100, TF32-projection stack, 3.21-4.13 ms per window"},
         "gaps_ms": phases_total - float(np.sum(phases[:, 0]) +
                                         np.sum(phases[:, 1])),

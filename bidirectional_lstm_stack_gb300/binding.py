@@ -101,6 +101,8 @@ def load():
             "lstm_test_heads_timeout": (i, [i, ctypes.c_uint, i]),
             "lstm_recurrence_floor": (i, [_vp, _vp, _vp, _vp, i, i, i, _vp]),
             "lstm_tf32_rate": (i, [i, i, ctypes.POINTER(ctypes.c_double)]),
+            "lstm_recurrence_fused": (i, [_vp, i, _vp, _vp, i, _vp, _vp, _vp, i, i, i, _vp]),
+            "lstm_stack_set_fused_batches": (i, [_vp, i]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -173,6 +175,17 @@ def lstm_recurrence(g, rp, bias, y, batch: int, steps: int, direction: int, stre
 def lstm_recurrence_floor(g, rp, bias, y, batch: int, steps: int, direction: int, stream=None):
     _check(load().lstm_recurrence_floor(_ptr(g), _ptr(rp), _ptr(bias), _ptr(y), batch, steps,
                                         direction, _stream(stream, g.device)))
+
+
+def lstm_recurrence_fused(x, in_width: int, wp_hi, wp_lo, kp: int, rp, bias, y, batch: int,
+                          steps: int, direction: int, stream=None):
+    _check(load().lstm_recurrence_fused(_ptr(x), in_width, _ptr(wp_hi), _ptr(wp_lo), kp,
+                                        _ptr(rp), _ptr(bias), _ptr(y), batch, steps, direction,
+                                        _stream(stream, x.device)))
+
+
+def lstm_stack_set_fused_batches(handle, max_batch: int) -> None:
+    _check(load().lstm_stack_set_fused_batches(handle, max_batch))
 
 
 def lstm_tf32_rate(device: int = 0, iterations: int = 20000) -> float:

@@ -281,6 +281,7 @@ struct lstm_stack {
         int batch = 0, steps = 0;
         bool timing = false;
         int math = LSTM_MATH_3XTF32;
+        bool fused = false;
         cudaGraphExec_t exec = nullptr;
         unsigned long long used = 0;
     };
@@ -290,6 +291,8 @@ struct lstm_stack {
     bool use_graphs = true;
     cudaStream_t capture = nullptr;
     int math = LSTM_MATH_3XTF32;  // projection products
+    int fused_max_batch = 0;      // batches up to this run the fused recurrence
+    int fused_fit = -1;           // windows the device runs fused at once (-1: not queried)
 };
 
 extern "C" const char *lstm_stack_last_error(void)
@@ -542,6 +545,28 @@ int check_forward_args(lstm_stack *s, const void *x, size_t x_len, const void *y
     return LSTM_OK;
 }
 
+// Whether a forward of `batch` windows runs the fused recurrence: enabled up
+// to fused_max_batch, and only while both directions' clusters of one window
+// each run at once on the device (larger batches take the projection kernel).
+bool fused_batch(lstm_stack *s, int batch)
+{
+    if (batch > s->fused_max_batch)
+        return false;
+    if (s->fused_fit < 0) {
+        int fit = -1;
+        for (int kp : {64, 256}) {
+            int n = 0;
+            if (recurrence_fused_max_clusters(kp, &n) != LSTM_OK) {
+                n = 0;
+                cudaGetLastError();
+            }
+            fit = fit < 0 || n < fit ? n : fit;
+        }
+        s->fused_fit = fit / 2;
+    }
+    return batch <= s->fused_fit;
+}
+
 int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps,
                    cudaStream_t stream)
 {
@@ -565,9 +590,25 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
                                                     cudaEventRecordExternal),
                            "event");
     };
+    const bool fused = fused_batch(s, batch);
     for (int l = 0; l < kLayers; ++l) {
         const CUtensorMap &src = l == 0 ? s->map_x : s->map_ping[(l - 1) & 1];
         float *dst = l == kLayers - 1 ? y : s->ping[l & 1];
+        if (fused) {
+            // the projection computed inside the recurrence (an empty
+            // projection phase)
+            const float *xin = l == 0 ? x : s->ping[(l - 1) & 1];
+            if ((st = mark(l, 0, 0)) || (st = mark(l, 0, 1)) || (st = mark(l, 1, 0)) ||
+                (st = mark(l, 2, 0)))
+                return st;
+            if ((st = launch_recurrence_fused(xin, s->in_width[l], s->wp_hi[l], s->wp_lo[l],
+                                              s->kp[l], s->rp[l], s->bias[l], dst, batch, steps,
+                                              kBothDirections, s->fault, stream)))
+                return st;
+            if ((st = mark(l, 1, 1)) || (st = mark(l, 2, 1)))
+                return st;
+            continue;
+        }
         if ((st = mark(l, 0, 0)))
             return st;
         st = launch_projection(src, s->map_w[l], s->gates, static_cast<int>(rows), s->kp[l],
@@ -611,7 +652,7 @@ int forward_replay(lstm_stack *s, const float *x, float *y, int batch, int steps
     lstm_stack::Graph *hit = nullptr, *victim = &s->graphs[0];
     for (auto &gr : s->graphs) {
         if (gr.exec && gr.x == x && gr.y == y && gr.batch == batch && gr.steps == steps &&
-            gr.timing == s->timing && gr.math == s->math) {
+            gr.timing == s->timing && gr.math == s->math && gr.fused == fused_batch(s, batch)) {
             hit = &gr;
             break;
         }
@@ -640,7 +681,11 @@ int forward_replay(lstm_stack *s, const float *x, float *y, int batch, int steps
         cudaGraphDestroy(graph);
         if (st != LSTM_OK)
             return st;
-        *victim = lstm_stack::Graph{x, y, batch, steps, s->timing, s->math, exec, 0};
+        *victim = lstm_stack::Graph{x,         y,
+                                    batch,     steps,
+                                    s->timing, s->math,
+                                    fused_batch(s, batch), exec,
+                                    0};
         hit = victim;
     }
     hit->used = ++s->uses;
@@ -664,6 +709,16 @@ extern "C" int lstm_stack_set_math(lstm_stack *s, int math)
     if (math != LSTM_MATH_3XTF32 && math != LSTM_MATH_TF32)
         return fail(LSTM_E_INVALID, "set_math: unknown math mode %d", math);
     s->math = math;
+    return LSTM_OK;
+}
+
+extern "C" int lstm_stack_set_fused_batches(lstm_stack *s, int max_batch)
+{
+    if (!s)
+        return fail(LSTM_E_INVALID, "set_fused_batches: null stack");
+    if (max_batch < 0)
+        return fail(LSTM_E_INVALID, "set_fused_batches: max_batch %d", max_batch);
+    s->fused_max_batch = max_batch;
     return LSTM_OK;
 }
 
@@ -901,6 +956,38 @@ extern "C" int lstm_recurrence_floor(const float *g, const float *rp, const floa
     if (!fault)
         return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
     return launch_recurrence_floor(g, rp, bias, y, batch, steps, launch_direction(direction), fault,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int lstm_recurrence_fused(const float *x, int in_width, const float *wp_hi,
+                                     const float *wp_lo, int kp, const float *rp,
+                                     const float *bias, float *y, int batch, int steps,
+                                     int direction, void *stream)
+{
+    if (!x || !wp_hi || !wp_lo)
+        return fail(LSTM_E_INVALID, "lstm_recurrence_fused: null pointer");
+    int dev = 0;
+    // the argument checks of lstm_recurrence, with x standing in for G
+    int st = recurrence_args(x, rp, bias, y, batch, steps, direction, &dev);
+    if (st != LSTM_OK)
+        return st;
+    if ((st = check_aligned(wp_hi, "wp_hi")) || (st = check_aligned(wp_lo, "wp_lo")))
+        return st;
+    DeviceGuard guard(dev);
+    int fit = 0;
+    if ((st = recurrence_fused_max_clusters(kp, &fit)))
+        return st;
+    const long clusters = static_cast<long>(batch) * (direction == LSTM_BOTH_DIRECTIONS ? 2 : 1);
+    if (clusters > fit)
+        return fail(LSTM_E_INVALID,
+                    "lstm_recurrence_fused: %ld clusters of one window each, the device runs %d "
+                    "at once",
+                    clusters, fit);
+    unsigned *fault = fault_word();
+    if (!fault)
+        return fail(LSTM_E_CUDA, "cannot resolve the device fault word");
+    return launch_recurrence_fused(x, in_width, wp_hi, wp_lo, kp, rp, bias, y, batch, steps,
+                                   launch_direction(direction), fault,
                                    static_cast<cudaStream_t>(stream));
 }
 

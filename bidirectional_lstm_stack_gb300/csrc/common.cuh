@@ -138,6 +138,14 @@ int launch_recurrence_variant(const float *g, const float *rp, const float *bias
 int launch_recurrence_floor(const float *g, const float *rp, const float *bias, float *y,
                             int batch, int steps, int direction, unsigned *fault,
                             cudaStream_t stream);
+// The recurrence with the projection fused in (small batches): x is the
+// layer input [batch][steps][in_width] (in_width a multiple of 4, at most kp),
+// wp_hi/wp_lo the layer's packed W planes [1024][kp] (kp 64 or 256); no G.
+int launch_recurrence_fused(const float *x, int in_width, const float *wp_hi, const float *wp_lo,
+                            int kp, const float *rp, const float *bias, float *y, int batch,
+                            int steps, int direction, unsigned *fault, cudaStream_t stream);
+// Clusters of the fused kernel (for kp) the device holds at once.
+int recurrence_fused_max_clusters(int kp, int *out);
 // Clusters of a variant the device can hold at once.
 int recurrence_max_clusters(int cluster, int nw, int nch, int threads, int *out);
 int recurrence_prepare(int device);
@@ -233,6 +241,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+                 : "memory");
+}
+// Global -> this CTA's shared memory, `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), credited to `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
 // Shared memory -> global through the tensor map; the TMA engine writes only

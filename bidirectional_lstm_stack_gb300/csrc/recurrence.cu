@@ -716,6 +716,313 @@ done:
     ptx::cluster_wait_acquire();
 }
 
+// Fused input projection (small batches): the recurrence computes its own
+// projection values instead of reading G.  Clusters of 8 CTAs of 256 threads,
+// one window per cluster.  Threads 0-127 run the recurrence exactly as the
+// one-window kernel above (the same lanes, weights, butterfly and cell);
+// threads 128-255 ("input lanes", one per recurrence lane: same unit, same
+// K-chunk index kc) hold that lane's slice of the layer's input weights W
+// (the 4 gate rows of the unit, columns kc*KIN/8 .. +KIN/8, W = hi + lo of
+// the packed planes, scaled by the gates' k_q) and, running up to PD steps
+// ahead, compute for every step the four partial sums of W x_t over their
+// columns.  The recurrence lane adds them to its four partial sums of R h
+// before the butterfly, so one reduction yields k_q (W x_t + R h) and the
+// bias is added after it, as the projection value is in the unfused kernel.
+// x_t reaches the CTA as one bulk copy per step (one input lane issues it XD
+// steps ahead into a ring), and the partial sums reach the recurrence lanes
+// through a shared-memory ring; every wait is bounded.  The products are fp32
+// FMAs (the projection kernel's 3xTF32 form differs from it in the last bits).
+template <int KIN>
+__global__ void __launch_bounds__(256, 1)
+recurrence_fused_kernel(const float *__restrict__ x, int in_width,
+                        const float *__restrict__ wp_hi, const float *__restrict__ wp_lo,
+                        const float *__restrict__ rp_in, const float *__restrict__ bias_in,
+                        float *__restrict__ y, int batch, int steps, int dir_in,
+                        unsigned *fault, unsigned long long wait_limit_ns, int withhold)
+{
+    constexpr int C = 8;
+    constexpr int U = kHidden / C;  // 16 units per CTA
+    constexpr int RT = 128;         // recurrence threads (and input threads)
+    constexpr int KX = KIN / KC;    // input columns per lane
+    constexpr int XD = 8;           // input-row ring slots
+    constexpr int PD = 8;           // partial-sum ring slots
+    // a row's K chunk kc (KX floats) sits at kc * XSTRIDE: the padding puts
+    // the 8 lanes of a quarter-warp, which read the 8 chunks, in distinct banks
+    constexpr int XSTRIDE = KX + 4;
+    static_assert(KX % 4 == 0 && U * KC == RT, "fused shape");
+
+    __shared__ __align__(16) float hbuf[2][HROW];
+    __shared__ __align__(16) float xrow[XD][KC * XSTRIDE];
+    __shared__ __align__(16) float4 xpart[PD][RT];
+    __shared__ __align__(8) uint64_t hbar[2];
+    __shared__ __align__(8) uint64_t xfull[XD], xempty[XD], pfull[PD], pempty[PD];
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x;
+    const bool input_lane = tid >= RT;
+    const int lt = tid & (RT - 1);
+    const int lane = tid & 31;
+    const int kc = lt & 7;
+    const int ul = lt >> 3;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cid = static_cast<int>(ptx::cluster_id_x());
+    const int direction = dir_in >= 0 ? dir_in : (cid & 1);
+    const int win = dir_in >= 0 ? cid : (cid >> 1);  // this cluster's window
+    const float *__restrict__ rp = rp_in + (dir_in >= 0 ? 0 : direction * kGates * kHidden);
+    const float *__restrict__ bias = bias_in + (dir_in >= 0 ? 0 : direction * kGates);
+    const int u = static_cast<int>(rank) * U + ul;
+    const int u0 = u & ~3;
+    // slot q of a lane's partial sums holds gate q ^ xq (the select-free
+    // butterfly's lane-dependent order, as in the one-window kernel)
+    const int xq = ((kc & 4) ? 2 : 0) | ((kc & 2) ? 1 : 0);
+    volatile int *abort_v = &abort_flag;
+    // The input lanes run ahead of the recurrence and mostly wait for a free
+    // ring slot: they wait with a sleep between polls, so that they leave
+    // the issue slots to the recurrence warps on the same SM sub-partitions.
+    auto input_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        const uint64_t start = ptx::globaltimer();
+        while (true) {
+            __nanosleep(256);
+            if (ptx::mbar_try_wait(bar, parity))
+                return true;
+            if (*abort_v)
+                return false;
+            if (ptx::globaltimer() - start > wait_limit_ns) {
+                atomicOr(fault, kFaultRecurrence);
+                *abort_v = 1;
+                return false;
+            }
+        }
+    };
+
+    // weights: recurrence lanes R (columns kc*16 ..), input lanes W
+    // (columns kc*KX ..), rows in slot order, scaled by k_q
+    float2 r2[4][KLEN / 2];
+    float2 w2[4][KX / 2];
+    if (!input_lane) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = 4 * u + (q ^ xq);
+            const float kq = (q ^ xq) == 2 ? -2.0f * kLog2e : -kLog2e;
+            const float2 *src = reinterpret_cast<const float2 *>(rp + row * kHidden + kc * KLEN);
+#pragma unroll
+            for (int i = 0; i < KLEN / 2; ++i)
+                r2[q][i] = make_float2(src[i].x * kq, src[i].y * kq);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = direction * kGates + 4 * u + (q ^ xq);
+            const float kq = (q ^ xq) == 2 ? -2.0f * kLog2e : -kLog2e;
+            const float2 *hi = reinterpret_cast<const float2 *>(wp_hi + row * KIN + kc * KX);
+            const float2 *lo = reinterpret_cast<const float2 *>(wp_lo + row * KIN + kc * KX);
+#pragma unroll
+            for (int i = 0; i < KX / 2; ++i)
+                w2[q][i] = make_float2((hi[i].x + lo[i].x) * kq, (hi[i].y + lo[i].y) * kq);
+        }
+    }
+    // after the reduction lane kc holds gate kc >> 1 (both lanes of a pair)
+    const int gq = kc >> 1;
+    const float gk = gq == 2 ? -2.0f * kLog2e : -kLog2e;
+    const float bias_v = bias[4 * u + gq] * gk;
+    const float act_m = gq == 2 ? 2.0f : 1.0f;
+    const float act_a = gq == 2 ? -1.0f : 0.0f;
+
+    for (int i = tid; i < 2 * HROW; i += 256)
+        (&hbuf[0][0])[i] = 0.0f;
+    for (int i = tid; i < XD * KC * XSTRIDE; i += 256)  // the padding stays zero
+        (&xrow[0][0])[i] = 0.0f;
+    ptx::fence_proxy_async_smem();  // before the bulk copies write the ring
+    const uint32_t bar_bytes = kHidden * 4;  // one window
+    if (tid == 0) {
+        ptx::mbar_init(&hbar[0], 1);
+        ptx::mbar_init(&hbar[1], 1);
+        for (int i = 0; i < XD; ++i) {
+            ptx::mbar_init(&xfull[i], 1);
+            ptx::mbar_init(&xempty[i], RT / 32);
+        }
+        for (int i = 0; i < PD; ++i) {
+            ptx::mbar_init(&pfull[i], RT / 32);
+            ptx::mbar_init(&pempty[i], RT / 32);
+        }
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+        if (steps > 1)
+            ptx::mbar_arrive_expect_tx(&hbar[1], bar_bytes);
+        if (steps > 2)
+            ptx::mbar_arrive_expect_tx(&hbar[0], bar_bytes);
+    }
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+    ptx::griddep_launch_dependents();
+
+    const uint32_t row_bytes = static_cast<uint32_t>(in_width) * 4;
+    // step s's input row into ring slot `slot`, one bulk copy per K chunk
+    // (the last chunk of a 60-wide row holds 4 columns; its rest stays zero)
+    auto x_load = [&](int s, int slot) {
+        const long t = direction ? steps - 1 - s : s;
+        const float *src = x + (static_cast<long>(win) * steps + t) * in_width;
+        ptx::mbar_arrive_expect_tx(&xfull[slot], row_bytes);
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            const int cols = min(KX, in_width - k * KX);
+            if (cols > 0)
+                ptx::bulk_load(&xrow[slot][k * XSTRIDE], src + k * KX,
+                               static_cast<uint32_t>(cols) * 4, &xfull[slot]);
+        }
+    };
+    int x_issued = 0;  // input rows whose copies were issued (input lane 0)
+    int x_done = 0;    // input rows consumed (every input lane)
+
+    if (withhold && rank == 0)
+        goto done;
+    if (input_lane) {
+        if (lt == 0)
+            for (; x_issued < XD && x_issued < steps; ++x_issued)
+                x_load(x_issued, x_issued);
+        for (int s = 0; s < steps; ++s) {
+            const int xs = s % XD, ps = s % PD;
+            if (!input_wait(&xfull[xs], (s / XD) & 1))
+                break;
+            float2 acc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                acc[q] = make_float2(0.0f, 0.0f);
+            const float4 *xp = reinterpret_cast<const float4 *>(&xrow[xs][kc * XSTRIDE]);
+#pragma unroll
+            for (int i = 0; i < KX / 4; ++i) {
+                const float4 v = xp[i];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[q] = __ffma2_rn(w2[q][2 * i], make_float2(v.x, v.y), acc[q]);
+                    acc[q] = __ffma2_rn(w2[q][2 * i + 1], make_float2(v.z, v.w), acc[q]);
+                }
+            }
+            x_done = s + 1;
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&xempty[xs]);
+            // the row XD steps on goes into this slot once every input lane
+            // has read it
+            if (lt == 0 && x_issued < steps) {
+                if (!input_wait(&xempty[xs], (s / XD) & 1))
+                    break;
+                x_load(x_issued, xs);
+                ++x_issued;
+            }
+            if (s >= PD && !input_wait(&pempty[ps], ((s / PD) - 1) & 1))
+                break;
+            xpart[ps][lt] = make_float4(acc[0].x + acc[0].y, acc[1].x + acc[1].y,
+                                        acc[2].x + acc[2].y, acc[3].x + acc[3].y);
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&pfull[ps]);
+        }
+        goto done;
+    }
+    {
+        // the peers this lane sends its warp's four units to (lanes 0-7)
+        const uint32_t hbase = ptx::smem_u32(&hbuf[0][0]);
+        const uint32_t bar_base = ptx::smem_u32(&hbar[0]);
+        const uint32_t send_off0 =
+            static_cast<uint32_t>(((u0 / KLEN) * CHUNK_STRIDE + (u0 % KLEN)) * 4);
+        const int peer = lane < C ? lane : C - 1;
+        uint32_t rdst[2], rbar[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            rdst[q] = ptx::map_to_rank(hbase + static_cast<uint32_t>(q * HROW * 4) + send_off0,
+                                       static_cast<uint32_t>(peer));
+            rbar[q] = ptx::map_to_rank(bar_base + static_cast<uint32_t>(q * 8),
+                                       static_cast<uint32_t>(peer));
+        }
+        float *yrow = y + static_cast<long>(win) * steps * kOutput + direction * kHidden + u0;
+        float c = 0.0f;
+        for (int s = 0; s < steps; ++s) {
+            const int par = s & 1, ps = s % PD;
+            const int t = direction ? steps - 1 - s : s;
+            // this step's input partial sums (normally long ready)
+            if (!ptx::mbar_wait_bounded(&pfull[ps], (s / PD) & 1, abort_v, fault,
+                                        kFaultRecurrence, wait_limit_ns))
+                break;
+            const float4 xs4 = xpart[ps][lt];
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&pempty[ps]);
+            // h_{s-1} complete in buffer par; re-arm it for h_{s+1}
+            if (s > 0) {
+                const uint32_t phase = ((s - 1) >> 1) & 1;
+                if (!ptx::mbar_try_wait_cluster(&hbar[par], phase)) {
+                    if (*abort_v)
+                        break;
+                    const uint64_t start = ptx::globaltimer();
+                    bool ok = true;
+                    while (!ptx::mbar_try_wait_cluster(&hbar[par], phase)) {
+                        if (*abort_v || ptx::globaltimer() - start > wait_limit_ns) {
+                            if (!*abort_v) {
+                                atomicOr(fault, kFaultRecurrence);
+                                *abort_v = 1;
+                            }
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok)
+                        break;
+                }
+                if (tid == 0 && s + 2 < steps)
+                    ptx::mbar_arrive_expect_tx(&hbar[par], bar_bytes);
+            }
+            // R h over this lane's K chunk, plus W x_t of the input lane
+            const float4 *hp = reinterpret_cast<const float4 *>(&hbuf[par][kc * CHUNK_STRIDE]);
+            const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+            const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y}, {h1.z, h1.w},
+                                  {h2.x, h2.y}, {h2.z, h2.w}, {h3.x, h3.y}, {h3.z, h3.w}};
+            const float xs[4] = {xs4.x, xs4.y, xs4.z, xs4.w};
+            float part[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc = __ffma2_rn(r2[q][i], hh[i], acc);
+                part[q] = (acc.x + acc.y) + xs[q];
+            }
+            float a[2], b2[1];
+            reduce_level<4, true>(part, a, 4, (kc & 4) != 0);
+            reduce_level<2, true>(a, b2, 2, (kc & 2) != 0);
+            const float held = b2[0] + __shfl_xor_sync(0xffffffffu, b2[0], 1);
+            const float act = fmaf(act_m, inv_one_plus_ex2(held + bias_v), act_a);
+            float gate[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                gate[q] = __shfl_sync(0xffffffffu, act, 2 * q, 8);
+            c = gate[1] * c + gate[0] * gate[2];
+            const float r = inv_one_plus_ex2(c * (-2.0f * kLog2e));
+            const float h = fmaf(2.0f * gate[3], r, -gate[3]);
+            float h4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                h4[j] = __shfl_sync(0xffffffffu, h, 8 * j + kc);
+            if (s + 1 < steps && lane < C)
+                ptx::st_async_v4(rdst[par ^ 1], h4[0], h4[1], h4[2], h4[3], rbar[par ^ 1]);
+            if (lane == 0)
+                *reinterpret_cast<float4 *>(yrow + static_cast<long>(t) * kOutput) =
+                    make_float4(h4[0], h4[1], h4[2], h4[3]);
+        }
+    }
+done:
+    if (input_lane && lt == 0) {
+        // every issued input row has landed before the shared memory goes away
+        for (int s = x_done; s < x_issued; ++s)
+            ptx::mbar_wait_drain(&xfull[s % XD], (s / XD) & 1, fault, kDefaultWaitLimitNs);
+    }
+    __syncwarp();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+}
+
 struct Variant {
     int cluster;
     int nw;       // windows per chunk
@@ -894,6 +1201,59 @@ int launch_recurrence_floor(const float *g, const float *rp, const float *bias, 
 {
     return launch_variant(*choose_variant(batch), g, rp, bias, y, batch, steps, direction, fault,
                           stream, true);
+}
+
+int recurrence_fused_max_clusters(int kp, int *out)
+{
+    const void *fn = kp <= 64 ? reinterpret_cast<const void *>(&recurrence_fused_kernel<64>)
+                              : reinterpret_cast<const void *>(&recurrence_fused_kernel<256>);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(8);
+    cfg.blockDim = dim3(256);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 8;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaOccupancyMaxActiveClusters(out, fn, &cfg), "fused max active clusters");
+}
+
+int launch_recurrence_fused(const float *x, int in_width, const float *wp_hi, const float *wp_lo,
+                            int kp, const float *rp, const float *bias, float *y, int batch,
+                            int steps, int direction, unsigned *fault, cudaStream_t stream)
+{
+    if (kp != 64 && kp != 256)
+        return fail(LSTM_E_INVALID, "fused recurrence: kp %d (64 or 256)", kp);
+    if (in_width <= 0 || in_width > kp || in_width % 4 != 0)
+        return fail(LSTM_E_INVALID, "fused recurrence: in_width %d (a multiple of 4 up to kp %d)",
+                    in_width, kp);
+    const long blocks = static_cast<long>(batch) * 8 * (direction == kBothDirections ? 2 : 1);
+    if (blocks > 0x7fffffffL)
+        return fail(LSTM_E_OVERFLOW, "fused recurrence: %d windows", batch);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 8;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    KernelTest test = kernel_test(kTestRecurrence);
+    int st;
+    if ((st = check_launch_injection("fused recurrence launch")))
+        return st;
+    void *args[] = {const_cast<float **>(&x), &in_width, const_cast<float **>(&wp_hi),
+                    const_cast<float **>(&wp_lo), const_cast<float **>(&rp),
+                    const_cast<float **>(&bias), &y, &batch, &steps, &direction, &fault,
+                    &test.wait_limit_ns, &test.withhold};
+    const void *fn = kp == 64 ? reinterpret_cast<const void *>(&recurrence_fused_kernel<64>)
+                              : reinterpret_cast<const void *>(&recurrence_fused_kernel<256>);
+    return cuda_status(cudaLaunchKernelExC(&cfg, fn, args), "fused recurrence launch");
 }
 
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias, float *y,

@@ -199,6 +199,18 @@ int lstm_stack_set_graphs(lstm_stack *s, int enable);
  * (null stack, unknown mode). */
 int lstm_stack_set_math(lstm_stack *s, int math);
 
+/* Forward passes with batch <= max_batch compute each layer's input
+ * projection inside its recurrence (lstm_recurrence_fused: no projection
+ * kernel, no gate buffer round trip; the pages' SURVEY-ranked follow-on for
+ * one window, the input projection of lstmproj.rs module docs folded into
+ * `recur`); larger batches, and max_batch 0 (the default), run the
+ * projection kernel and the recurrence, and so do batches whose clusters
+ * (8 CTAs of 256 threads per window and direction) the device cannot run all
+ * at once.  The fused products are fp32 FMAs, so results differ from the
+ * default path in the last bits.  Errors: LSTM_E_INVALID (null,
+ * max_batch < 0). */
+int lstm_stack_set_fused_batches(lstm_stack *s, int max_batch);
+
 /* Releases everything the stack owns (waits for its pending work first).
  * NULL is ignored. */
 void lstm_stack_destroy(lstm_stack *s);
@@ -305,6 +317,26 @@ int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
                             float *y, int batch, int steps, int direction,
                             int cluster_size, int windows_per_chunk, int chunks,
                             int threads_per_block, void *stream);
+
+/* Step 2+3 fused, device, for small batches: one layer's recurrence that
+ * computes its own input projection.  Each cluster (8 CTAs of 256 threads)
+ * runs one window; half of each CTA's threads hold the layer's input weights
+ * for the CTA's units (W = wp_hi + wp_lo, the packed planes) and, running
+ * ahead of the recurrence, turn every step's input row into partial sums
+ * that the recurrence lanes add to theirs before the reduction, so
+ * z = W x_t + R h + bias with no G buffer (lstmproj.rs module docs: the
+ * projection of every step, then the recurrence).
+ *   x     : device [batch][steps][in_width], in_width a multiple of 4, <= kp
+ *           (the layer input: the stack input or the previous layer's y)
+ *   wp_hi, wp_lo : device [1024][kp], kp 64 or 256 (lstm_pack_layer)
+ *   rp, bias, y, batch, steps, direction : as lstm_recurrence
+ * The products are fp32 FMAs (not 3xTF32).  All clusters must run at once:
+ * batch (times 2 for LSTM_BOTH_DIRECTIONS) at most the clusters the device
+ * holds (LSTM_E_INVALID otherwise).  Errors as lstm_recurrence. */
+int lstm_recurrence_fused(const float *x, int in_width, const float *wp_hi,
+                          const float *wp_lo, int kp, const float *rp,
+                          const float *bias, float *y, int batch, int steps,
+                          int direction, void *stream);
 
 /* Measurement: the recurrence's per-step latency floor.  Launches exactly
  * what lstm_recurrence launches for this batch (same variant, grid, cluster
