@@ -1023,6 +1023,205 @@ done:
     ptx::cluster_wait_acquire();
 }
 
+// Two units per 8-lane group (one window per cluster, clusters of 8 CTAs of
+// 64 threads): lane kc of group g holds the R slices of two hidden units,
+// base + g and base + 4 + g (base = the warp's first of 8 units), for K chunk
+// kc, loads its h chunk once and multiplies it into 8 gate rows.  Against one
+// unit per group this halves the shared-memory loads of h per step (every
+// 128-bit load costs the load/store unit four cycles however many lanes
+// read the same address) and the warps per SM, for twice the FFMA2 chains per
+// lane.  The partial sums of the two units are reduced like two windows of
+// the two-window variants (the same 8-value butterfly, select-free: lane kc
+// keeps its partial sums in the order p -> p ^ kc, which here only changes
+// which unit and gate row a register slot holds, since every slot reads the
+// same h), so each unit's z is the sum of the same eight chunk partials in the
+// same order as in every other variant: results are bitwise identical.
+template <bool FLOOR = false>
+__global__ void __launch_bounds__(64, 1)
+recurrence_u2_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
+                     const float *__restrict__ bias_in, float *__restrict__ y, int batch, int steps,
+                     int dir_in, unsigned *fault, unsigned long long wait_limit_ns, int withhold)
+{
+    constexpr int C = 8;
+    constexpr int THREADS = 64;
+    constexpr int GD = 64;  // projection-value ring depth (steps)
+
+    __shared__ __align__(16) float hbuf[2][HROW];
+    __shared__ __align__(8) uint64_t hbar[2];
+    __shared__ int abort_flag;
+    __shared__ __align__(16) float gring[GD][THREADS];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int kc = tid & 7;
+    const int grp = (tid >> 3) & 3;
+    const int jj = kc >> 2;                    // after the reduction: unit index 0/1
+    const int q = kc & 3;                      // and gate
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cid = static_cast<int>(ptx::cluster_id_x());
+    const int direction = dir_in >= 0 ? dir_in : (cid & 1);
+    const int win = dir_in >= 0 ? cid : (cid >> 1);
+    const float *__restrict__ rp = rp_in + (dir_in >= 0 ? 0 : direction * kGates * kHidden);
+    const float *__restrict__ bias = bias_in + (dir_in >= 0 ? 0 : direction * kGates);
+    const int base = static_cast<int>(rank) * 16 + (tid >> 5) * 8;  // the warp's 8 units
+    volatile int *abort_v = &abort_flag;
+
+    // R slices of the group's two units for chunk kc, scaled by k_q; slot
+    // (j, gq) holds unit index j ^ (kc >> 2), gate gq ^ (kc & 3)
+    float2 r2[2][4][KLEN / 2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq) {
+            const int jl = j ^ (kc >> 2), ql = gq ^ (kc & 3);
+            const int row = 4 * (base + 4 * jl + grp) + ql;
+            const float kq = ql == 2 ? -2.0f * kLog2e : -kLog2e;
+            const float2 *src = reinterpret_cast<const float2 *>(rp + row * kHidden + kc * KLEN);
+#pragma unroll
+            for (int i = 0; i < KLEN / 2; ++i)
+                r2[j][gq][i] = make_float2(src[i].x * kq, src[i].y * kq);
+        }
+    // the value this lane holds after the reduction: unit base + 4 jj + grp, gate q
+    const int u_mine = base + 4 * jj + grp;
+    const float gk = q == 2 ? -2.0f * kLog2e : -kLog2e;
+    const float bias_v = bias[4 * u_mine + q] * gk;
+    const float act_m = q == 2 ? 2.0f : 1.0f;
+    const float act_a = q == 2 ? -1.0f : 0.0f;
+    const float *gcol = g + direction * kGates + 4 * u_mine + q +
+                        static_cast<long>(win) * steps * kGateColumns;
+
+    for (int i = tid; i < 2 * HROW; i += THREADS)
+        (&hbuf[0][0])[i] = 0.0f;
+    const uint32_t bar_bytes = kHidden * 4;
+    if (tid == 0) {
+        ptx::mbar_init(&hbar[0], 1);
+        ptx::mbar_init(&hbar[1], 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+        if (steps > 1)
+            ptx::mbar_arrive_expect_tx(&hbar[1], bar_bytes);
+        if (steps > 2)
+            ptx::mbar_arrive_expect_tx(&hbar[0], bar_bytes);
+    }
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+    ptx::griddep_launch_dependents();
+
+    // senders: lane group*4 + kc%4 (< 8) pushes units base + 4 jj .. +3 to
+    // that peer; lanes kc = 0 and 4 of group 0 store them to y
+    const int sender = grp * 4 + (kc & 3);
+    const int u4 = base + 4 * jj;  // first of the four units this lane gathers
+    const uint32_t hbase = ptx::smem_u32(&hbuf[0][0]);
+    const uint32_t bar_base = ptx::smem_u32(&hbar[0]);
+    const uint32_t send_off =
+        static_cast<uint32_t>(((u4 / KLEN) * CHUNK_STRIDE + (u4 % KLEN)) * 4);
+    const int peer = sender < C ? sender : C - 1;
+    uint32_t rdst[2], rbar[2];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        rdst[b] = ptx::map_to_rank(hbase + static_cast<uint32_t>(b * HROW * 4) + send_off,
+                                   static_cast<uint32_t>(peer));
+        rbar[b] = ptx::map_to_rank(bar_base + static_cast<uint32_t>(b * 8),
+                                   static_cast<uint32_t>(peer));
+    }
+    float *yrow = y + static_cast<long>(win) * steps * kOutput + direction * kHidden + u4;
+
+    auto gissue = [&](int s) {
+        const long t = direction ? steps - 1 - s : s;
+        const bool ok = s < steps;
+        ptx::cp_async_4(ptx::smem_u32(&gring[s & (GD - 1)][tid]),
+                        ok ? gcol + t * kGateColumns : g, ok ? 4u : 0u);
+        ptx::cp_async_commit();
+    };
+    for (int s = 0; s < GD; ++s)
+        gissue(s);
+
+    float c = 0.0f;
+    auto step = [&](auto PAR, int s) -> bool {
+        constexpr int par = decltype(PAR)::value;
+        const int t = direction ? steps - 1 - s : s;
+        ptx::cp_async_wait<GD - 1>();
+        const float gv = gring[s & (GD - 1)][tid];
+        if (s > 0) {
+            const uint32_t phase = ((s - 1) >> 1) & 1;
+            if (!ptx::mbar_try_wait_cluster(&hbar[par], phase)) {
+                if (*abort_v)
+                    return false;
+                const uint64_t start = ptx::globaltimer();
+                while (!ptx::mbar_try_wait_cluster(&hbar[par], phase)) {
+                    if (*abort_v)
+                        return false;
+                    if (ptx::globaltimer() - start > wait_limit_ns) {
+                        atomicOr(fault, kFaultRecurrence);
+                        *abort_v = 1;
+                        return false;
+                    }
+                }
+            }
+            if (tid == 0 && s + 2 < steps)
+                ptx::mbar_arrive_expect_tx(&hbar[par], bar_bytes);
+        }
+        float h;
+        if constexpr (FLOOR) {
+            h = fmaf(hbuf[par][kc * CHUNK_STRIDE], 0.5f, gv * 0.001f);
+        } else {
+            const float4 *hp = reinterpret_cast<const float4 *>(&hbuf[par][kc * CHUNK_STRIDE]);
+            const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+            const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y}, {h1.z, h1.w},
+                                  {h2.x, h2.y}, {h2.z, h2.w}, {h3.x, h3.y}, {h3.z, h3.w}};
+            float part[8];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int gq = 0; gq < 4; ++gq) {
+                    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc = __ffma2_rn(r2[j][gq][i], hh[i], acc);
+                    part[4 * j + gq] = acc.x + acc.y;
+                }
+            float a[4], b2[2], held[1];
+            reduce_level<8, true>(part, a, 4, (kc & 4) != 0);
+            reduce_level<4, true>(a, b2, 2, (kc & 2) != 0);
+            reduce_level<2, true>(b2, held, 1, (kc & 1) != 0);
+            const float w = held[0] + fmaf(gv, gk, bias_v);
+            const float act = fmaf(act_m, inv_one_plus_ex2(w), act_a);
+            float gate[4];
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq)
+                gate[gq] = __shfl_sync(0xffffffffu, act, 4 * jj + gq, 8);
+            c = gate[1] * c + gate[0] * gate[2];
+            const float r = inv_one_plus_ex2(c * (-2.0f * kLog2e));
+            h = fmaf(2.0f * gate[3], r, -gate[3]);
+        }
+        float h4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            h4[k] = __shfl_sync(0xffffffffu, h, 8 * k + kc);
+        if (s + 1 < steps && sender < C)
+            ptx::st_async_v4(rdst[par ^ 1], h4[0], h4[1], h4[2], h4[3], rbar[par ^ 1]);
+        if (sender == 0 && lane < 8)
+            *reinterpret_cast<float4 *>(yrow + static_cast<long>(t) * kOutput) =
+                make_float4(h4[0], h4[1], h4[2], h4[3]);
+        gissue(s + GD);
+        return true;
+    };
+
+    if (withhold && rank == 0)
+        goto done;
+    for (int s0 = 0; s0 < steps; s0 += 2) {
+        if (!step(std::integral_constant<int, 0>{}, s0))
+            break;
+        if (s0 + 1 < steps && !step(std::integral_constant<int, 1>{}, s0 + 1))
+            break;
+    }
+done:
+    ptx::cp_async_wait_all();
+    __syncwarp();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+}
+
 struct Variant {
     int cluster;
     int nw;       // windows per chunk
@@ -1055,6 +1254,9 @@ const Variant kVariants[] = {
     variant<16, 2, 1, 64>(),    variant<4, 4, 2>(),      variant<4, 4, 4>(),
     variant<4, 8, 1>(),         variant<4, 8, 2>(),      variant<4, 4, 1>(),
     variant<8, 4, 1, 128>(),    variant<8, 8, 1, 128>(),
+    // two units per 8-lane group, one window per cluster of 64-thread CTAs
+    Variant{8, 1, 1, 1, 64, reinterpret_cast<const void *>(&recurrence_u2_kernel<false>),
+            reinterpret_cast<const void *>(&recurrence_u2_kernel<true>)},
 };
 
 // threads == 0: the variant's default block size
@@ -1070,31 +1272,48 @@ const Variant *find_variant(int cluster, int nw, int nch, int threads = 0)
 int max_active_clusters(const Variant &v, int *out);
 
 // The default variant for a batch: the candidate with the least estimated
-// step time, waves x full-load step time, where a wave is as many clusters
-// (for both directions) as the device runs at once
-// (cudaOccupancyMaxActiveClusters, queried per device) and the full-load
-// step times are measured with both directions running (GB300, T = 589, us):
-//   narrow clusters of 8, 128 threads, one window per cluster      0.57
-//   the same with 2 windows per group                             0.70
-//   clusters of 4, one window per group                           0.58
-//   clusters of 4, 2 chunks of 2 windows per lane                 0.85
-//   narrow clusters of 8, 4 windows per group                     1.10
-//   clusters of 4, 2 chunks of 4 windows (chunk-major)            1.33
-//   clusters of 4, 2 chunks of 8 windows (chunk-major)            2.22
-// (more windows per chunk: fewer gather shuffles per window and more
-// independent work per lane, so more windows per step on the same SMs).  A
-// partly loaded wave runs faster than its full-load time (0.40 us at one
-// window); ties go to the earlier candidate.
+// time per step.  A wave is as many clusters (for both directions) as the
+// device runs at once (cudaOccupancyMaxActiveClusters, queried per device);
+// a batch takes some full waves and a last, partly loaded one, and a wave's
+// step time grows with its load: the clusters share SMs, L1 and the
+// exchange network.  Step times measured with both directions running
+// (GB300, T = 589, us) at last-wave loads 0, 1/4, 1/2, 3/4 and 1:
+//   narrow clusters of 8, 128 threads, one window per cluster
+//       .345 .402 .427 .490 .533
+//   narrow clusters of 8, 64 threads, two units per lane group
+//       .370 .394 .410 .458 .474
+//   narrow clusters of 8, 128 threads, 2 windows per group
+//       .432 .490 .532 .600 .641
+//   clusters of 4, one window per group
+//       .411 .411 .444 .515 .519
+//   clusters of 4, 2 chunks of 2 windows per lane
+//       .749 .787 .790 .797 .798
+//   narrow clusters of 8, 4 windows per group
+//       .533 .690 .794 .900 1.062
+//   clusters of 4, 2 chunks of 4 windows (chunk-major)
+//       1.16 1.27 1.27 1.275 1.277
+//   clusters of 4, 2 chunks of 8 windows (chunk-major)
+//       1.785 2.18 2.18 2.185 2.19
+// (between the points the time is interpolated linearly).  More windows per
+// chunk: fewer gather shuffles per window and more independent work per
+// lane, so more windows per step on the same SMs but a slower step; two
+// units per lane group halve the h loads per unit, which pays once the
+// wave shares its SMs.  Ties go to the earlier candidate.
 const Variant *choose_variant(int batch)
 {
     struct Candidate {
         int cluster, nw, nch, threads;
-        float us_per_step;  // full load
+        float us[5];  // step time at last-wave load 0, 1/4, 1/2, 3/4, 1
     };
-    static const Candidate cand[] = {{8, 1, 1, 128, 0.57f}, {8, 2, 1, 128, 0.70f},
-                                     {4, 1, 1, 0, 0.58f},   {4, 2, 2, 0, 0.85f},
-                                     {8, 4, 1, 128, 1.10f}, {4, 4, 2, 0, 1.33f},
-                                     {4, 8, 2, 0, 2.22f}};
+    static const Candidate cand[] = {
+        {8, 1, 1, 128, {0.345f, 0.402f, 0.427f, 0.490f, 0.533f}},
+        {8, 1, 1, 64, {0.370f, 0.394f, 0.410f, 0.458f, 0.474f}},
+        {8, 2, 1, 128, {0.432f, 0.490f, 0.532f, 0.600f, 0.641f}},
+        {4, 1, 1, 0, {0.411f, 0.411f, 0.444f, 0.515f, 0.519f}},
+        {4, 2, 2, 0, {0.749f, 0.787f, 0.790f, 0.797f, 0.798f}},
+        {8, 4, 1, 128, {0.533f, 0.690f, 0.794f, 0.900f, 1.062f}},
+        {4, 4, 2, 0, {1.160f, 1.270f, 1.270f, 1.275f, 1.277f}},
+        {4, 8, 2, 0, {1.785f, 2.180f, 2.180f, 2.185f, 2.190f}}};
     constexpr int N = sizeof(cand) / sizeof(cand[0]);
     static std::mutex mu;
     static int fits[64][N];
@@ -1122,8 +1341,14 @@ const Variant *choose_variant(int batch)
             continue;
         const long tiles = (static_cast<long>(batch) + v->tile - 1) / v->tile;
         const long per_wave = fits[dev][i] / 2;  // clusters per direction at once
-        const long waves = (tiles + per_wave - 1) / per_wave;
-        const float cost = static_cast<float>(waves) * cand[i].us_per_step;
+        const long full = tiles / per_wave;
+        const long rest = tiles - full * per_wave;
+        float cost = static_cast<float>(full) * cand[i].us[4];
+        if (rest > 0) {
+            const float x = 4.0f * static_cast<float>(rest) / static_cast<float>(per_wave);
+            const int k = x >= 4.0f ? 3 : static_cast<int>(x);
+            cost += cand[i].us[k] + (x - static_cast<float>(k)) * (cand[i].us[k + 1] - cand[i].us[k]);
+        }
         if (!best || cost < best_cost) {
             best = v;
             best_cost = cost;
