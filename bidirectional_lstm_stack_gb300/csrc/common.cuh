@@ -421,6 +421,14 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes)
                  : "memory");
 }
+// The same for 16 bytes (both addresses 16-byte aligned; `bytes` 16 or 0),
+// cached in L2 only.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;" ::: "memory");

@@ -44,6 +44,7 @@
 // The arithmetic per (window, unit, gate) is the same for every cluster size
 // and tile width (same K chunks, same pairing, same reduction tree), so all
 // variants give bitwise-identical results.
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 #include <utility>
@@ -428,14 +429,20 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
             const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
             const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y}, {h1.z, h1.w},
                                   {h2.x, h2.y}, {h2.z, h2.w}, {h3.x, h3.y}, {h3.z, h3.w}};
+            // the four gate rows' chains advance together (independent
+            // FMAs back to back); each chain's order over i is fixed
+            float2 acc[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float2 acc = make_float2(0.0f, 0.0f);
+            for (int q = 0; q < 4; ++q)
+                acc[q] = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc = __ffma2_rn(r2[q][i], hh[i], acc);
-                part[w * 4 + q] = acc.x + acc.y;
-            }
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    acc[q] = __ffma2_rn(r2[q][i], hh[i], acc[q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                part[w * 4 + q] = acc[q].x + acc[q].y;
         }
     };
     // 2. fixed butterfly over the 8 K-chunk lanes
@@ -598,14 +605,18 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
                     const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y},
                                           {h1.z, h1.w}, {h2.x, h2.y}, {h2.z, h2.w},
                                           {h3.x, h3.y}, {h3.z, h3.w}};
+                    float2 acc[4];
     #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float2 acc = make_float2(0.0f, 0.0f);
+                    for (int q = 0; q < 4; ++q)
+                        acc[q] = make_float2(0.0f, 0.0f);
     #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            acc = __ffma2_rn(r2[q][i], hh[i], acc);
-                        part[ch][w * 4 + q] = acc.x + acc.y;
-                    }
+                    for (int i = 0; i < 8; ++i)
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            acc[q] = __ffma2_rn(r2[q][i], hh[i], acc[q]);
+    #pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        part[ch][w * 4 + q] = acc[q].x + acc[q].y;
                 }
             }
 
@@ -1169,17 +1180,21 @@ recurrence_u2_kernel(const float *__restrict__ g, const float *__restrict__ rp_i
             const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
             const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y}, {h1.z, h1.w},
                                   {h2.x, h2.y}, {h2.z, h2.w}, {h3.x, h3.y}, {h3.z, h3.w}};
+            // the eight rows' chains advance together; each chain's order
+            // over i is fixed
+            float2 acc[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                acc[r] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    acc[r] = __ffma2_rn(r2[r >> 2][r & 3][i], hh[i], acc[r]);
             float part[8];
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int gq = 0; gq < 4; ++gq) {
-                    float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        acc = __ffma2_rn(r2[j][gq][i], hh[i], acc);
-                    part[4 * j + gq] = acc.x + acc.y;
-                }
+            for (int r = 0; r < 8; ++r)
+                part[r] = acc[r].x + acc[r].y;
             float a[4], b2[2], held[1];
             reduce_level<8, true>(part, a, 4, (kc & 4) != 0);
             reduce_level<4, true>(a, b2, 2, (kc & 2) != 0);
@@ -1222,6 +1237,311 @@ done:
     ptx::cluster_wait_acquire();
 }
 
+// Two units per 8-lane group for several windows per lane: NW = 4 or 8
+// windows per chunk, NCH = 1 or 2 chunks, clusters of C = 4 or 8 CTAs of
+// 512 / C threads (a CTA's 128 / C units, two per group).  Lane kc of group g
+// holds the R slices of units base + g and base + 4 + g (base = the warp's
+// first of 8 units) for K chunk kc and multiplies each window's h chunk into
+// their 8 gate rows: half the shared-memory loads of h per multiply-add of
+// the one-unit variants.  The select-free butterfly keeps a chunk's partial
+// sums in the order L -> L ^ (NW kc), L = 8 w + 4 j + q (window w, unit j,
+// gate q), so the three levels leave lane kc the four gates of whole cells
+// (window kc / 2 of unit kc % 2 for NW = 4; both units of window kc for
+// NW = 8) and the cell update needs no gate gather.  The order only permutes
+// which unit a register slot holds and which window row a slot reads (the
+// senders store window w of K chunk k at row w ^ (NW k / 8)): every unit's z
+// is the same sums in the same order as in every other variant, so results
+// are bitwise identical.  Two chunks run chunk-major with a barrier pair
+// each, so one chunk's exchange is in flight while the other computes.
+template <int C, int NW, int NCH, bool FLOOR = false>
+__global__ void __launch_bounds__(512 / C, 1)
+recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
+                      const float *__restrict__ bias_in, float *__restrict__ y, int batch,
+                      int steps, int dir_in, unsigned *fault, unsigned long long wait_limit_ns,
+                      int withhold)
+{
+    constexpr int THREADS = 512 / C;
+    constexpr int UPC = kHidden / C;  // units per CTA
+    constexpr int TW = NW * NCH;      // windows per cluster
+    constexpr int V = 8 * NW;         // partial sums per lane and chunk
+    constexpr int HV = V / 8;         // values a lane holds after the reduction
+    constexpr int CELLS = HV / 4;     // cells a lane updates per chunk
+    constexpr int NPEER = C / 4;      // peers each holder of an h quad sends to
+    constexpr bool CM = NCH > 1;
+    constexpr int NBAR = CM ? NCH : 1;
+    static_assert((C == 4 || C == 8) && (NW == 4 || NW == 8) && (NCH == 1 || NCH == 2),
+                  "shape");
+    // projection values: a ring of GD steps in shared memory, each lane's
+    // four gate values of a cell one 16-byte asynchronous copy
+    constexpr int GD_FIT = (45056 - 2 * TW * HROW * 4) / (NCH * CELLS * THREADS * 16);
+    static_assert(GD_FIT >= 4, "ring");
+    constexpr int GD = GD_FIT >= 32 ? 32 : GD_FIT >= 16 ? 16 : GD_FIT >= 8 ? 8 : 4;
+    constexpr float K0 = -kLog2e, K2 = -2.0f * kLog2e;  // k_q of the gates, the candidate
+
+    __shared__ __align__(16) float hbuf[2][TW][HROW];
+    __shared__ __align__(8) uint64_t hbar[2][NBAR];
+    __shared__ int abort_flag;
+    __shared__ __align__(16) float4 gring[GD][NCH * CELLS][THREADS];
+
+    const int tid = threadIdx.x;
+    const int kc = tid & 7;
+    const int grp = (tid >> 3) & 3;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cid = static_cast<int>(ptx::cluster_id_x());
+    const int direction = dir_in >= 0 ? dir_in : (cid & 1);
+    const int tile = dir_in >= 0 ? cid : (cid >> 1);
+    const float *__restrict__ rp = rp_in + (dir_in >= 0 ? 0 : direction * kGates * kHidden);
+    const float *__restrict__ bias = bias_in + (dir_in >= 0 ? 0 : direction * kGates);
+    const int base = static_cast<int>(rank) * UPC + (tid >> 5) * 8;  // the warp's 8 units
+    const int tile_w0 = tile * TW;
+    volatile int *abort_v = &abort_flag;
+    // window and unit parts of the lane order L -> L ^ (HV k) of K chunk k
+    auto xw = [](int k) { return (HV * k) >> 3; };
+    auto xj = [](int k) { return ((HV * k) >> 2) & 1; };
+
+    // R slices: slot (js, q) holds gate q of unit index js ^ xj(kc), scaled by k_q
+    float2 r2[2][4][KLEN / 2];
+#pragma unroll
+    for (int js = 0; js < 2; ++js)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = 4 * (base + 4 * (js ^ xj(kc)) + grp) + q;
+            const float kq = q == 2 ? K2 : K0;
+            const float2 *src = reinterpret_cast<const float2 *>(rp + row * kHidden + kc * KLEN);
+#pragma unroll
+            for (int i = 0; i < KLEN / 2; ++i)
+                r2[js][q][i] = make_float2(src[i].x * kq, src[i].y * kq);
+        }
+
+    // the cells this lane updates: logical values HV kc + 4 ci .. + 3
+    int wc[CELLS];
+    float bias_v[CELLS][4];
+    const float *gsrc[CELLS];
+    uint32_t send_off[CELLS];
+    int u4c[CELLS];
+#pragma unroll
+    for (int ci = 0; ci < CELLS; ++ci) {
+        const int l = HV * kc + 4 * ci;
+        wc[ci] = l >> 3;
+        const int jc = (l >> 2) & 1;
+        const int u = base + 4 * jc + grp;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            bias_v[ci][q] = bias[4 * u + q] * (q == 2 ? K2 : K0);
+        gsrc[ci] = g + direction * kGates + 4 * u +
+                   static_cast<long>(tile_w0 + wc[ci]) * steps * kGateColumns;
+        // after the h gather: units u4 .. u4 + 3 of window wc, in K chunk u4 / 16
+        const int u4 = base + 4 * jc;
+        u4c[ci] = u4;
+        const int k = u4 / KLEN;
+        send_off[ci] = static_cast<uint32_t>(
+            ((wc[ci] ^ xw(k)) * HROW + k * CHUNK_STRIDE + (u4 % KLEN)) * 4);
+    }
+
+    uint32_t bar_bytes[NBAR];
+#pragma unroll
+    for (int b = 0; b < NBAR; ++b) {
+        const int w0 = tile_w0 + (CM ? b * NW : 0);
+        bar_bytes[b] = static_cast<uint32_t>(kHidden * 4 * max(0, min(CM ? NW : TW, batch - w0)));
+    }
+
+    for (int i = tid; i < 2 * TW * HROW; i += THREADS)
+        (&hbuf[0][0][0])[i] = 0.0f;
+    if (tid == 0) {
+        for (int b = 0; b < NBAR; ++b) {
+            ptx::mbar_init(&hbar[0][b], 1);
+            ptx::mbar_init(&hbar[1][b], 1);
+        }
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+        // a chunk with no window inside the batch has no barrier traffic
+        for (int b = 0; b < NBAR; ++b) {
+            if (bar_bytes[b] == 0)
+                continue;
+            if (steps > 1)
+                ptx::mbar_arrive_expect_tx(&hbar[1][b], bar_bytes[b]);
+            if (steps > 2)
+                ptx::mbar_arrive_expect_tx(&hbar[0][b], bar_bytes[b]);
+        }
+    }
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+    ptx::griddep_launch_dependents();
+
+    // this lane's pushes: the four holders of an h quad (one per group)
+    // send to peers grp, grp + 4 (C = 8) or grp (C = 4)
+    const uint32_t hbase = ptx::smem_u32(&hbuf[0][0][0]);
+    const uint32_t bar_base = ptx::smem_u32(&hbar[0][0]);
+    uint32_t rdst[CELLS][NPEER][2], rbar[NPEER][2];
+#pragma unroll
+    for (int r = 0; r < NPEER; ++r) {
+        const uint32_t peer = static_cast<uint32_t>(grp + 4 * r);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int ci = 0; ci < CELLS; ++ci)
+                rdst[ci][r][b] = ptx::map_to_rank(
+                    hbase + static_cast<uint32_t>(b * TW * HROW * 4) + send_off[ci], peer);
+            rbar[r][b] = ptx::map_to_rank(bar_base + static_cast<uint32_t>(b * NBAR * 8), peer);
+        }
+    }
+
+    auto valid = [&](int ch, int ci) { return tile_w0 + ch * NW + wc[ci] < batch; };
+    auto gissue = [&](int s) {
+        const long t = direction ? steps - 1 - s : s;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+            for (int ci = 0; ci < CELLS; ++ci) {
+                const bool ok = s < steps && valid(ch, ci);
+                const float *src =
+                    ok ? gsrc[ci] + (static_cast<long>(ch) * NW * steps + t) * kGateColumns : g;
+                ptx::cp_async_16(ptx::smem_u32(&gring[s & (GD - 1)][ch * CELLS + ci][tid]), src,
+                                 ok ? 16u : 0u);
+            }
+        ptx::cp_async_commit();
+    };
+    for (int s = 0; s < GD; ++s)
+        gissue(s);
+
+    float c[NCH][CELLS];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int ci = 0; ci < CELLS; ++ci)
+            c[ch][ci] = 0.0f;
+
+    // waits until phase `phase` of `bar` completes; false if the wait ran out
+    // here or in another warp (this thread then neither re-arms nor pushes)
+    auto wait_phase = [&](uint64_t *bar, uint32_t phase) -> bool {
+        if (ptx::mbar_try_wait_cluster(bar, phase))
+            return true;
+        if (*abort_v)
+            return false;
+        const uint64_t start = ptx::globaltimer();
+        while (!ptx::mbar_try_wait_cluster(bar, phase)) {
+            if (*abort_v)
+                return false;
+            if (ptx::globaltimer() - start > wait_limit_ns) {
+                atomicOr(fault, kFaultRecurrence);
+                *abort_v = 1;
+                return false;
+            }
+        }
+        return true;
+    };
+
+    auto step = [&](auto PAR, int s) -> bool {
+        constexpr int par = decltype(PAR)::value;
+        const int t = direction ? steps - 1 - s : s;
+        const bool push = s + 1 < steps;
+        ptx::cp_async_wait<GD - 1>();
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            // this chunk's h_{s-1} complete in buffer `par` (a chunk past the
+            // batch has no traffic); then re-arm the barrier for h_{s+1}
+            if (s > 0 && bar_bytes[ch] != 0) {
+                if (!wait_phase(&hbar[par][ch], ((s - 1) >> 1) & 1))
+                    return false;
+                if (tid == 0 && s + 2 < steps)
+                    ptx::mbar_arrive_expect_tx(&hbar[par][ch], bar_bytes[ch]);
+            }
+            float h[CELLS];
+            if constexpr (FLOOR) {
+#pragma unroll
+                for (int ci = 0; ci < CELLS; ++ci) {
+                    const float4 gv = gring[s & (GD - 1)][ch * CELLS + ci][tid];
+                    h[ci] = fmaf(hbuf[par][ch * NW][kc * CHUNK_STRIDE], 0.5f, gv.x * 0.001f);
+                }
+            } else {
+                float part[V];
+#pragma unroll
+                for (int ws = 0; ws < NW; ++ws) {
+                    const float4 *hp =
+                        reinterpret_cast<const float4 *>(&hbuf[par][ch * NW + ws][kc * CHUNK_STRIDE]);
+                    const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+                    const float2 hh[8] = {{h0.x, h0.y}, {h0.z, h0.w}, {h1.x, h1.y},
+                                          {h1.z, h1.w}, {h2.x, h2.y}, {h2.z, h2.w},
+                                          {h3.x, h3.y}, {h3.z, h3.w}};
+                    // the eight rows' chains advance together; each
+                    // chain's order over i is fixed
+                    float2 acc[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        acc[r] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+#pragma unroll
+                        for (int r = 0; r < 8; ++r)
+                            acc[r] = __ffma2_rn(r2[r >> 2][r & 3][i], hh[i], acc[r]);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        part[ws * 8 + r] = acc[r].x + acc[r].y;
+                }
+                float a[V / 2], b2[V / 4], held[V / 8];
+                reduce_level<V, true>(part, a, 4, (kc & 4) != 0);
+                reduce_level<V / 2, true>(a, b2, 2, (kc & 2) != 0);
+                reduce_level<V / 4, true>(b2, held, 1, (kc & 1) != 0);
+#pragma unroll
+                for (int ci = 0; ci < CELLS; ++ci) {
+                    const float4 gv = gring[s & (GD - 1)][ch * CELLS + ci][tid];
+                    const float gq[4] = {gv.x, gv.y, gv.z, gv.w};
+                    float act[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float w =
+                            held[4 * ci + q] + fmaf(gq[q], q == 2 ? K2 : K0, bias_v[ci][q]);
+                        act[q] = q == 2 ? fmaf(2.0f, inv_one_plus_ex2(w), -1.0f)
+                                        : fmaf(1.0f, inv_one_plus_ex2(w), 0.0f);
+                    }
+                    c[ch][ci] = act[1] * c[ch][ci] + act[0] * act[2];
+                    const float r = inv_one_plus_ex2(c[ch][ci] * (-2.0f * kLog2e));
+                    h[ci] = fmaf(2.0f * act[3], r, -act[3]);
+                }
+            }
+            // gather the group's four units of each cell's window, push the
+            // quad to the peers, store it to y
+#pragma unroll
+            for (int ci = 0; ci < CELLS; ++ci) {
+                float h4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    h4[k] = __shfl_sync(0xffffffffu, h[ci], 8 * k + kc);
+                if (valid(ch, ci)) {
+                    if (push) {
+                        const uint32_t off = static_cast<uint32_t>(ch * NW * HROW * 4);
+                        const uint32_t bar_off = static_cast<uint32_t>(CM ? ch * 8 : 0);
+#pragma unroll
+                        for (int r = 0; r < NPEER; ++r)
+                            ptx::st_async_v4(rdst[ci][r][par ^ 1] + off, h4[0], h4[1], h4[2],
+                                             h4[3], rbar[r][par ^ 1] + bar_off);
+                    }
+                    if (grp == 0)
+                        *reinterpret_cast<float4 *>(
+                            y + (static_cast<long>(tile_w0 + ch * NW + wc[ci]) * steps + t) * kOutput +
+                            direction * kHidden + u4c[ci]) = make_float4(h4[0], h4[1], h4[2], h4[3]);
+                }
+            }
+        }
+        gissue(s + GD);
+        return true;
+    };
+
+    if (withhold && rank == 0)
+        goto done;
+    for (int s0 = 0; s0 < steps; s0 += 2) {
+        if (!step(std::integral_constant<int, 0>{}, s0))
+            break;
+        if (s0 + 1 < steps && !step(std::integral_constant<int, 1>{}, s0 + 1))
+            break;
+    }
+done:
+    ptx::cp_async_wait_all();
+    __syncwarp();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+}
+
 struct Variant {
     int cluster;
     int nw;       // windows per chunk
@@ -1241,6 +1561,14 @@ Variant variant()
                        &recurrence_kernel<C, NW, NCH, THREADS, true>)};
 }
 
+template <int C, int NW, int NCH>
+Variant variant_u2w()
+{
+    return Variant{C, NW, NCH, NW * NCH, 512 / C,
+                   reinterpret_cast<const void *>(&recurrence_u2w_kernel<C, NW, NCH>),
+                   reinterpret_cast<const void *>(&recurrence_u2w_kernel<C, NW, NCH, true>)};
+}
+
 // "Narrow" variants (one window group per CTA: 128 threads for clusters of
 // 8, 64 for clusters of 16) give each SM sub-partition fewer warps, for small
 // batches where wider CTAs would mostly compute padding windows.
@@ -1257,6 +1585,10 @@ const Variant kVariants[] = {
     // two units per 8-lane group, one window per cluster of 64-thread CTAs
     Variant{8, 1, 1, 1, 64, reinterpret_cast<const void *>(&recurrence_u2_kernel<false>),
             reinterpret_cast<const void *>(&recurrence_u2_kernel<true>)},
+    // two units per 8-lane group, several windows per lane
+    variant_u2w<8, 4, 1>(), variant_u2w<8, 4, 2>(), variant_u2w<4, 4, 1>(),
+    variant_u2w<4, 4, 2>(), variant_u2w<8, 8, 1>(), variant_u2w<4, 8, 1>(),
+    variant_u2w<8, 8, 2>(),
 };
 
 // threads == 0: the variant's default block size
@@ -1272,55 +1604,50 @@ const Variant *find_variant(int cluster, int nw, int nch, int threads = 0)
 int max_active_clusters(const Variant &v, int *out);
 
 // The default variant for a batch: the candidate with the least estimated
-// time per step.  A wave is as many clusters (for both directions) as the
-// device runs at once (cudaOccupancyMaxActiveClusters, queried per device);
-// a batch takes some full waves and a last, partly loaded one, and a wave's
-// step time grows with its load: the clusters share SMs, L1 and the
-// exchange network.  Step times measured with both directions running
-// (GB300, T = 589, us) at last-wave loads 0, 1/4, 1/2, 3/4 and 1:
-//   narrow clusters of 8, 128 threads, one window per cluster
-//       .345 .402 .427 .490 .533
-//   narrow clusters of 8, 64 threads, two units per lane group
-//       .370 .394 .410 .458 .474
-//   narrow clusters of 8, 128 threads, 2 windows per group
-//       .432 .490 .532 .600 .641
-//   clusters of 4, one window per group
-//       .411 .411 .444 .515 .519
-//   clusters of 4, 2 chunks of 2 windows per lane
-//       .749 .787 .790 .797 .798
-//   narrow clusters of 8, 4 windows per group
-//       .533 .690 .794 .900 1.062
-//   clusters of 4, 2 chunks of 4 windows (chunk-major)
-//       1.16 1.27 1.27 1.275 1.277
-//   clusters of 4, 2 chunks of 8 windows (chunk-major)
-//       1.785 2.18 2.18 2.185 2.19
-// (between the points the time is interpolated linearly).  More windows per
-// chunk: fewer gather shuffles per window and more independent work per
-// lane, so more windows per step on the same SMs but a slower step; two
-// units per lane group halve the h loads per unit, which pays once the
-// wave shares its SMs.  Ties go to the earlier candidate.
+// time per step.  A launch's step time is set by how many clusters share the
+// GPU: it stays flat while the clusters (both directions) fit one SM each
+// way, then jumps as clusters start to share SMs (their FFMA2, shared-memory
+// loads and exchanges queue behind one another).  Each candidate carries its
+// measured step times (GB300, 152 SMs, both directions in one launch,
+// T = 589, us) as plateaus: "up to k tiles per direction: t", including the
+// second wave where a candidate stays competitive there; a batch past the
+// last plateau runs as repeated waves of it.  On another SM count the tile
+// counts scale with it.  Chosen this way, the step is within 1.5 % of the
+// fastest candidate's at every batch from 1 to 320 windows (measured).
+// Ties go to the earlier candidate.
 const Variant *choose_variant(int batch)
 {
+    struct Plateau {
+        int tiles;  // up to this many tiles per direction
+        float us;   // time per step
+    };
     struct Candidate {
-        int cluster, nw, nch, threads;
-        float us[5];  // step time at last-wave load 0, 1/4, 1/2, 3/4, 1
+        int cluster, nw, nch, threads, n;
+        Plateau p[7];
     };
     static const Candidate cand[] = {
-        {8, 1, 1, 128, {0.345f, 0.402f, 0.427f, 0.490f, 0.533f}},
-        {8, 1, 1, 64, {0.370f, 0.394f, 0.410f, 0.458f, 0.474f}},
-        {8, 2, 1, 128, {0.432f, 0.490f, 0.532f, 0.600f, 0.641f}},
-        {4, 1, 1, 0, {0.411f, 0.411f, 0.444f, 0.515f, 0.519f}},
-        {4, 2, 2, 0, {0.749f, 0.787f, 0.790f, 0.797f, 0.798f}},
-        {8, 4, 1, 128, {0.533f, 0.690f, 0.794f, 0.900f, 1.062f}},
-        {4, 4, 2, 0, {1.160f, 1.270f, 1.270f, 1.275f, 1.277f}},
-        {4, 8, 2, 0, {1.785f, 2.180f, 2.180f, 2.185f, 2.190f}}};
+        // narrow clusters of 8, 128 threads, one window per cluster
+        {8, 1, 1, 128, 6, {{4, .344f}, {7, .356f}, {11, .403f}, {18, .417f}, {25, .462f},
+                           {37, .535f}}},
+        // narrow clusters of 8, 64 threads, two units per lane group
+        {8, 1, 1, 64, 5, {{4, .365f}, {18, .389f}, {26, .445f}, {37, .469f}, {72, .934f}}},
+        // narrow clusters of 8, 128 threads, 2 windows per group
+        {8, 2, 1, 128, 4, {{1, .431f}, {7, .462f}, {18, .546f}, {25, .647f}}},
+        // clusters of 4, 128 threads, two units per group, 4 windows per lane
+        {4, 4, 1, 128, 7, {{9, .716f}, {18, .748f}, {33, 1.095f}, {37, 1.179f}, {55, 1.702f},
+                           {73, 2.107f}, {74, 2.29f}}},
+        // narrow clusters of 8, 128 threads, 4 windows per group
+        {8, 4, 1, 128, 5, {{4, .626f}, {7, .682f}, {11, .754f}, {18, .81f}, {25, 1.062f}}},
+        // clusters of 4, 128 threads, two units per group, 2 chunks of 4 windows
+        {4, 4, 2, 128, 3, {{18, 1.215f}, {33, 1.995f}, {37, 2.36f}}}};
     constexpr int N = sizeof(cand) / sizeof(cand[0]);
     static std::mutex mu;
     static int fits[64][N];
+    static int sms[64];
     static bool known[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return find_variant(4, 8, 2);
+        return find_variant(4, 4, 1, 128);
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!known[dev]) {
@@ -1330,31 +1657,39 @@ const Variant *choose_variant(int batch)
                     find_variant(cand[i].cluster, cand[i].nw, cand[i].nch, cand[i].threads);
                 fits[dev][i] = (v && max_active_clusters(*v, &n) == LSTM_OK) ? n : 0;
             }
+            if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) !=
+                    cudaSuccess ||
+                sms[dev] <= 0)
+                sms[dev] = 152;
             known[dev] = true;
         }
     }
+    auto scaled = [&](int tiles) {
+        return std::max(1, static_cast<int>(static_cast<long>(tiles) * sms[dev] / 152));
+    };
     const Variant *best = nullptr;
-    float best_cost = 0.0f;
+    double best_cost = 0.0;
     for (int i = 0; i < N; ++i) {
-        const Variant *v = find_variant(cand[i].cluster, cand[i].nw, cand[i].nch, cand[i].threads);
+        const Candidate &c = cand[i];
+        const Variant *v = find_variant(c.cluster, c.nw, c.nch, c.threads);
         if (!v || fits[dev][i] < 2)
             continue;
         const long tiles = (static_cast<long>(batch) + v->tile - 1) / v->tile;
-        const long per_wave = fits[dev][i] / 2;  // clusters per direction at once
-        const long full = tiles / per_wave;
-        const long rest = tiles - full * per_wave;
-        float cost = static_cast<float>(full) * cand[i].us[4];
-        if (rest > 0) {
-            const float x = 4.0f * static_cast<float>(rest) / static_cast<float>(per_wave);
-            const int k = x >= 4.0f ? 3 : static_cast<int>(x);
-            cost += cand[i].us[k] + (x - static_cast<float>(k)) * (cand[i].us[k + 1] - cand[i].us[k]);
-        }
+        const long last = scaled(c.p[c.n - 1].tiles);
+        const long waves = (tiles + last - 1) / last;
+        const long k = tiles - (waves - 1) * last;
+        double cost = static_cast<double>(waves - 1) * c.p[c.n - 1].us;
+        for (int j = 0; j < c.n; ++j)
+            if (k <= scaled(c.p[j].tiles)) {
+                cost += c.p[j].us;
+                break;
+            }
         if (!best || cost < best_cost) {
             best = v;
             best_cost = cost;
         }
     }
-    return best ? best : find_variant(4, 8, 2);
+    return best ? best : find_variant(4, 4, 1, 128);
 }
 
 int launch_variant(const Variant &v, const float *g, const float *rp, const float *bias, float *y,

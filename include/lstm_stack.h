@@ -308,9 +308,10 @@ int lstm_recurrence(const float *g, const float *rp, const float *bias,
  * Variants (cluster, windows_per_chunk, chunks, threads): (16|8, 1|2|4|8, 1,
  * 0), (4, 1|2|4|8, 1, 0), (2, 1, 1, 0), (4, 1, 2|4|8, 0), (4, 2, 2|4|8, 0),
  * (4, 4, 2|4, 0), (4, 8, 2, 0), (8, 2, 4, 0), and the narrow
- * (8, 1|2|4|8, 1, 128), (16, 1|2, 1, 64); and (8, 1, 1, 64), where each
- * 8-lane group holds two units' weights for a K chunk (one window per
- * cluster; the formula above does not apply to it).  Every
+ * (8, 1|2|4|8, 1, 128), (16, 1|2, 1, 64); and the two-unit variants, where
+ * each 8-lane group holds two units' weights for a K chunk, so windows per
+ * cluster = windows_per_chunk * chunks: (8, 1, 1, 64), (8, 4|8, 1|2, 64)
+ * and (4, 4, 1|2, 128), (4, 8, 1, 128).  Every
  * variant computes the same sums in the same order, so all give bitwise
  * identical y (the pages' three recurrence kernels are likewise bitwise
  * identical, lstmproj.rs module docs).  Errors as lstm_recurrence, plus
