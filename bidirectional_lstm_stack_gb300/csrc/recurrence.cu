@@ -1542,6 +1542,325 @@ done:
     ptx::cluster_wait_acquire();
 }
 
+// Tensor-core recurrence for large batches: one cluster of 4 CTAs of 128
+// threads per (direction, tile of 16 windows).  CTA rank r owns units
+// [32 r, 32 r + 32): 128 gate rows, row m = 32 q + u for gate q of unit
+// 32 r + u.  Its R rows, scaled by k_q and split into TF32 hi and lo parts,
+// stay in tensor memory for the whole kernel as the MMAs' A operand
+// (columns 0-127 hi, 128-255 lo).  Each step
+//     z (128 rows x 16 windows, tensor memory) = A_hi.h_hi + A_hi.h_lo + A_lo.h_hi
+// over K = 128: 48 tcgen05.mma kind::tf32 (M = 128, N = 16, K = 8) issued by
+// one thread, with h (16 windows x 128 units, the B operand) in shared memory
+// as TF32 hi and lo planes in the 64-byte-swizzled K-major layout.  Then warp
+// q copies the z of gate q (its 32 tensor-memory lanes) into shared memory,
+// and each thread updates 4 cells (window tid / 8, units 4 (tid % 8) .. + 3)
+// with its prefetched projection values and the bias, stores h to y and,
+// split into hi and lo, into its CTA's slice of the next step's B buffer;
+// one thread then copies that 4 KiB slice into the same place of the three
+// peer CTAs (cp.async.bulk shared::cta -> shared::cluster, credited to their
+// mbarrier).  Padding windows past the batch are computed on zero projection
+// values (each window's column of z depends on its own row of h only) and
+// never stored.  The sums run in another order than the FFMA variants', so
+// results agree with theirs to rounding, not bitwise.
+constexpr int TC_N = 16;                           // windows per tile
+constexpr int TC_C = 4;                            // CTAs per cluster
+constexpr int TC_THREADS = 128;
+constexpr int TC_GD = 4;                           // projection-value ring depth (steps)
+constexpr int TC_KB_BYTES = TC_N * 64;             // one 16-column K-block of one plane
+constexpr int TC_SLICE_BYTES = 2 * 2 * TC_KB_BYTES;  // a CTA's 32 units: 2 planes x 2 K-blocks
+constexpr int TC_B_BYTES = TC_C * TC_SLICE_BYTES;    // one step's h
+constexpr int TC_OFF_Z = 2 * TC_B_BYTES;             // after the two B buffers
+constexpr int TC_Z_BYTES = 4 * TC_N * 32 * 4;        // z of 4 gates x 16 windows x 32 units
+constexpr int TC_OFF_G = TC_OFF_Z + TC_Z_BYTES;
+constexpr int TC_G_BYTES = TC_GD * TC_THREADS * 16 * 4;  // 16 projection values per thread
+constexpr int TC_OFF_BAR = TC_OFF_G + TC_G_BYTES;
+// More than half of an SM's shared memory, so one CTA per SM: each holds all
+// 512 tensor-memory columns, and a second CTA on the SM would wait in its
+// allocation for the first to end.
+constexpr int TC_SMEM = 120 * 1024 + 1024;
+constexpr uint32_t TC_AHI = 0, TC_ALO = 128, TC_D = 256, TC_TMEM_COLS = 512;
+constexpr uint32_t TC_IDESC = ptx::tf32_idesc(128, TC_N);
+static_assert(TC_OFF_BAR + 64 + 1024 <= TC_SMEM, "tensor-core recurrence shared memory");
+
+template <bool FLOOR = false>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+recurrence_tc_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
+                     const float *__restrict__ bias_in, float *__restrict__ y, int batch,
+                     int steps, int dir_in, unsigned *fault, unsigned long long wait_limit_ns,
+                     int withhold)
+{
+    constexpr float K0 = -kLog2e, K2 = -2.0f * kLog2e;  // k_q of the gates, the candidate
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *hfull = reinterpret_cast<uint64_t *>(smem + TC_OFF_BAR);  // [2]: peers' slices
+    uint64_t *mma_bar = hfull + 2;    // this step's MMAs complete
+    uint64_t *drain_bar = hfull + 3;  // every MMA issued complete (teardown)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(hfull + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *zbuf = reinterpret_cast<float *>(smem + TC_OFF_Z);   // [4 gates][16 windows][32 units]
+    float *gring = reinterpret_cast<float *>(smem + TC_OFF_G);  // [GD][128 threads][16]
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cid = static_cast<int>(ptx::cluster_id_x());
+    const int direction = dir_in >= 0 ? dir_in : (cid & 1);
+    const int tile = dir_in >= 0 ? cid : (cid >> 1);
+    const float *__restrict__ rp = rp_in + (dir_in >= 0 ? 0 : direction * kGates * kHidden);
+    const float *__restrict__ bias = bias_in + (dir_in >= 0 ? 0 : direction * kGates);
+    const int tile_w0 = tile * TC_N;
+    // the cells of this thread: window n of the tile, units ub .. ub + 3
+    const int n = tid >> 3, quad = tid & 7;
+    const int ub = 32 * static_cast<int>(rank) + 4 * quad;
+    const bool valid = tile_w0 + n < batch;
+    const uint32_t slice_bytes_in = 3u * TC_SLICE_BYTES;  // per step, from the 3 peers
+
+    if (tid == 0) {
+        ptx::mbar_init(&hfull[0], 1);
+        ptx::mbar_init(&hfull[1], 1);
+        ptx::mbar_init(mma_bar, 1);
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        // arm buffer 1 for h_0 and buffer 0 for h_1
+        if (steps > 1)
+            ptx::mbar_arrive_expect_tx(&hfull[1], slice_bytes_in);
+        if (steps > 2)
+            ptx::mbar_arrive_expect_tx(&hfull[0], slice_bytes_in);
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(tmem_slot, TC_TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    // h_{-1} = 0 in both buffers
+    for (int i = tid; i < 2 * TC_B_BYTES / 16; i += TC_THREADS)
+        reinterpret_cast<float4 *>(smem)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    // R rows into tensor memory: lane 32 q + u holds gate q of unit 32 r + u
+    if constexpr (!FLOOR) {
+        const int q = warp;
+        const float kq = q == 2 ? K2 : K0;
+        const float *src = rp + (4 * (32 * static_cast<int>(rank) + lane) + q) * kHidden;
+#pragma unroll 1
+        for (int cb = 0; cb < kHidden / 32; ++cb) {
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float v = src[32 * cb + i] * kq;
+                const float h = ptx::tf32_rna(v);
+                hi[i] = __float_as_uint(h);
+                lo[i] = __float_as_uint(ptx::tf32_rna(v - h));
+            }
+            ptx::tmem_st_32x32b_x32(tmem + lane_base + TC_AHI + 32 * cb, hi);
+            ptx::tmem_st_32x32b_x32(tmem + lane_base + TC_ALO + 32 * cb, lo);
+        }
+        ptx::tmem_st_wait();
+    }
+    float bias_v[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            bias_v[j][q] = bias[4 * (ub + j) + q] * (q == 2 ? K2 : K0);
+    // G columns of units ub .. ub + 3 (16 consecutive values) of window n
+    const float *gsrc = g + direction * kGates + 4 * ub +
+                        static_cast<long>(tile_w0 + n) * steps * kGateColumns;
+    float *yrow = y + static_cast<long>(tile_w0 + n) * steps * kOutput + direction * kHidden + ub;
+
+    // B buffers: [parity][slice = rank][plane][K-block of 16][16 rows x 64 B];
+    // this thread's 16 bytes of h (units ub .. ub + 3, window n) in plane 0,
+    // the 64-byte swizzle applied (16-byte chunk c of row n sits at
+    // c ^ ((n / 2) % 4) within its 512-byte group of 8 rows)
+    const uint32_t b_base = ptx::smem_u32(smem);
+    const uint32_t chunk_off = rank * TC_SLICE_BYTES + (quad >> 2) * TC_KB_BYTES +
+                               (n >> 3) * 512 + (n & 7) * 64 +
+                               static_cast<uint32_t>(((quad & 3) ^ ((n >> 1) & 3)) * 16);
+
+    ptx::tc_fence_before();
+    // every CTA of the cluster initialised before anyone copies into it
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+    ptx::tc_fence_after();
+    ptx::griddep_launch_dependents();
+
+    auto gissue = [&](int s) {
+        const long t = direction ? steps - 1 - s : s;
+        const bool ok = valid && s < steps;
+        const float *src = ok ? gsrc + t * kGateColumns : g;
+        float *dst = gring + ((s % TC_GD) * TC_THREADS + tid) * 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            ptx::cp_async_16(ptx::smem_u32(dst + 4 * i), ok ? src + 4 * i : g, ok ? 16u : 0u);
+        ptx::cp_async_commit();
+    };
+    for (int s = 0; s < TC_GD; ++s)
+        gissue(s);
+
+    // bounded wait of one thread; on timeout it records the fault and the
+    // abort flag, which every thread reads after the next CTA barrier
+    auto wait_bounded = [&](uint64_t *bar, uint32_t parity, bool cluster_scope) -> bool {
+        auto try_once = [&]() {
+            return cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity)
+                                 : ptx::mbar_try_wait(bar, parity);
+        };
+        if (try_once())
+            return true;
+        const uint64_t start = ptx::globaltimer();
+        while (!try_once()) {
+            if (*abort_flag)
+                return false;
+            if (ptx::globaltimer() - start > wait_limit_ns) {
+                atomicOr(fault, kFaultRecurrence);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+        return true;
+    };
+
+    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (!(withhold && rank == 0)) {
+        for (int s = 0; s < steps; ++s) {
+            const int par = s & 1;
+            const int t = direction ? steps - 1 - s : s;
+            // 1. the peers' slices of h_{s-1} in buffer `par` (this CTA's own
+            //    slice was written before the last CTA barrier); then the MMAs
+            if (tid == 0) {
+                bool ok = true;
+                if (s > 0) {
+                    ok = wait_bounded(&hfull[par], ((s - 1) >> 1) & 1, true);
+                    if (ok && s + 2 < steps)
+                        ptx::mbar_arrive_expect_tx(&hfull[par], slice_bytes_in);
+                }
+                if (ok) {
+                    ptx::tc_fence_after();
+                    if constexpr (!FLOOR) {
+                        const uint32_t bb = b_base + static_cast<uint32_t>(par * TC_B_BYTES);
+#pragma unroll
+                        for (int k8 = 0; k8 < kHidden / 8; ++k8) {
+                            const int kb = k8 >> 1;
+                            const uint32_t bhi = bb + static_cast<uint32_t>(
+                                                          (kb >> 1) * TC_SLICE_BYTES +
+                                                          (kb & 1) * TC_KB_BYTES + (k8 & 1) * 32);
+                            const uint32_t blo = bhi + 2 * TC_KB_BYTES;
+                            ptx::mma_tf32_tmem_a(tmem + TC_D, tmem + TC_AHI + 8 * k8,
+                                                 ptx::sw64_desc(bhi), TC_IDESC, k8 != 0);
+                            ptx::mma_tf32_tmem_a(tmem + TC_D, tmem + TC_AHI + 8 * k8,
+                                                 ptx::sw64_desc(blo), TC_IDESC, 1);
+                            ptx::mma_tf32_tmem_a(tmem + TC_D, tmem + TC_ALO + 8 * k8,
+                                                 ptx::sw64_desc(bhi), TC_IDESC, 1);
+                        }
+                    }
+                    ptx::mma_commit(mma_bar);
+                }
+            }
+            __syncthreads();
+            if (*abort_flag)
+                break;
+            // 2. z into shared memory: warp q holds gate q of the 32 units
+            //    (the tensor-memory load is warp-collective: the whole warp
+            //    takes it only if every lane's wait succeeded)
+            if (__all_sync(0xffffffffu, wait_bounded(mma_bar, static_cast<uint32_t>(s & 1), false))) {
+                ptx::tc_fence_after();
+                if constexpr (!FLOOR) {
+                    uint32_t r[16];
+                    ptx::tmem_ld_32x32b_x16(tmem + lane_base + TC_D, r);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < TC_N; ++j)
+                        zbuf[(warp * TC_N + j) * 32 + lane] = __uint_as_float(r[j]);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncthreads();
+            if (*abort_flag)
+                break;
+            // 3. the cells of units ub .. ub + 3, window n
+            ptx::cp_async_wait<TC_GD - 1>();
+            const float4 *gv =
+                reinterpret_cast<const float4 *>(gring + ((s % TC_GD) * TC_THREADS + tid) * 16);
+            float h[4];
+            if constexpr (FLOOR) {
+                // the new h depends on one received value and on G only
+                const float hv = *reinterpret_cast<const float *>(
+                    smem + par * TC_B_BYTES + ((rank + 1) & 3) * TC_SLICE_BYTES +
+                    (chunk_off - rank * TC_SLICE_BYTES));
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    h[j] = fmaf(hv, 0.5f, gv[j].x * 0.001f);
+            } else {
+                float4 zq[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    zq[q] = *reinterpret_cast<const float4 *>(&zbuf[(q * TC_N + n) * 32 + 4 * quad]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 gj = gv[j];  // unit ub + j, gates 0..3
+                    const float zj[4] = {(&zq[0].x)[j], (&zq[1].x)[j], (&zq[2].x)[j],
+                                         (&zq[3].x)[j]};
+                    const float gg[4] = {gj.x, gj.y, gj.z, gj.w};
+                    float a[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float w = zj[q] + fmaf(gg[q], q == 2 ? K2 : K0, bias_v[j][q]);
+                        a[q] = q == 2 ? fmaf(2.0f, inv_one_plus_ex2(w), -1.0f)
+                                      : inv_one_plus_ex2(w);
+                    }
+                    c[j] = a[1] * c[j] + a[0] * a[2];
+                    const float r = inv_one_plus_ex2(c[j] * (-2.0f * kLog2e));
+                    h[j] = fmaf(2.0f * a[3], r, -a[3]);
+                }
+            }
+            if (valid)
+                *reinterpret_cast<float4 *>(yrow + static_cast<long>(t) * kOutput) =
+                    make_float4(h[0], h[1], h[2], h[3]);
+            // 4. h_s (hi, lo) into this CTA's slice of buffer par ^ 1; the
+            //    slice to the peers once every thread has written it
+            const bool push = s + 1 < steps;
+            if (push) {
+                float4 hi, lo;
+                ptx::split4(make_float4(h[0], h[1], h[2], h[3]), hi, lo);
+                uint8_t *dst = smem + (par ^ 1) * TC_B_BYTES + chunk_off;
+                *reinterpret_cast<float4 *>(dst) = hi;
+                *reinterpret_cast<float4 *>(dst + 2 * TC_KB_BYTES) = lo;
+                ptx::fence_proxy_async_smem();
+            }
+            __syncthreads();
+            if (push && tid < TC_C - 1) {
+                // thread i copies the slice to the i-th other CTA
+                const uint32_t peer = (rank + 1 + static_cast<uint32_t>(tid)) & (TC_C - 1);
+                const uint32_t off = static_cast<uint32_t>((par ^ 1) * TC_B_BYTES) +
+                                     rank * TC_SLICE_BYTES;
+                ptx::bulk_copy_to_peer(ptx::map_to_rank(b_base + off, peer), b_base + off,
+                                       TC_SLICE_BYTES,
+                                       ptx::map_to_rank(ptx::smem_u32(&hfull[par ^ 1]), peer));
+            }
+            gissue(s + TC_GD);
+        }
+    }
+    ptx::cp_async_wait_all();
+    // every MMA issued has completed before tensor memory is freed
+    if (tid == 0) {
+        ptx::mma_commit(drain_bar);
+        ptx::mbar_wait_drain(drain_bar, 0, fault, kDefaultWaitLimitNs);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    // no CTA leaves while a peer may still copy into its shared memory
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TC_TMEM_COLS);
+    }
+}
+
 struct Variant {
     int cluster;
     int nw;       // windows per chunk
@@ -1550,6 +1869,7 @@ struct Variant {
     int threads;  // per CTA
     const void *fn;
     const void *floor_fn;  // the same variant in FLOOR mode
+    int smem = 0;          // dynamic shared memory per CTA
 };
 
 template <int C, int NW, int NCH = 1, int THREADS = threads_for<C>()>
@@ -1589,6 +1909,10 @@ const Variant kVariants[] = {
     variant_u2w<8, 4, 1>(), variant_u2w<8, 4, 2>(), variant_u2w<4, 4, 1>(),
     variant_u2w<4, 4, 2>(), variant_u2w<8, 8, 1>(), variant_u2w<4, 8, 1>(),
     variant_u2w<8, 8, 2>(),
+    // tensor cores: clusters of 4 CTAs of 128 threads, 16 windows per cluster
+    Variant{4, 16, 1, TC_N, TC_THREADS,
+            reinterpret_cast<const void *>(&recurrence_tc_kernel<false>),
+            reinterpret_cast<const void *>(&recurrence_tc_kernel<true>), TC_SMEM},
 };
 
 // threads == 0: the variant's default block size
@@ -1703,7 +2027,7 @@ int launch_variant(const Variant &v, const float *g, const float *rp, const floa
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(static_cast<unsigned>(v.threads));
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = static_cast<size_t>(v.smem);
     cfg.stream = stream;
     // Launched after the kernel before it has ended (no programmatic
     // dependent launch): started early, the clusters were placed on the SMs
@@ -1735,6 +2059,16 @@ int launch_variant(const Variant &v, const float *g, const float *rp, const floa
 int recurrence_prepare(int)
 {
     for (const Variant &v : kVariants) {
+        if (v.smem > 48 * 1024) {
+            for (const void *fn : {v.fn, v.floor_fn}) {
+                int st = cuda_status(cudaFuncSetAttribute(fn,
+                                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                          v.smem),
+                                     "recurrence shared-memory attribute");
+                if (st != LSTM_OK)
+                    return st;
+            }
+        }
         if (v.cluster > 8) {
             for (const void *fn : {v.fn, v.floor_fn}) {
                 int st = cuda_status(
@@ -1847,6 +2181,7 @@ int max_active_clusters(const Variant &vr, int *out)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(v->cluster));
     cfg.blockDim = dim3(static_cast<unsigned>(v->threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(v->smem);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(v->cluster);

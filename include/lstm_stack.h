@@ -311,11 +311,16 @@ int lstm_recurrence(const float *g, const float *rp, const float *bias,
  * (8, 1|2|4|8, 1, 128), (16, 1|2, 1, 64); and the two-unit variants, where
  * each 8-lane group holds two units' weights for a K chunk, so windows per
  * cluster = windows_per_chunk * chunks: (8, 1, 1, 64), (8, 4|8, 1|2, 64)
- * and (4, 4, 1|2, 128), (4, 8, 1, 128).  Every
- * variant computes the same sums in the same order, so all give bitwise
+ * and (4, 4, 1|2, 128), (4, 8, 1, 128).  Every one of these
+ * variants computes the same sums in the same order, so all give bitwise
  * identical y (the pages' three recurrence kernels are likewise bitwise
- * identical, lstmproj.rs module docs).  Errors as lstm_recurrence, plus
- * LSTM_E_INVALID for an unknown variant. */
+ * identical, lstmproj.rs module docs).  The variant (4, 16, 1, 128) runs the
+ * matrix-vector products on the tensor cores instead (tcgen05.mma kind::tf32
+ * in three TF32 products, R resident in tensor memory, 16 windows per
+ * cluster of 4 CTAs): other summation order, so it matches the others to
+ * rounding rather than bitwise; slower than the FFMA variants at every batch
+ * on GB300, so never chosen by lstm_recurrence.  Errors as lstm_recurrence,
+ * plus LSTM_E_INVALID for an unknown variant. */
 int lstm_recurrence_variant(const float *g, const float *rp, const float *bias,
                             float *y, int batch, int steps, int direction,
                             int cluster_size, int windows_per_chunk, int chunks,

@@ -112,6 +112,37 @@ def test_recurrence_wait_timeout_sets_fault_and_recovers(layers):
     assert_within(y.cpu().numpy()[..., :128], ref[..., :128], what="recurrence after timeout")
 
 
+def test_tensor_core_recurrence_wait_timeout_sets_fault_and_recovers(layers):
+    # CTA 0 of every cluster withholds its h slices; the peers' bounded waits
+    # run out, the kernel frees its tensor memory and ends, and the next
+    # launch is correct
+    import torch
+    lib = binding.load()
+    rng = np.random.default_rng(10)
+    _, _, rp, bias = binding.lstm_pack_layer(layers[1]["w"], layers[1]["r"], layers[1]["b"],
+                                             256, 256)
+    batch, steps = 20, 24
+    g = cuda(rng.standard_normal((batch * steps, 1024)).astype(np.float32))
+    y = torch.zeros((batch, steps, 256), device="cuda")
+    rpt, bt = cuda(rp), cuda(bias)
+    assert binding.lstm_fault_status() == 0
+    lib.lstm_test_recurrence_timeout(1, 20000, 0)
+    try:
+        binding.lstm_recurrence_variant(g, rpt, bt, y, batch, steps,
+                                        binding.LSTM_BOTH_DIRECTIONS, 4, 16, 1, 128)
+        torch.cuda.synchronize()
+        assert binding.lstm_fault_status() == FAULT_RECURRENCE
+    finally:
+        lib.lstm_test_recurrence_timeout(0, 0, 0)
+    binding.lstm_recurrence_variant(g, rpt, bt, y, batch, steps, binding.LSTM_BOTH_DIRECTIONS,
+                                    4, 16, 1, 128)
+    torch.cuda.synchronize()
+    assert binding.lstm_fault_status() == 0
+    ref = oracle.recurrence(g.cpu().numpy().astype(np.float64), layers[1]["r"], layers[1]["b"],
+                            batch, steps)
+    assert_within(y.cpu().numpy(), ref, what="tensor-core recurrence after timeout")
+
+
 def test_forward_host_reports_a_timed_out_wait(layers):
     lib = binding.load()
     x = synthetic.stack_input(synthetic.WORKLOADS["b1_t64"])

@@ -102,6 +102,38 @@ def test_partly_and_wholly_empty_chunks(variant, batch):
     assert binding.lstm_fault_status() == 0
 
 
+# tensor cores (tcgen05, 3xTF32, A in tensor memory): clusters of 4 CTAs of
+# 128 threads, 16 windows per cluster; another summation order than the FFMA
+# variants, so compared with the oracle only
+TC_VARIANT = (4, 16, 1, 128)
+
+
+@pytest.mark.parametrize("batch,steps", [(1, 1), (1, 2), (3, 5), (16, 7), (17, 33), (40, 64),
+                                         (33, 3)])
+def test_tensor_core_variant_matches_oracle(batch, steps):
+    import torch
+    lay, G, rp, bias = _layer_inputs(batch, steps, seed=26)
+    ref = oracle.recurrence(G.astype(np.float64), lay["r"], lay["b"], batch, steps)
+    apart = _run(G, rp, bias, batch, steps, TC_VARIANT)
+    assert_within(apart, ref, what=f"tensor cores b{batch} t{steps}, directions apart")
+    y = torch.full((batch, steps, 256), float("nan"), device="cuda")
+    binding.lstm_recurrence_variant(cuda(G), cuda(rp), cuda(bias), y, batch, steps,
+                                    binding.LSTM_BOTH_DIRECTIONS, *TC_VARIANT)
+    torch.cuda.synchronize()
+    assert_within(y.cpu().numpy(), ref, what=f"tensor cores b{batch} t{steps}, one launch")
+    assert binding.lstm_fault_status() == 0
+
+
+def test_tensor_core_variant_large_inputs():
+    # inputs 30x larger: saturated gates, the TF32 lo parts carrying the
+    # products' low bits
+    batch, steps = 21, 19
+    lay, G, rp, bias = _layer_inputs(batch, steps, seed=27, scale=30.0)
+    y = _run(G, rp, bias, batch, steps, TC_VARIANT)
+    ref = oracle.recurrence(G.astype(np.float64), lay["r"], lay["b"], batch, steps)
+    assert_within(y, ref, what="tensor cores, large inputs")
+
+
 def test_variants_are_bitwise_identical():
     batch, steps = 37, 41
     _, G, rp, bias = _layer_inputs(batch, steps, seed=23)
@@ -155,7 +187,7 @@ def test_chosen_variants_run_in_one_wave(variant, batch):
 
 
 def test_max_clusters_query():
-    for v in VARIANTS:
+    for v in VARIANTS + [TC_VARIANT]:
         n = binding.lstm_recurrence_max_clusters(*v)
         assert n >= 1, (v, n)
     with pytest.raises(binding.LSTMError):
