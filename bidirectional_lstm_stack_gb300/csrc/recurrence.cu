@@ -87,6 +87,14 @@ __device__ __forceinline__ float inv_one_plus_ex2(float w)
     return __fdividef(1.0f, 1.0f + ex2_approx(w));
 }
 
+// The cell update c' = f c + i g, with one fixed rounding order (the product
+// i g rounded, then one fused multiply-add), so every kernel computes the
+// same bits whatever the compiler would contract.
+__device__ __forceinline__ float cell_update(float i, float f, float g, float c)
+{
+    return fmaf(f, c, __fmul_rn(i, g));
+}
+
 // One butterfly level: lanes that differ in `mask` exchange half of their
 // N values; each keeps the sums for the half its mask bit selects.
 // PERM: the lane whose mask bit is set holds its values in an order with the
@@ -473,7 +481,7 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
             const int src = V >= 8 ? (4 * wl + q) / HV : 2 * q;
             gate[q] = __shfl_sync(0xffffffffu, act[q % HV], src, 8);
         }
-        c[ch] = gate[1] * c[ch] + gate[0] * gate[2];
+        c[ch] = cell_update(gate[0], gate[1], gate[2], c[ch]);
         // h = o tanh(c) = o (2 r - 1) with r = 1 / (1 + 2^(-2 log2(e) c)):
         // one fused multiply-add after r
         const float r = inv_one_plus_ex2(c[ch] * (-2.0f * kLog2e));
@@ -652,7 +660,7 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
                     const int src = V >= 8 ? (4 * wl + q) / HV : 2 * q;
                     gate[q] = __shfl_sync(0xffffffffu, act[q % HV], src, 8);
                 }
-                c[ch] = gate[1] * c[ch] + gate[0] * gate[2];
+                c[ch] = cell_update(gate[0], gate[1], gate[2], c[ch]);
                 // h = o tanh(c) = o (2 r - 1) with r = 1 / (1 + 2^(-2 log2(e) c)):
                 // one fused multiply-add after r
                 const float r = inv_one_plus_ex2(c[ch] * (-2.0f * kLog2e));
@@ -1009,7 +1017,7 @@ recurrence_fused_kernel(const float *__restrict__ x, int in_width,
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 gate[q] = __shfl_sync(0xffffffffu, act, 2 * q, 8);
-            c = gate[1] * c + gate[0] * gate[2];
+            c = cell_update(gate[0], gate[1], gate[2], c);
             const float r = inv_one_plus_ex2(c * (-2.0f * kLog2e));
             const float h = fmaf(2.0f * gate[3], r, -gate[3]);
             float h4[4];
@@ -1205,7 +1213,7 @@ recurrence_u2_kernel(const float *__restrict__ g, const float *__restrict__ rp_i
 #pragma unroll
             for (int gq = 0; gq < 4; ++gq)
                 gate[gq] = __shfl_sync(0xffffffffu, act, 4 * jj + gq, 8);
-            c = gate[1] * c + gate[0] * gate[2];
+            c = cell_update(gate[0], gate[1], gate[2], c);
             const float r = inv_one_plus_ex2(c * (-2.0f * kLog2e));
             h = fmaf(2.0f * gate[3], r, -gate[3]);
         }
@@ -1265,11 +1273,14 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
     constexpr int TW = NW * NCH;      // windows per cluster
     constexpr int V = 8 * NW;         // partial sums per lane and chunk
     constexpr int HV = V / 8;         // values a lane holds after the reduction
-    constexpr int CELLS = HV / 4;     // cells a lane updates per chunk
+    // cells a lane updates per chunk; with two windows a lane holds two of
+    // a cell's four gates and completes the cell with its partner lane kc ^ 1
+    constexpr int CELLS = HV >= 4 ? HV / 4 : 1;
     constexpr int NPEER = C / 4;      // peers each holder of an h quad sends to
     constexpr bool CM = NCH > 1;
     constexpr int NBAR = CM ? NCH : 1;
-    static_assert((C == 4 || C == 8) && (NW == 4 || NW == 8) && (NCH == 1 || NCH == 2),
+    static_assert((C == 4 || C == 8) && (NW == 2 || NW == 4 || NW == 8) &&
+                      (NCH == 1 || NCH == 2),
                   "shape");
     // projection values: a ring of GD steps in shared memory, each lane's
     // four gate values of a cell one 16-byte asynchronous copy
@@ -1295,18 +1306,21 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
     const int base = static_cast<int>(rank) * UPC + (tid >> 5) * 8;  // the warp's 8 units
     const int tile_w0 = tile * TW;
     volatile int *abort_v = &abort_flag;
-    // window and unit parts of the lane order L -> L ^ (HV k) of K chunk k
+    // window, unit and gate parts of the lane order L -> L ^ (HV k) of K chunk k
     auto xw = [](int k) { return (HV * k) >> 3; };
     auto xj = [](int k) { return ((HV * k) >> 2) & 1; };
+    auto xq = [](int k) { return (HV * k) & 3; };
 
-    // R slices: slot (js, q) holds gate q of unit index js ^ xj(kc), scaled by k_q
+    // R slices: slot (js, q) holds gate q ^ xq(kc) of unit index js ^ xj(kc),
+    // scaled by k_q
     float2 r2[2][4][KLEN / 2];
 #pragma unroll
     for (int js = 0; js < 2; ++js)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int row = 4 * (base + 4 * (js ^ xj(kc)) + grp) + q;
-            const float kq = q == 2 ? K2 : K0;
+            const int ql = q ^ xq(kc);
+            const int row = 4 * (base + 4 * (js ^ xj(kc)) + grp) + ql;
+            const float kq = ql == 2 ? K2 : K0;
             const float2 *src = reinterpret_cast<const float2 *>(rp + row * kHidden + kc * KLEN);
 #pragma unroll
             for (int i = 0; i < KLEN / 2; ++i)
@@ -1482,6 +1496,26 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
                 reduce_level<V, true>(part, a, 4, (kc & 4) != 0);
                 reduce_level<V / 2, true>(a, b2, 2, (kc & 2) != 0);
                 reduce_level<V / 4, true>(b2, held, 1, (kc & 1) != 0);
+                if constexpr (NW == 2) {
+                    // held[i]: gate 2 qh + i of this lane's cell (qh = kc & 1);
+                    // lane kc ^ 1 holds the other two: swap the activated pair
+                    const float4 gv = gring[s & (GD - 1)][ch][tid];
+                    const bool qh = (kc & 1) != 0;
+                    const float w0 = held[0] + fmaf(qh ? gv.z : gv.x, qh ? K2 : K0,
+                                                    qh ? bias_v[0][2] : bias_v[0][0]);
+                    const float w1 = held[1] + fmaf(qh ? gv.w : gv.y, K0,
+                                                    qh ? bias_v[0][3] : bias_v[0][1]);
+                    const float a0 =
+                        fmaf(qh ? 2.0f : 1.0f, inv_one_plus_ex2(w0), qh ? -1.0f : 0.0f);
+                    const float a1 = inv_one_plus_ex2(w1);
+                    const float o0 = __shfl_xor_sync(0xffffffffu, a0, 1);
+                    const float o1 = __shfl_xor_sync(0xffffffffu, a1, 1);
+                    const float gi = qh ? o0 : a0, gf = qh ? o1 : a1;
+                    const float gg = qh ? a0 : o0, go = qh ? a1 : o1;
+                    c[ch][0] = cell_update(gi, gf, gg, c[ch][0]);
+                    const float r = inv_one_plus_ex2(c[ch][0] * (-2.0f * kLog2e));
+                    h[0] = fmaf(2.0f * go, r, -go);
+                } else {
 #pragma unroll
                 for (int ci = 0; ci < CELLS; ++ci) {
                     const float4 gv = gring[s & (GD - 1)][ch * CELLS + ci][tid];
@@ -1494,9 +1528,10 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
                         act[q] = q == 2 ? fmaf(2.0f, inv_one_plus_ex2(w), -1.0f)
                                         : fmaf(1.0f, inv_one_plus_ex2(w), 0.0f);
                     }
-                    c[ch][ci] = act[1] * c[ch][ci] + act[0] * act[2];
+                    c[ch][ci] = cell_update(act[0], act[1], act[2], c[ch][ci]);
                     const float r = inv_one_plus_ex2(c[ch][ci] * (-2.0f * kLog2e));
                     h[ci] = fmaf(2.0f * act[3], r, -act[3]);
+                }
                 }
             }
             // gather the group's four units of each cell's window, push the
@@ -1507,7 +1542,9 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     h4[k] = __shfl_sync(0xffffffffu, h[ci], 8 * k + kc);
-                if (valid(ch, ci)) {
+                // with two windows the pair kc, kc ^ 1 holds the same cell:
+                // the even lane sends and stores it
+                if (valid(ch, ci) && (NW != 2 || (kc & 1) == 0)) {
                     if (push) {
                         const uint32_t off = static_cast<uint32_t>(ch * NW * HROW * 4);
                         const uint32_t bar_off = static_cast<uint32_t>(CM ? ch * 8 : 0);
@@ -1812,7 +1849,7 @@ recurrence_tc_kernel(const float *__restrict__ g, const float *__restrict__ rp_i
                         a[q] = q == 2 ? fmaf(2.0f, inv_one_plus_ex2(w), -1.0f)
                                       : inv_one_plus_ex2(w);
                     }
-                    c[j] = a[1] * c[j] + a[0] * a[2];
+                    c[j] = cell_update(a[0], a[1], a[2], c[j]);
                     const float r = inv_one_plus_ex2(c[j] * (-2.0f * kLog2e));
                     h[j] = fmaf(2.0f * a[3], r, -a[3]);
                 }
@@ -1908,7 +1945,8 @@ const Variant kVariants[] = {
     // two units per 8-lane group, several windows per lane
     variant_u2w<8, 4, 1>(), variant_u2w<8, 4, 2>(), variant_u2w<4, 4, 1>(),
     variant_u2w<4, 4, 2>(), variant_u2w<8, 8, 1>(), variant_u2w<4, 8, 1>(),
-    variant_u2w<8, 8, 2>(),
+    variant_u2w<8, 8, 2>(),     variant_u2w<8, 2, 1>(), variant_u2w<8, 2, 2>(),
+    variant_u2w<4, 2, 1>(),     variant_u2w<4, 2, 2>(),
     // tensor cores: clusters of 4 CTAs of 128 threads, 16 windows per cluster
     Variant{4, 16, 1, TC_N, TC_THREADS,
             reinterpret_cast<const void *>(&recurrence_tc_kernel<false>),
@@ -1937,7 +1975,10 @@ int max_active_clusters(const Variant &v, int *out);
 // second wave where a candidate stays competitive there; a batch past the
 // last plateau runs as repeated waves of it.  On another SM count the tile
 // counts scale with it.  Chosen this way, the step is within 1.5 % of the
-// fastest candidate's at every batch from 1 to 320 windows (measured).
+// fastest candidate's at every batch from 1 to 320 windows (measured: 1-7
+// windows one unit per group, 8-37 two units, 38-74 two units and two
+// windows per lane, 75-100 4 windows per group, then two units and 4 windows
+// per lane, in two chunks from 221 to 264).
 // Ties go to the earlier candidate.
 const Variant *choose_variant(int batch)
 {
@@ -1955,8 +1996,8 @@ const Variant *choose_variant(int batch)
                            {37, .535f}}},
         // narrow clusters of 8, 64 threads, two units per lane group
         {8, 1, 1, 64, 5, {{4, .365f}, {18, .389f}, {26, .445f}, {37, .469f}, {72, .934f}}},
-        // narrow clusters of 8, 128 threads, 2 windows per group
-        {8, 2, 1, 128, 4, {{1, .431f}, {7, .462f}, {18, .546f}, {25, .647f}}},
+        // clusters of 4, 128 threads, two units per group, 2 windows per lane
+        {4, 2, 1, 128, 5, {{18, .522f}, {37, .654f}, {64, 1.253f}, {74, 1.30f}, {88, 1.87f}}},
         // clusters of 4, 128 threads, two units per group, 4 windows per lane
         {4, 4, 1, 128, 7, {{9, .716f}, {18, .748f}, {33, 1.095f}, {37, 1.179f}, {55, 1.702f},
                            {73, 2.107f}, {74, 2.29f}}},
