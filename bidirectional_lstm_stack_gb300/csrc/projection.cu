@@ -350,8 +350,11 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
             // tile's mainloop has issued c/NSLICE of its K blocks, so G
             // streams to memory under the next tile's compute instead of
             // every CTA writing its whole tile at once and stalling the loads.
+            // With a resident W tile the ring carries only X and a tile has
+            // 4 K blocks, so the stores go out unpaced (measured: 3.5 % faster
+            // at 150 784 rows, no change at fewer).
             constexpr int NSLICE = BN / OUT_COLS;
-            const bool paced = t + stride < tiles;
+            const bool paced = !S::RESIDENT_W && t + stride < tiles;
             const long next_kb = static_cast<long>(ti + 1) * kblocks;
 #pragma unroll 1
             for (int c = 0; c < NSLICE; ++c, ++slices) {
