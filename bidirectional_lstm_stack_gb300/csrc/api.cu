@@ -611,16 +611,21 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
         }
         if ((st = mark(l, 0, 0)))
             return st;
+        int proj_ctas = 0;
         st = launch_projection(src, s->map_w[l], s->gates, static_cast<int>(rows), s->kp[l],
-                               s->math, s->fault, stream);
+                               s->math, s->fault, stream, &proj_ctas);
         if (st != LSTM_OK)
             return st;
         if ((st = mark(l, 0, 1)) || (st = mark(l, 1, 0)) || (st = mark(l, 2, 0)))
             return st;
         // forward and reverse in one grid on the caller's stream: the next
-        // layer's projection follows it on the same stream
+        // layer's projection follows it on the same stream; with few windows
+        // (both grids fit on the SMs side by side) it starts while the
+        // projection runs (phase timing puts an event between them, so
+        // there it starts after)
         if ((st = launch_recurrence(s->gates, s->rp[l], s->bias[l], dst, batch, steps,
-                                    kBothDirections, s->fault, stream)))
+                                    kBothDirections, s->fault, stream,
+                                    s->timing ? -1 : proj_ctas)))
             return st;
         if ((st = mark(l, 1, 1)) || (st = mark(l, 2, 1)))
             return st;

@@ -110,8 +110,9 @@ int encode_projection_w(ProjectionW *w, const float *wp_hi, const float *wp_lo, 
 // G[rows][1024] = X . Wp^T in 3xTF32 (math LSTM_MATH_3XTF32) or with single
 // TF32 products (LSTM_MATH_TF32, the lo plane unused); x_map from
 // encode_matrix_map (G's own store map is encoded per launch).
+// grid_out (optional): the CTAs launched (the persistent grid).
 int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, int rows, int kp,
-                      int math, unsigned *fault, cudaStream_t stream);
+                      int math, unsigned *fault, cudaStream_t stream, int *grid_out = nullptr);
 int projection_prepare(int device);
 // Store map of a row-major fp32 matrix [rows][cols] written in 32 x 32
 // slices with the 128-byte swizzle (the projection's G).
@@ -126,9 +127,14 @@ constexpr int kHeadWBoxRows = 128;
 // both, rp [2][512][128] and bias [2][512], forward and reverse clusters
 // alternating in the grid.
 constexpr int kBothDirections = -1;
+// co_resident_ctas >= 0: the kernel before it on the stream runs that many
+// CTAs (the projection, one per SM); when both grids fit on the SMs side by
+// side the recurrence is launched as its programmatic dependent, so its
+// set-up (R into registers, barriers, the cluster barrier) overlaps that
+// kernel, and it waits (griddepcontrol.wait) before it reads G.
 int launch_recurrence(const float *g, const float *rp, const float *bias,
                       float *y, int batch, int steps, int direction,
-                      unsigned *fault, cudaStream_t stream);
+                      unsigned *fault, cudaStream_t stream, int co_resident_ctas = -1);
 int launch_recurrence_variant(const float *g, const float *rp, const float *bias,
                               float *y, int batch, int steps, int direction,
                               int cluster, int nw, int nch, int threads, unsigned *fault,

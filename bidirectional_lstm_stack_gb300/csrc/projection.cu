@@ -182,6 +182,9 @@ projection_kernel(const __grid_constant__ CUtensorMap x_map,
     // the kernel before this one; X (that kernel's output) and G (which it
     // may still read) are touched only after it has completed.
     ptx::griddep_wait();
+    // ... and the recurrence after this one may be scheduled now (on the SMs
+    // this grid leaves free); it waits for this grid's end before it reads G
+    ptx::griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     const int first = static_cast<int>(blockIdx.x);
     const int stride = static_cast<int>(gridDim.x);
@@ -490,7 +493,7 @@ const void *const kKernels[] = {
 template <class S>
 int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
                  const CUtensorMap &wlo_map, const CUtensorMap &out_map, int rows, int kp,
-                 unsigned *fault, cudaStream_t stream)
+                 unsigned *fault, cudaStream_t stream, int *grid_out)
 {
     if (rows <= 0 || kp <= 0 || kp % 32 != 0)
         return fail(LSTM_E_INVALID, "tensor-core GEMM: rows %d, kp %d", rows, kp);
@@ -510,6 +513,8 @@ int launch_tiles(const CUtensorMap &x_map, const CUtensorMap &whi_map,
         fit -= fit % S::TILES_N;
     }
     const long grid = tiles < fit ? tiles : fit;
+    if (grid_out)
+        *grid_out = static_cast<int>(grid);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(THREADS);
@@ -574,7 +579,7 @@ int encode_projection_w(ProjectionW *w, const float *wp_hi, const float *wp_lo, 
 }
 
 int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, int rows, int kp,
-                      int math, unsigned *fault, cudaStream_t stream)
+                      int math, unsigned *fault, cudaStream_t stream, int *grid_out)
 {
     if (math != LSTM_MATH_3XTF32 && math != LSTM_MATH_TF32)
         return fail(LSTM_E_INVALID, "projection: unknown math mode %d", math);
@@ -589,9 +594,9 @@ int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, 
     const bool resident = kp <= RESIDENT_KBLOCKS * BK;
     if (math == LSTM_MATH_TF32)
         return resident ? launch_tiles<GatesTf32ResidentShape>(x_map, w.hi, w.lo, g_map, rows, kp,
-                                                                fault, stream)
+                                                                fault, stream, grid_out)
                         : launch_tiles<GatesTf32Shape>(x_map, w.hi, w.lo, g_map, rows, kp, fault,
-                                                       stream);
+                                                       stream, grid_out);
     // When the 256-column tiles would fill at most half of the CTAs that run
     // at once, 128-column tiles give every CTA half the work on twice as many
     // SMs.
@@ -602,12 +607,13 @@ int launch_projection(const CUtensorMap &x_map, const ProjectionW &w, float *g, 
     const long tiles = (static_cast<long>(rows) + BM - 1) / BM * GatesShape::TILES_N;
     if (2 * tiles <= fit)
         return resident ? launch_tiles<GatesNarrowResidentShape>(x_map, w.hi_narrow, w.lo_narrow,
-                                                                 g_map, rows, kp, fault, stream)
+                                                                 g_map, rows, kp, fault, stream, grid_out)
                         : launch_tiles<GatesNarrowShape>(x_map, w.hi_narrow, w.lo_narrow, g_map,
-                                                         rows, kp, fault, stream);
+                                                         rows, kp, fault, stream, grid_out);
     return resident ? launch_tiles<GatesResidentShape>(x_map, w.hi, w.lo, g_map, rows, kp, fault,
-                                                       stream)
-                    : launch_tiles<GatesShape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream);
+                                                       stream, grid_out)
+                    : launch_tiles<GatesShape>(x_map, w.hi, w.lo, g_map, rows, kp, fault, stream,
+                                               grid_out);
 }
 
 } // namespace lstm

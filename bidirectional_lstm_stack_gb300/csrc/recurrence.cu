@@ -389,6 +389,9 @@ recurrence_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
     // programmatic dependent) may be scheduled from here on; it waits for
     // this one to end before it touches G or this layer's output.
     ptx::griddep_launch_dependents();
+    // launched as a programmatic dependent of the kernel that writes its
+    // input: wait for that kernel's end before the first read of it
+    ptx::griddep_wait();
     if constexpr (SRING) {
         for (int s = 0; s < GD; ++s)
             gissue(s);
@@ -876,6 +879,9 @@ recurrence_fused_kernel(const float *__restrict__ x, int in_width,
     ptx::cluster_arrive_release();
     ptx::cluster_wait_acquire();
     ptx::griddep_launch_dependents();
+    // launched as a programmatic dependent of the kernel that writes its
+    // input: wait for that kernel's end before the first read of it
+    ptx::griddep_wait();
 
     const uint32_t row_bytes = static_cast<uint32_t>(in_width) * 4;
     // step s's input row into ring slot `slot`, one bulk copy per K chunk
@@ -1125,6 +1131,9 @@ recurrence_u2_kernel(const float *__restrict__ g, const float *__restrict__ rp_i
     ptx::cluster_arrive_release();
     ptx::cluster_wait_acquire();
     ptx::griddep_launch_dependents();
+    // launched as a programmatic dependent of the kernel that writes its
+    // input: wait for that kernel's end before the first read of it
+    ptx::griddep_wait();
 
     // senders: lane group*4 + kc%4 (< 8) pushes units base + 4 jj .. +3 to
     // that peer; lanes kc = 0 and 4 of group 0 store them to y
@@ -1381,6 +1390,9 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
     ptx::cluster_arrive_release();
     ptx::cluster_wait_acquire();
     ptx::griddep_launch_dependents();
+    // launched as a programmatic dependent of the kernel that writes its
+    // input: wait for that kernel's end before the first read of it
+    ptx::griddep_wait();
 
     // this lane's pushes: the four holders of an h quad (one per group)
     // send to peers grp, grp + 4 (C = 8) or grp (C = 4)
@@ -1725,6 +1737,9 @@ recurrence_tc_kernel(const float *__restrict__ g, const float *__restrict__ rp_i
     ptx::cluster_wait_acquire();
     ptx::tc_fence_after();
     ptx::griddep_launch_dependents();
+    // launched as a programmatic dependent of the kernel that writes its
+    // input: wait for that kernel's end before the first read of it
+    ptx::griddep_wait();
 
     auto gissue = [&](int s) {
         const long t = direction ? steps - 1 - s : s;
@@ -2059,7 +2074,7 @@ const Variant *choose_variant(int batch)
 
 int launch_variant(const Variant &v, const float *g, const float *rp, const float *bias, float *y,
                    int batch, int steps, int direction, unsigned *fault, cudaStream_t stream,
-                   bool floor = false)
+                   bool floor = false, bool pdl = false)
 {
     const long tiles = (static_cast<long>(batch) + v.tile - 1) / v.tile;
     const long blocks = tiles * v.cluster * (direction == kBothDirections ? 2 : 1);
@@ -2070,18 +2085,21 @@ int launch_variant(const Variant &v, const float *g, const float *rp, const floa
     cfg.blockDim = dim3(static_cast<unsigned>(v.threads));
     cfg.dynamicSmemBytes = static_cast<size_t>(v.smem);
     cfg.stream = stream;
-    // Launched after the kernel before it has ended (no programmatic
-    // dependent launch): started early, the clusters were placed on the SMs
-    // that kernel had already left, several to an SM, and the whole layer ran
-    // at the pace of the most crowded SM (b32_t589: 2.23 instead of 1.36 ms
-    // per forward).
-    cudaLaunchAttribute attr[1];
+    // Normally launched after the kernel before it has ended: started early
+    // (programmatic dependent launch) while that kernel covers the GPU, the
+    // clusters were placed on the SMs it had already left, several to an SM,
+    // and the whole layer ran at the pace of the most crowded SM (b32_t589:
+    // 2.23 instead of 1.36 ms per forward).  `pdl` (both grids fit side by
+    // side): started early, so the set-up overlaps that kernel.
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(v.cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     // failure-test settings (kernel parameters: reading them from a device
     // variable at kernel start measured 3-7 % slower per step)
     KernelTest test = kernel_test(kTestRecurrence);
@@ -2124,10 +2142,21 @@ int recurrence_prepare(int)
 }
 
 int launch_recurrence(const float *g, const float *rp, const float *bias, float *y, int batch,
-                      int steps, int direction, unsigned *fault, cudaStream_t stream)
+                      int steps, int direction, unsigned *fault, cudaStream_t stream,
+                      int co_resident_ctas)
 {
-    return launch_variant(*choose_variant(batch), g, rp, bias, y, batch, steps, direction, fault,
-                          stream);
+    const Variant &v = *choose_variant(batch);
+    bool pdl = false;
+    if (co_resident_ctas >= 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+            const long tiles = (static_cast<long>(batch) + v.tile - 1) / v.tile;
+            const long blocks = tiles * v.cluster * (direction == kBothDirections ? 2 : 1);
+            pdl = blocks + co_resident_ctas <= sms;
+        }
+    }
+    return launch_variant(v, g, rp, bias, y, batch, steps, direction, fault, stream, false, pdl);
 }
 
 int launch_recurrence_floor(const float *g, const float *rp, const float *bias, float *y,
