@@ -579,15 +579,21 @@ int forward_device(lstm_stack *s, const float *x, float *y, int batch, int steps
         s->map_x_base = x;
         s->map_x_rows = rows;
     }
-    // phase events are recorded as external events, so they also fire when the
-    // pass is replayed from a captured graph; the recurrence of both
-    // directions is one launch, so its time fills both recurrence slots
+    // phase events: while the pass is being captured they are recorded as
+    // external events, so they also fire when the graph is replayed (the flag
+    // is valid only during capture; launched directly they are plain
+    // records); the recurrence of both directions is one launch, so its time
+    // fills both recurrence slots
     auto ev = [&](int layer, int part, int end) { return s->phase[(layer * 3 + part) * 2 + end]; };
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (s->timing && (st = cuda_status(cudaStreamIsCapturing(stream, &capture), "capture status")))
+        return st;
+    const unsigned record_flags =
+        capture == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
     auto mark = [&](int layer, int part, int end) -> int {
         if (!s->timing)
             return LSTM_OK;
-        return cuda_status(cudaEventRecordWithFlags(ev(layer, part, end), stream,
-                                                    cudaEventRecordExternal),
+        return cuda_status(cudaEventRecordWithFlags(ev(layer, part, end), stream, record_flags),
                            "event");
     };
     const bool fused = fused_batch(s, batch);

@@ -148,6 +148,30 @@ def test_graph_replay_matches_direct_launches(stack):
         assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32))
 
 
+def test_small_batch_early_recurrence_start_changes_no_bit(stack):
+    # at one window the recurrence is launched as a programmatic dependent of
+    # the projection (its set-up overlaps the projection); with phase timing
+    # on an event sits between them and it starts after: the same bits, with
+    # and without graph replay
+    import torch
+    x = cuda(synthetic.stack_input(synthetic.WORKLOADS["b1_t589"]))
+    outs = []
+    try:
+        for timing, graphs in ((True, False), (False, False), (False, True), (False, True)):
+            binding.lstm_stack_enable_phase_timing(stack.handle, timing)
+            binding.lstm_stack_set_graphs(stack.handle, graphs)
+            y = torch.full((1, 589, 256), float("nan"), device="cuda")
+            stack(x, y)
+            torch.cuda.synchronize()
+            outs.append(y.cpu().numpy())
+    finally:
+        binding.lstm_stack_enable_phase_timing(stack.handle, False)
+        binding.lstm_stack_set_graphs(stack.handle, True)
+    for o in outs[1:]:
+        assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32))
+    assert binding.lstm_fault_status() == 0
+
+
 def test_forward_inside_a_caller_graph_capture(stack, layers):
     # the forward is capturable: a caller's CUDA graph records its launches
     import torch
