@@ -700,7 +700,12 @@ int forward_replay(lstm_stack *s, const float *x, float *y, int batch, int steps
         hit = victim;
     }
     hit->used = ++s->uses;
-    return cuda_status(cudaGraphLaunch(hit->exec, stream), "graph launch");
+    if ((st = cuda_status(cudaGraphLaunch(hit->exec, stream), "graph launch")))
+        return st;
+    // a graph captured with phase timing records the phase events on replay
+    if (s->timing)
+        s->timed_once = true;
+    return LSTM_OK;
 }
 
 }  // namespace

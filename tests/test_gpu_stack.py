@@ -172,6 +172,37 @@ def test_small_batch_early_recurrence_start_changes_no_bit(stack):
     assert binding.lstm_fault_status() == 0
 
 
+@pytest.mark.parametrize("timing", [False, True])
+@pytest.mark.parametrize("graphs", [False, True])
+@pytest.mark.parametrize("math", ["3xtf32", "tf32"])
+@pytest.mark.parametrize("fused", [0, 1])
+def test_setting_combinations(stack, layers, timing, graphs, math, fused):
+    # every combination of phase timing, graph replay, projection math and
+    # the fused small-batch mode runs and stays within the stack's tolerance
+    # of the exact float64 stack (the TF32 mode's own error is ~3e-5)
+    import torch
+    x = synthetic.stack_input(synthetic.WORKLOADS["b1_t64"])
+    h = stack.handle
+    try:
+        binding.lstm_stack_enable_phase_timing(h, timing)
+        binding.lstm_stack_set_graphs(h, graphs)
+        binding.lstm_stack_set_math(h, binding.LSTM_MATH_TF32 if math == "tf32"
+                                    else binding.LSTM_MATH_3XTF32)
+        binding.lstm_stack_set_fused_batches(h, fused)
+        y = stack(cuda(x))
+        torch.cuda.synchronize()
+        if timing:
+            assert np.all(binding.lstm_stack_phase_times(h) >= 0)
+    finally:
+        binding.lstm_stack_enable_phase_timing(h, False)
+        binding.lstm_stack_set_graphs(h, True)
+        binding.lstm_stack_set_math(h, binding.LSTM_MATH_3XTF32)
+        binding.lstm_stack_set_fused_batches(h, 0)
+    what = f"timing {timing} graphs {graphs} math {math} fused {fused}"
+    assert_within(y.cpu().numpy(), oracle.lstm_stack(x, layers), what=what)
+    assert binding.lstm_fault_status() == 0
+
+
 def test_forward_inside_a_caller_graph_capture(stack, layers):
     # the forward is capturable: a caller's CUDA graph records its launches
     import torch
