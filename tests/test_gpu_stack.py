@@ -193,6 +193,10 @@ def test_setting_combinations(stack, layers, timing, graphs, math, fused):
         torch.cuda.synchronize()
         if timing:
             assert np.all(binding.lstm_stack_phase_times(h) >= 0)
+        # the host-memory entry point runs the same kernels: the same bits
+        yh = np.empty((1, 64, 256), np.float32)
+        binding.lstm_stack_forward_host(h, np.ascontiguousarray(x), yh, 1, 64)
+        assert np.array_equal(yh.view(np.uint32), y.cpu().numpy().view(np.uint32))
     finally:
         binding.lstm_stack_enable_phase_timing(h, False)
         binding.lstm_stack_set_graphs(h, True)
