@@ -1061,14 +1061,14 @@ done:
 // which unit and gate row a register slot holds, since every slot reads the
 // same h), so each unit's z is the sum of the same eight chunk partials in the
 // same order as in every other variant: results are bitwise identical.
-template <bool FLOOR = false>
-__global__ void __launch_bounds__(64, 1)
+template <bool FLOOR = false, int C = 8>
+__global__ void __launch_bounds__(512 / C, 1)
 recurrence_u2_kernel(const float *__restrict__ g, const float *__restrict__ rp_in,
                      const float *__restrict__ bias_in, float *__restrict__ y, int batch, int steps,
                      int dir_in, unsigned *fault, unsigned long long wait_limit_ns, int withhold)
 {
-    constexpr int C = 8;
-    constexpr int THREADS = 64;
+    static_assert(C == 4 || C == 8, "cluster");
+    constexpr int THREADS = 512 / C;  // the CTA's 128 / C units, two per lane group
     constexpr int GD = 64;  // projection-value ring depth (steps)
 
     __shared__ __align__(16) float hbuf[2][HROW];
@@ -1088,7 +1088,7 @@ recurrence_u2_kernel(const float *__restrict__ g, const float *__restrict__ rp_i
     const int win = dir_in >= 0 ? cid : (cid >> 1);
     const float *__restrict__ rp = rp_in + (dir_in >= 0 ? 0 : direction * kGates * kHidden);
     const float *__restrict__ bias = bias_in + (dir_in >= 0 ? 0 : direction * kGates);
-    const int base = static_cast<int>(rank) * 16 + (tid >> 5) * 8;  // the warp's 8 units
+    const int base = static_cast<int>(rank) * (kHidden / C) + (tid >> 5) * 8;  // the warp's 8 units
     volatile int *abort_v = &abort_flag;
 
     // R slices of the group's two units for chunk kc, scaled by k_q; slot
@@ -1957,6 +1957,9 @@ const Variant kVariants[] = {
     // two units per 8-lane group, one window per cluster of 64-thread CTAs
     Variant{8, 1, 1, 1, 64, reinterpret_cast<const void *>(&recurrence_u2_kernel<false>),
             reinterpret_cast<const void *>(&recurrence_u2_kernel<true>)},
+    // the same in clusters of 4 CTAs of 128 threads
+    Variant{4, 1, 1, 1, 128, reinterpret_cast<const void *>(&recurrence_u2_kernel<false, 4>),
+            reinterpret_cast<const void *>(&recurrence_u2_kernel<true, 4>)},
     // two units per 8-lane group, several windows per lane
     variant_u2w<8, 4, 1>(), variant_u2w<8, 4, 2>(), variant_u2w<4, 4, 1>(),
     variant_u2w<4, 4, 2>(), variant_u2w<8, 8, 1>(), variant_u2w<4, 8, 1>(),
@@ -1991,8 +1994,8 @@ int max_active_clusters(const Variant &v, int *out);
 // last plateau runs as repeated waves of it.  On another SM count the tile
 // counts scale with it.  Chosen this way, the step is within 1.5 % of the
 // fastest candidate's at every batch from 1 to 320 windows (measured: 1-7
-// windows one unit per group, 8-37 two units, 38-74 two units and two
-// windows per lane, 75-100 4 windows per group, then two units and 4 windows
+// windows one unit per group, 8-37 two units in clusters of 4, 38-74 two
+// units and two windows per lane, 75-100 4 windows per group, then two units and 4 windows
 // per lane, in two chunks from 221 to 264).
 // Ties go to the earlier candidate.
 const Variant *choose_variant(int batch)
@@ -2009,8 +2012,9 @@ const Variant *choose_variant(int batch)
         // narrow clusters of 8, 128 threads, one window per cluster
         {8, 1, 1, 128, 6, {{4, .344f}, {7, .356f}, {11, .403f}, {18, .417f}, {25, .462f},
                            {37, .535f}}},
-        // narrow clusters of 8, 64 threads, two units per lane group
-        {8, 1, 1, 64, 5, {{4, .365f}, {18, .389f}, {26, .445f}, {37, .469f}, {72, .934f}}},
+        // clusters of 4, 128 threads, two units per lane group (of 8 CTAs of 64
+        // threads: 0.389 / 0.462 us at 8 / 32 windows against 0.365 / 0.446)
+        {4, 1, 1, 128, 4, {{8, .365f}, {18, .376f}, {37, .448f}, {48, .874f}}},
         // clusters of 4, 128 threads, two units per group, 2 windows per lane
         {4, 2, 1, 128, 5, {{18, .522f}, {37, .654f}, {64, 1.253f}, {74, 1.30f}, {88, 1.87f}}},
         // clusters of 4, 128 threads, two units per group, 4 windows per lane

@@ -17,7 +17,7 @@ VARIANTS = [(16, 1, 1, 0), (16, 2, 1, 0), (16, 4, 1, 0), (16, 8, 1, 0), (8, 1, 1
             (4, 4, 1, 0), (4, 4, 2, 0), (4, 4, 4, 0), (4, 8, 1, 0), (4, 8, 2, 0),
             (8, 4, 1, 128), (8, 8, 1, 128), (8, 1, 1, 64), (8, 4, 1, 64), (8, 4, 2, 64),
             (4, 4, 1, 128), (4, 4, 2, 128), (8, 8, 1, 64), (4, 8, 1, 128), (8, 8, 2, 64),
-            (8, 2, 1, 64), (8, 2, 2, 64), (4, 2, 1, 128), (4, 2, 2, 128)]
+            (8, 2, 1, 64), (8, 2, 2, 64), (4, 2, 1, 128), (4, 2, 2, 128), (4, 1, 1, 128)]
 # two hidden units per 8-lane group: (cluster, threads) of these variants
 TWO_UNIT = {(8, 64), (4, 128)}
 
@@ -76,8 +76,8 @@ def test_every_variant_matches_oracle(variant):
 
 @pytest.mark.parametrize("steps", [3, 4, 5, 6, 7, 8, 9, 10, 11])
 @pytest.mark.parametrize("variant", [(8, 1, 1, 128), (4, 2, 4, 0), (4, 4, 4, 0), (4, 8, 2, 0),
-                                     (8, 1, 1, 64), (4, 4, 1, 128), (4, 4, 2, 128),
-                                     (8, 2, 1, 64), (8, 2, 2, 64)])
+                                     (8, 1, 1, 64), (4, 1, 1, 128), (4, 4, 1, 128),
+                                     (4, 4, 2, 128), (8, 2, 1, 64), (8, 2, 2, 64)])
 def test_every_tail_length(variant, steps):
     # the step loop runs groups of 4 steps (2 with four or more chunks per
     # lane) and checks for the sequence end only in the last two groups:
@@ -173,7 +173,7 @@ def test_unknown_variant_is_rejected():
     assert e.value.code == binding.LSTM_E_INVALID
 
 
-@pytest.mark.parametrize("variant,batch", [((8, 1, 1, 128), 7), ((8, 1, 1, 64), 37),
+@pytest.mark.parametrize("variant,batch", [((8, 1, 1, 128), 7), ((4, 1, 1, 128), 37),
                                            ((4, 2, 1, 128), 74), ((4, 4, 1, 128), 148),
                                            ((4, 4, 2, 128), 264), ((8, 4, 1, 128), 100)])
 def test_chosen_variants_run_in_one_wave(variant, batch):
