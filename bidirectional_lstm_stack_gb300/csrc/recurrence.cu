@@ -1285,10 +1285,12 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
     // cells a lane updates per chunk; with two windows a lane holds two of
     // a cell's four gates and completes the cell with its partner lane kc ^ 1
     constexpr int CELLS = HV >= 4 ? HV / 4 : 1;
-    constexpr int NPEER = C / 4;      // peers each holder of an h quad sends to
+    // peers each holder of an h quad sends to (with C = 2 only the first two
+    // of its four holders send)
+    constexpr int NPEER = C >= 4 ? C / 4 : 1;
     constexpr bool CM = NCH > 1;
     constexpr int NBAR = CM ? NCH : 1;
-    static_assert((C == 4 || C == 8) && (NW == 2 || NW == 4 || NW == 8) &&
+    static_assert((C == 2 || C == 4 || C == 8) && (NW == 2 || NW == 4 || NW == 8) &&
                       (NCH == 1 || NCH == 2),
                   "shape");
     // projection values: a ring of GD steps in shared memory, each lane's
@@ -1401,7 +1403,7 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
     uint32_t rdst[CELLS][NPEER][2], rbar[NPEER][2];
 #pragma unroll
     for (int r = 0; r < NPEER; ++r) {
-        const uint32_t peer = static_cast<uint32_t>(grp + 4 * r);
+        const uint32_t peer = static_cast<uint32_t>(min(grp + 4 * r, C - 1));
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
 #pragma unroll
@@ -1562,8 +1564,9 @@ recurrence_u2w_kernel(const float *__restrict__ g, const float *__restrict__ rp_
                         const uint32_t bar_off = static_cast<uint32_t>(CM ? ch * 8 : 0);
 #pragma unroll
                         for (int r = 0; r < NPEER; ++r)
-                            ptx::st_async_v4(rdst[ci][r][par ^ 1] + off, h4[0], h4[1], h4[2],
-                                             h4[3], rbar[r][par ^ 1] + bar_off);
+                            if (C >= 4 || grp < C)
+                                ptx::st_async_v4(rdst[ci][r][par ^ 1] + off, h4[0], h4[1],
+                                                 h4[2], h4[3], rbar[r][par ^ 1] + bar_off);
                     }
                     if (grp == 0)
                         *reinterpret_cast<float4 *>(
@@ -1964,7 +1967,8 @@ const Variant kVariants[] = {
     variant_u2w<8, 4, 1>(), variant_u2w<8, 4, 2>(), variant_u2w<4, 4, 1>(),
     variant_u2w<4, 4, 2>(), variant_u2w<8, 8, 1>(), variant_u2w<4, 8, 1>(),
     variant_u2w<8, 8, 2>(),     variant_u2w<8, 2, 1>(), variant_u2w<8, 2, 2>(),
-    variant_u2w<4, 2, 1>(),     variant_u2w<4, 2, 2>(),
+    variant_u2w<4, 2, 1>(),     variant_u2w<4, 2, 2>(),  variant_u2w<2, 4, 2>(),
+    variant_u2w<2, 4, 1>(),
     // tensor cores: clusters of 4 CTAs of 128 threads, 16 windows per cluster
     Variant{4, 16, 1, TC_N, TC_THREADS,
             reinterpret_cast<const void *>(&recurrence_tc_kernel<false>),
@@ -1995,8 +1999,9 @@ int max_active_clusters(const Variant &v, int *out);
 // counts scale with it.  Chosen this way, the step is within 1.5 % of the
 // fastest candidate's at every batch from 1 to 320 windows (measured: 1-7
 // windows one unit per group, 8-37 two units in clusters of 4, 38-74 two
-// units and two windows per lane, 75-100 4 windows per group, then two units and 4 windows
-// per lane, in two chunks from 221 to 264).
+// units and two windows per lane, 75-100 4 windows per group, 101-152 two
+// units and 4 windows per lane in clusters of 2, then in clusters of 4 (two
+// waves), in two chunks from 221 to 264 and in clusters of 2 from 265 to 304).
 // Ties go to the earlier candidate.
 const Variant *choose_variant(int batch)
 {
@@ -2023,7 +2028,11 @@ const Variant *choose_variant(int batch)
         // narrow clusters of 8, 128 threads, 4 windows per group
         {8, 4, 1, 128, 5, {{4, .626f}, {7, .682f}, {11, .754f}, {18, .81f}, {25, 1.062f}}},
         // clusters of 4, 128 threads, two units per group, 2 chunks of 4 windows
-        {4, 4, 2, 128, 3, {{18, 1.215f}, {33, 1.995f}, {37, 2.36f}}}};
+        {4, 4, 2, 128, 3, {{18, 1.215f}, {33, 1.995f}, {37, 2.36f}}},
+        // clusters of 2, 256 threads (one peer per push), two units per group,
+        // 4 windows per lane, and 2 chunks of 4
+        {2, 4, 1, 256, 2, {{38, 1.081f}, {76, 2.155f}}},
+        {2, 4, 2, 256, 1, {{38, 2.03f}}}};
     constexpr int N = sizeof(cand) / sizeof(cand[0]);
     static std::mutex mu;
     static int fits[64][N];

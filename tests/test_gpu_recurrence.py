@@ -17,9 +17,10 @@ VARIANTS = [(16, 1, 1, 0), (16, 2, 1, 0), (16, 4, 1, 0), (16, 8, 1, 0), (8, 1, 1
             (4, 4, 1, 0), (4, 4, 2, 0), (4, 4, 4, 0), (4, 8, 1, 0), (4, 8, 2, 0),
             (8, 4, 1, 128), (8, 8, 1, 128), (8, 1, 1, 64), (8, 4, 1, 64), (8, 4, 2, 64),
             (4, 4, 1, 128), (4, 4, 2, 128), (8, 8, 1, 64), (4, 8, 1, 128), (8, 8, 2, 64),
-            (8, 2, 1, 64), (8, 2, 2, 64), (4, 2, 1, 128), (4, 2, 2, 128), (4, 1, 1, 128)]
+            (8, 2, 1, 64), (8, 2, 2, 64), (4, 2, 1, 128), (4, 2, 2, 128), (4, 1, 1, 128),
+            (2, 4, 2, 256), (2, 4, 1, 256)]
 # two hidden units per 8-lane group: (cluster, threads) of these variants
-TWO_UNIT = {(8, 64), (4, 128)}
+TWO_UNIT = {(8, 64), (4, 128), (2, 256)}
 
 
 def _layer_inputs(batch, steps, layer_index=0, seed=21, scale=1.0):
@@ -93,7 +94,7 @@ def test_every_tail_length(variant, steps):
 @pytest.mark.parametrize("batch", [1, 4, 5, 9, 17, 23])
 @pytest.mark.parametrize("variant", [(4, 4, 2, 0), (4, 4, 4, 0), (4, 8, 2, 0), (8, 4, 1, 128),
                                      (4, 4, 2, 128), (8, 4, 2, 64), (4, 8, 1, 128),
-                                     (8, 2, 2, 64), (4, 2, 2, 128)])
+                                     (8, 2, 2, 64), (4, 2, 2, 128), (2, 4, 2, 256)])
 def test_partly_and_wholly_empty_chunks(variant, batch):
     # tiles whose last chunks hold no window of the batch (those chunks have
     # no barrier traffic at all in the chunk-major variants)
@@ -175,7 +176,8 @@ def test_unknown_variant_is_rejected():
 
 @pytest.mark.parametrize("variant,batch", [((8, 1, 1, 128), 7), ((4, 1, 1, 128), 37),
                                            ((4, 2, 1, 128), 74), ((4, 4, 1, 128), 148),
-                                           ((4, 4, 2, 128), 264), ((8, 4, 1, 128), 100)])
+                                           ((4, 4, 2, 128), 264), ((8, 4, 1, 128), 100),
+                                           ((2, 4, 1, 256), 152), ((2, 4, 2, 256), 304)])
 def test_chosen_variants_run_in_one_wave(variant, batch):
     # the batch sizes each variant is chosen for fit on the GPU at once, both
     # directions together (more registers or shared memory per CTA would
