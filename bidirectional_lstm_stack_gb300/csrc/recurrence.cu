@@ -44,6 +44,15 @@
 // The arithmetic per (window, unit, gate) is the same for every cluster size
 // and tile width (same K chunks, same pairing, same reduction tree), so all
 // variants give bitwise-identical results.
+//
+// Kernels in this file: recurrence_kernel (one hidden unit per 8-lane group,
+// the design above); recurrence_u2_kernel and recurrence_u2w_kernel (two
+// units per 8-lane group: half the shared-memory loads of h per multiply-add;
+// one, or 2, 4 or 8 windows per lane), bitwise identical to it;
+// recurrence_fused_kernel (the input projection computed beside the
+// recurrence, small batches, opt-in); recurrence_tc_kernel (the products on
+// the tensor cores, slower at this shape, never chosen).  choose_variant
+// picks a variant per batch from measured step times.
 #include <algorithm>
 #include <mutex>
 #include <type_traits>
